@@ -1,0 +1,139 @@
+/*
+ * ssd.h -- C ABI of the SSD selective-state scan library (libssd.so, sm_103a).
+ *
+ * The operation (page "Mamba-2架构与LaCT并行计算技术解析", §1.1, the state
+ * equations, and §1.2, independent heads): for every head h and every token t
+ *
+ *     delta_t = softplus(raw_dt_t + delta_init)
+ *     H_t     = exp(-delta_t) * H_{t-1} + delta_t * x_t B_t^T       (H is P x N, fp32)
+ *     y_t     = H_t C_t
+ *
+ * with H = 0 before the first token of every sequence (the zero-initial-state
+ * note under the same equations).  The library evaluates it in the chunked,
+ * semiseparable way of page "长序列 Mamba 多卡训练算力和显存怎么同时省" §一:
+ * diagonal blocks inside each chunk, a small state passed between chunks.
+ * Packed variable-length input follows the cu_seqlens convention of the same
+ * page, §三: the state restarts at every sequence boundary.
+ *
+ * General rules for every entry point:
+ *  - All tensor arguments are DEVICE pointers on the current CUDA device,
+ *    contiguous, row-major, 16-byte aligned.  The caller owns every buffer;
+ *    the library allocates nothing and keeps no pointer after a call returns.
+ *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy
+ *    default stream).  No call synchronises except ssd_device_status().
+ *  - Host-side argument checks run before any launch; on failure nothing is
+ *    launched and a nonzero ssd_status_t is returned.  Errors that only the
+ *    device can see (a malformed cu_seqlens array) are recorded in a status
+ *    word inside the workspace and read with ssd_device_status().
+ *  - Calls that share a workspace must not overlap on the GPU.
+ *
+ * Layouts (T = batch * seqlen tokens, H heads, P = headdim, N = dstate,
+ * G = ngroups; head h reads B/C group h / (H / G)):
+ *     x, y, dy, dx     [T][H][P]   dtype = problem.dtype
+ *     raw_dt, d_raw_dt [T][H]      float32
+ *     B, C, dB, dC     [T][G][N]   dtype = problem.dtype
+ *     final_state      [nseq or batch][H][P][N] float32
+ *     cu_seqlens       [nseq + 1]  int32, cu[0] = 0, cu[nseq] = T, non-decreasing
+ */
+#ifndef SSD_H_
+#define SSD_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define SSD_API_VERSION 1
+
+typedef enum {
+    SSD_OK = 0,
+    SSD_ERR_INVALID_ARG = 1,   /* null pointer, bad size or inconsistent problem */
+    SSD_ERR_UNSUPPORTED = 2,   /* valid problem outside the supported shape set */
+    SSD_ERR_ALIGNMENT = 3,     /* a pointer is not 16-byte aligned (workspace: 256) */
+    SSD_ERR_WORKSPACE = 4,     /* workspace missing or smaller than ssd_workspace_size() */
+    SSD_ERR_CUDA = 5,          /* a CUDA runtime call failed (launch error) */
+    SSD_ERR_TIMEOUT = 6,       /* a bounded device-side wait gave up (device status) */
+    SSD_ERR_DEVICE = 7         /* device-side check failed, e.g. bad cu_seqlens (device status) */
+} ssd_status_t;
+
+typedef enum { SSD_DTYPE_F32 = 0, SSD_DTYPE_BF16 = 1 } ssd_dtype_t;
+
+typedef struct {
+    int64_t batch;       /* rows of a dense batch; must be 1 when cu_seqlens is used */
+    int64_t seqlen;      /* tokens per row; with cu_seqlens: total packed tokens T */
+    int32_t nheads;      /* H */
+    int32_t headdim;     /* P */
+    int32_t dstate;      /* N */
+    int32_t ngroups;     /* G, divides H (B and C are shared by H / G heads) */
+    int32_t chunk_size;  /* Q, the diagonal-block length; the result does not depend on it */
+    int32_t nseq;        /* 0: dense batch; > 0: number of packed sequences in cu_seqlens */
+    float delta_init;    /* added to raw_dt before softplus (e.g. -4.6) */
+    int32_t dtype;       /* ssd_dtype_t of x, B, C, y, dy, dx, dB, dC */
+} ssd_problem_t;
+
+/* Supported shapes: P in {8,16,32,64,128}; N in {8,16,32,64,128};
+ * chunk_size in {16,32,64,128,256}; T <= 2^31 - 1; G divides H.
+ * bf16 problems with P = 64, N in {64,128}, chunk_size = 64 run on the
+ * tensor-core path; every other supported problem runs on the SIMT path. */
+
+/* Bytes of device workspace that ssd_forward (for_backward = 0) or
+ * ssd_backward (for_backward = 1) needs for `prob`.  Pure host function.
+ * Returns SSD_ERR_INVALID_ARG / SSD_ERR_UNSUPPORTED for a bad problem. */
+ssd_status_t ssd_workspace_size(const ssd_problem_t* prob, int for_backward, size_t* bytes);
+
+/* Forward scan.  Reads x, raw_dt, B, C (and cu_seqlens when prob->nseq > 0,
+ * else it must be NULL); writes y and, when final_state is not NULL, the
+ * state after the last token of every sequence (row) -- the quantity that
+ * crosses from one chunk to the next, page "长序列 Mamba 多卡训练算力和显存
+ * 怎么同时省" §一.  workspace: >= ssd_workspace_size(prob, 0) bytes, 256-byte
+ * aligned, contents ignored on entry. */
+ssd_status_t ssd_forward(const ssd_problem_t* prob, const void* x, const float* raw_dt,
+                         const void* B, const void* C, const int32_t* cu_seqlens, void* y,
+                         float* final_state, void* workspace, size_t workspace_bytes,
+                         void* stream);
+
+/* Backward of ssd_forward for an upstream gradient dy of y (the gradient of
+ * final_state is taken as zero).  Writes dx [T][H][P], d_raw_dt [T][H]
+ * (float32, includes the softplus derivative), dB and dC [T][G][N] (summed
+ * over the heads of each group, fp32 accumulation, one rounding to dtype).
+ * Reverse-mode derivative of the recurrence of page "Mamba-2架构与LaCT并行
+ * 计算技术解析" §1.1; the forward states are recomputed, per the
+ * recompute-from-checkpoints idea of that page's §4.1.  workspace: >=
+ * ssd_workspace_size(prob, 1) bytes, 256-byte aligned. */
+ssd_status_t ssd_backward(const ssd_problem_t* prob, const void* x, const float* raw_dt,
+                          const void* B, const void* C, const int32_t* cu_seqlens,
+                          const void* dy, void* dx, float* d_raw_dt, void* dB, void* dC,
+                          void* workspace, size_t workspace_bytes, void* stream);
+
+/* Synchronises `stream` and returns in *device_status the status word that
+ * the last call using `workspace` left (SSD_OK, SSD_ERR_DEVICE, SSD_ERR_TIMEOUT).
+ * Returns SSD_ERR_CUDA if the synchronisation itself failed. */
+ssd_status_t ssd_device_status(const void* workspace, void* stream, int32_t* device_status);
+
+/* Which kernel path a problem takes: "tensor-core", "simt", or NULL for an
+ * unsupported problem.  Pure host function. */
+const char* ssd_dispatch_path(const ssd_problem_t* prob, int for_backward);
+
+/* Number of kernels the last ssd_forward / ssd_backward call on this host
+ * thread launched (memsets not counted). */
+int ssd_last_launch_count(void);
+
+/* Per-kernel timing.  While enabled, every kernel launch is bracketed by CUDA
+ * events recorded on the launch stream; ssd_profiler_entry() synchronises
+ * them and reports, per kernel name, the launch count and total device time.
+ * Not thread-safe; meant for benchmarks. */
+ssd_status_t ssd_profiler_enable(int on);
+void ssd_profiler_reset(void);
+int ssd_profiler_count(void);
+ssd_status_t ssd_profiler_entry(int index, const char** name, int64_t* launches,
+                                double* total_ms);
+
+const char* ssd_status_string(ssd_status_t status);
+int ssd_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SSD_H_ */

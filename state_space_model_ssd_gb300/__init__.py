@@ -1,0 +1,184 @@
+"""GB300 SSD selective-state scan: a thin Python binding over libssd.so.
+
+Every step of the scan runs in the library's CUDA kernels; this module only
+marshals arguments (shapes, dtypes, device pointers, the current CUDA stream)
+and allocates outputs and workspace with torch.  There is no CPU fallback: a
+missing library or a non-CUDA tensor raises.
+
+    y, final_state = forward(x, raw_dt, B, C, delta_init=-4.6)
+    grads = backward(x, raw_dt, B, C, dy, delta_init=-4.6)
+
+Layouts: x, y, dy, dx ``[batch, L, H, P]``; raw_dt ``[batch, L, H]`` float32;
+B, C ``[batch, L, G, N]``; with ``cu_seqlens`` (int32, ``[nseq + 1]``) the batch
+is 1 and the tokens are packed sequences.
+"""
+
+from __future__ import annotations
+
+import ctypes
+from typing import Optional
+
+from . import _lib
+from ._lib import SSDError, check
+
+__all__ = ["forward", "backward", "workspace_size", "dispatch_path", "make_problem",
+           "last_launch_count", "profiler", "SSDError"]
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _dtype_code(t) -> int:
+    torch = _torch()
+    if t.dtype == torch.float32:
+        return _lib.DTYPE_F32
+    if t.dtype == torch.bfloat16:
+        return _lib.DTYPE_BF16
+    raise TypeError("x/B/C must be float32 or bfloat16, got %s" % t.dtype)
+
+
+def make_problem(x, B, delta_init: float, chunk_size: int = 64, cu_seqlens=None) -> _lib.Problem:
+    if x.dim() != 4 or B.dim() != 4:
+        raise ValueError("x must be [batch, L, H, P] and B [batch, L, G, N]")
+    bsz, L, H, P = x.shape
+    G, N = B.shape[2], B.shape[3]
+    nseq = 0
+    if cu_seqlens is not None:
+        if bsz != 1:
+            raise ValueError("packed sequences need batch == 1")
+        nseq = cu_seqlens.numel() - 1
+    return _lib.Problem(bsz, L, H, P, N, G, int(chunk_size), nseq, float(delta_init),
+                        _dtype_code(x))
+
+
+def _ptr(t) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _check_tensor(t, name, dtype=None, device=None):
+    if not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor" % name)
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    if device is not None and t.device != device:
+        raise ValueError("%s is on %s, expected %s" % (name, t.device, device))
+
+
+def workspace_size(problem: _lib.Problem, for_backward: bool) -> int:
+    n = ctypes.c_size_t(0)
+    check(_lib.lib().ssd_workspace_size(ctypes.byref(problem), int(for_backward),
+                                        ctypes.byref(n)), "ssd_workspace_size")
+    return int(n.value)
+
+
+def dispatch_path(problem: _lib.Problem, for_backward: bool = False) -> Optional[str]:
+    r = _lib.lib().ssd_dispatch_path(ctypes.byref(problem), int(for_backward))
+    return None if r is None else r.decode()
+
+
+def last_launch_count() -> int:
+    return int(_lib.lib().ssd_last_launch_count())
+
+
+def _workspace(nbytes: int, device, workspace=None):
+    torch = _torch()
+    if workspace is not None:
+        if workspace.numel() * workspace.element_size() < nbytes:
+            raise ValueError("workspace too small: need %d bytes" % nbytes)
+        return workspace
+    return torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
+
+
+def _stream(stream):
+    torch = _torch()
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def forward(x, raw_dt, B, C, delta_init: float, chunk_size: int = 64, cu_seqlens=None,
+            final_state: bool = True, out=None, workspace=None, stream=None):
+    """Runs ssd_forward.  Returns ``(y, final_state or None)``."""
+    torch = _torch()
+    dev = x.device
+    _check_tensor(x, "x")
+    _check_tensor(raw_dt, "raw_dt", torch.float32, dev)
+    _check_tensor(B, "B", x.dtype, dev)
+    _check_tensor(C, "C", x.dtype, dev)
+    if cu_seqlens is not None:
+        _check_tensor(cu_seqlens, "cu_seqlens", torch.int32, dev)
+    prob = make_problem(x, B, delta_init, chunk_size, cu_seqlens)
+    nseq = prob.nseq if prob.nseq > 0 else prob.batch
+    y = torch.empty_like(x) if out is None else out
+    fs = None
+    if final_state:
+        fs = torch.empty((nseq, prob.nheads, prob.headdim, prob.dstate), dtype=torch.float32,
+                         device=dev)
+    ws = _workspace(workspace_size(prob, False), dev, workspace)
+    with torch.cuda.device(dev):
+        st = _lib.lib().ssd_forward(ctypes.byref(prob), _ptr(x), _ptr(raw_dt), _ptr(B), _ptr(C),
+                                    _ptr(cu_seqlens), _ptr(y), _ptr(fs), _ptr(ws),
+                                    ws.numel(), _stream(stream))
+    check(st, "ssd_forward")
+    return y, fs
+
+
+def backward(x, raw_dt, B, C, dy, delta_init: float, chunk_size: int = 64, cu_seqlens=None,
+             out=None, workspace=None, stream=None):
+    """Runs ssd_backward.  Returns a dict ``dx, d_raw_dt, dB, dC``."""
+    torch = _torch()
+    dev = x.device
+    _check_tensor(x, "x")
+    _check_tensor(raw_dt, "raw_dt", torch.float32, dev)
+    _check_tensor(B, "B", x.dtype, dev)
+    _check_tensor(C, "C", x.dtype, dev)
+    _check_tensor(dy, "dy", x.dtype, dev)
+    if cu_seqlens is not None:
+        _check_tensor(cu_seqlens, "cu_seqlens", torch.int32, dev)
+    prob = make_problem(x, B, delta_init, chunk_size, cu_seqlens)
+    if out is None:
+        out = {"dx": torch.empty_like(x), "d_raw_dt": torch.empty_like(raw_dt),
+               "dB": torch.empty_like(B), "dC": torch.empty_like(C)}
+    ws = _workspace(workspace_size(prob, True), dev, workspace)
+    with torch.cuda.device(dev):
+        st = _lib.lib().ssd_backward(ctypes.byref(prob), _ptr(x), _ptr(raw_dt), _ptr(B),
+                                     _ptr(C), _ptr(cu_seqlens), _ptr(dy), _ptr(out["dx"]),
+                                     _ptr(out["d_raw_dt"]), _ptr(out["dB"]), _ptr(out["dC"]),
+                                     _ptr(ws), ws.numel(), _stream(stream))
+    check(st, "ssd_backward")
+    return out
+
+
+def device_status(workspace, stream=None) -> int:
+    v = ctypes.c_int32(0)
+    check(_lib.lib().ssd_device_status(_ptr(workspace), _stream(stream), ctypes.byref(v)),
+          "ssd_device_status")
+    return int(v.value)
+
+
+class profiler:
+    """Per-kernel device time from events the library records around each launch."""
+
+    @staticmethod
+    def enable(on: bool = True) -> None:
+        _lib.lib().ssd_profiler_enable(int(on))
+
+    @staticmethod
+    def reset() -> None:
+        _lib.lib().ssd_profiler_reset()
+
+    @staticmethod
+    def read() -> dict:
+        l = _lib.lib()
+        out = {}
+        for i in range(l.ssd_profiler_count()):
+            name = ctypes.c_char_p()
+            n = ctypes.c_int64()
+            ms = ctypes.c_double()
+            check(l.ssd_profiler_entry(i, ctypes.byref(name), ctypes.byref(n), ctypes.byref(ms)),
+                  "ssd_profiler_entry")
+            out[name.value.decode()] = (int(n.value), float(ms.value))
+        return out

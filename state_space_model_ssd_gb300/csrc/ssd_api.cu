@@ -1,0 +1,368 @@
+// C ABI of the SSD scan library: argument checks, workspace layout, path
+// dispatch and launch bookkeeping.  No kernel arithmetic lives here.
+#include <math.h>
+#include <string.h>
+
+#include <string>
+#include <vector>
+
+#include "ssd_internal.cuh"
+
+namespace ssd {
+
+namespace {
+
+thread_local int g_last_launches = 0;
+
+// ---- profiler: events bracketing every launch while enabled
+struct ProfRecord {
+    std::string name;
+    cudaEvent_t start, stop;
+};
+struct ProfTotal {
+    std::string name;
+    long long launches;
+    double ms;
+};
+bool g_prof_on = false;
+std::vector<ProfRecord> g_prof_pending;
+std::vector<ProfTotal> g_prof_totals;
+std::vector<cudaEvent_t> g_event_pool;
+const char* g_prof_name = nullptr;
+cudaEvent_t g_prof_start = nullptr;
+
+cudaEvent_t take_event() {
+    if (!g_event_pool.empty()) {
+        cudaEvent_t e = g_event_pool.back();
+        g_event_pool.pop_back();
+        return e;
+    }
+    cudaEvent_t e = nullptr;
+    if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+    return e;
+}
+
+void prof_flush() {
+    for (auto& r : g_prof_pending) {
+        float ms = 0.f;
+        cudaEventSynchronize(r.stop);
+        cudaEventElapsedTime(&ms, r.start, r.stop);
+        bool found = false;
+        for (auto& t : g_prof_totals)
+            if (t.name == r.name) {
+                t.launches += 1;
+                t.ms += ms;
+                found = true;
+                break;
+            }
+        if (!found) g_prof_totals.push_back({r.name, 1, (double)ms});
+        g_event_pool.push_back(r.start);
+        g_event_pool.push_back(r.stop);
+    }
+    g_prof_pending.clear();
+}
+
+constexpr size_t kAlign = 256;
+size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
+
+bool is_pow2_in(int v, int lo, int hi) {
+    if (v < lo || v > hi) return false;
+    return (v & (v - 1)) == 0;
+}
+
+// Segment length: whole chunks, and enough (segment, head) work units to
+// fill the GPU several times over; at most 16 chunks so that the states kept
+// between segments stay small next to the activations.
+int choose_segment_length(long long T, int nseq, int H, int Q) {
+    const long long target_units = 8LL * 152;
+    const long long chunks = (T + Q - 1) / Q;
+    int k = 16;
+    while (k > 1 && (chunks / k + (nseq > 1 ? nseq : 0)) * H < target_units) k >>= 1;
+    return k * Q;
+}
+
+ssd_status_t make_prob(const ssd_problem_t* p, Prob* out) {
+    if (!p || !out) return SSD_ERR_INVALID_ARG;
+    if (p->batch < 1 || p->seqlen < 0 || p->nheads < 1 || p->ngroups < 1 || p->nseq < 0)
+        return SSD_ERR_INVALID_ARG;
+    if (p->nheads % p->ngroups != 0) return SSD_ERR_INVALID_ARG;
+    if (!isfinite(p->delta_init)) return SSD_ERR_INVALID_ARG;
+    if (p->dtype != SSD_DTYPE_F32 && p->dtype != SSD_DTYPE_BF16) return SSD_ERR_INVALID_ARG;
+    if (p->headdim < 1 || p->dstate < 1 || p->chunk_size < 1) return SSD_ERR_INVALID_ARG;
+    if (p->nseq > 0 && p->batch != 1) return SSD_ERR_INVALID_ARG;
+    if (!is_pow2_in(p->headdim, 8, 128) || !is_pow2_in(p->dstate, 8, 128) ||
+        !is_pow2_in(p->chunk_size, 16, 256))
+        return SSD_ERR_UNSUPPORTED;
+    const long long T = p->batch * p->seqlen;
+    if (p->seqlen > 0x7fffffffLL || T > 0x7fffffffLL) return SSD_ERR_UNSUPPORTED;
+    Prob& b = *out;
+    b.T = T;
+    b.varlen = p->nseq > 0;
+    b.nseq = b.varlen ? p->nseq : (int)p->batch;
+    b.rowlen = b.varlen ? 0 : p->seqlen;
+    b.H = p->nheads;
+    b.P = p->headdim;
+    b.N = p->dstate;
+    b.G = p->ngroups;
+    b.Q = p->chunk_size;
+    b.delta_init = p->delta_init;
+    b.dtype = p->dtype;
+    b.tc = tc_supported(p->dtype, p->headdim, p->dstate, p->chunk_size);
+    b.Ls = choose_segment_length(T, b.nseq, b.H, b.Q);
+    b.nseg_max = (T + b.Ls - 1) / b.Ls + (b.varlen ? b.nseq : 0);
+    if (b.nseg_max < 1) b.nseg_max = 1;
+    if (b.nseg_max > 0x7fffffffLL) return SSD_ERR_UNSUPPORTED;
+    return SSD_OK;
+}
+
+Layout make_layout(const Prob& b, bool bwd) {
+    Layout l;
+    size_t off = 0;
+    const size_t PN = (size_t)b.P * b.N;
+    l.header = off;
+    off = align_up(off + sizeof(WsHeader));
+    l.segtab = off;
+    off = align_up(off + sizeof(SegInfo) * (size_t)b.nseg_max);
+    l.A = off;
+    off = align_up(off + sizeof(float) * (size_t)b.nseg_max * b.H * PN);
+    l.lam = off;
+    off = align_up(off + sizeof(float) * (size_t)b.nseg_max * b.H);
+    l.adj = l.rq = l.rqsuf = l.dbacc = l.dcacc = 0;
+    if (bwd) {
+        l.adj = off;
+        off = align_up(off + sizeof(float) * (size_t)b.nseg_max * b.H * PN);
+        l.rq = off;
+        off = align_up(off + sizeof(float) * (size_t)b.nseg_max * b.H);
+        l.rqsuf = off;
+        off = align_up(off + sizeof(float) * (size_t)b.nseg_max * b.H);
+        l.dbacc = off;
+        off = align_up(off + sizeof(float) * (size_t)b.T * b.G * b.N);
+        l.dcacc = off;
+        off = align_up(off + sizeof(float) * (size_t)b.T * b.G * b.N);
+    }
+    l.total = off;
+    return l;
+}
+
+bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+Args make_args(const Prob& b, const Layout& l, void* ws) {
+    Args a;
+    memset(&a, 0, sizeof(a));
+    char* base = static_cast<char*>(ws);
+    a.hdr = reinterpret_cast<WsHeader*>(base + l.header);
+    a.segtab = reinterpret_cast<SegInfo*>(base + l.segtab);
+    a.A = reinterpret_cast<float*>(base + l.A);
+    a.lam = reinterpret_cast<float*>(base + l.lam);
+    if (l.adj) {
+        a.adj = reinterpret_cast<float*>(base + l.adj);
+        a.rq = reinterpret_cast<float*>(base + l.rq);
+        a.rqsuf = reinterpret_cast<float*>(base + l.rqsuf);
+        a.dbacc = reinterpret_cast<float*>(base + l.dbacc);
+        a.dcacc = reinterpret_cast<float*>(base + l.dcacc);
+    }
+    a.T = b.T;
+    a.rowlen = b.rowlen;
+    a.nseg_max = b.nseg_max;
+    a.nseq = b.nseq;
+    a.H = b.H;
+    a.P = b.P;
+    a.N = b.N;
+    a.G = b.G;
+    a.Q = b.Q;
+    a.Ls = b.Ls;
+    a.delta_init = b.delta_init;
+    return a;
+}
+
+ssd_status_t check_common(const ssd_problem_t* prob, const int32_t* cu, void* ws,
+                          size_t ws_bytes, bool bwd, Prob* b, Layout* l) {
+    ssd_status_t st = make_prob(prob, b);
+    if (st != SSD_OK) return st;
+    if ((prob->nseq > 0) != (cu != nullptr)) return SSD_ERR_INVALID_ARG;
+    if (cu && ((uintptr_t)cu & 3u)) return SSD_ERR_ALIGNMENT;
+    *l = make_layout(*b, bwd);
+    if (!ws) return SSD_ERR_WORKSPACE;
+    if ((uintptr_t)ws % kAlign) return SSD_ERR_ALIGNMENT;
+    if (ws_bytes < l->total) return SSD_ERR_WORKSPACE;
+    return SSD_OK;
+}
+
+}  // namespace
+
+void Launch::begin(const char* name) {
+    ++count;
+    if (g_prof_on) {
+        g_prof_name = name;
+        g_prof_start = take_event();
+        if (g_prof_start) cudaEventRecord(g_prof_start, stream);
+    }
+}
+
+cudaError_t Launch::end() {
+    cudaError_t e = cudaGetLastError();
+    if (g_prof_on && g_prof_start) {
+        cudaEvent_t stop = take_event();
+        if (stop) {
+            cudaEventRecord(stop, stream);
+            g_prof_pending.push_back({std::string(g_prof_name), g_prof_start, stop});
+        }
+        g_prof_start = nullptr;
+    }
+    return e;
+}
+
+}  // namespace ssd
+
+using namespace ssd;
+
+extern "C" {
+
+int ssd_version(void) { return SSD_API_VERSION; }
+
+const char* ssd_status_string(ssd_status_t s) {
+    switch (s) {
+        case SSD_OK: return "ok";
+        case SSD_ERR_INVALID_ARG: return "invalid argument";
+        case SSD_ERR_UNSUPPORTED: return "unsupported problem shape";
+        case SSD_ERR_ALIGNMENT: return "misaligned pointer";
+        case SSD_ERR_WORKSPACE: return "workspace missing or too small";
+        case SSD_ERR_CUDA: return "CUDA runtime error";
+        case SSD_ERR_TIMEOUT: return "device-side wait timed out";
+        case SSD_ERR_DEVICE: return "device-side check failed";
+    }
+    return "unknown status";
+}
+
+ssd_status_t ssd_workspace_size(const ssd_problem_t* prob, int for_backward, size_t* bytes) {
+    if (!bytes) return SSD_ERR_INVALID_ARG;
+    Prob b;
+    ssd_status_t st = make_prob(prob, &b);
+    if (st != SSD_OK) return st;
+    *bytes = make_layout(b, for_backward != 0).total;
+    return SSD_OK;
+}
+
+const char* ssd_dispatch_path(const ssd_problem_t* prob, int for_backward) {
+    (void)for_backward;
+    Prob b;
+    if (make_prob(prob, &b) != SSD_OK) return nullptr;
+    return b.tc ? "tensor-core" : "simt";
+}
+
+int ssd_last_launch_count(void) { return g_last_launches; }
+
+ssd_status_t ssd_forward(const ssd_problem_t* prob, const void* x, const float* raw_dt,
+                         const void* B, const void* C, const int32_t* cu_seqlens, void* y,
+                         float* final_state, void* workspace, size_t workspace_bytes,
+                         void* stream) {
+    g_last_launches = 0;
+    Prob b;
+    Layout l;
+    ssd_status_t st = check_common(prob, cu_seqlens, workspace, workspace_bytes, false, &b, &l);
+    if (st != SSD_OK) return st;
+    if (!x || !raw_dt || !B || !C || !y) return SSD_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(raw_dt) || !aligned16(B) || !aligned16(C) || !aligned16(y) ||
+        (final_state && !aligned16(final_state)))
+        return SSD_ERR_ALIGNMENT;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    Args a = make_args(b, l, workspace);
+    a.x = x;
+    a.raw = raw_dt;
+    a.B = B;
+    a.C = C;
+    a.cu = cu_seqlens;
+    a.y = y;
+    a.final_state = final_state;
+    if (cudaMemsetAsync(a.hdr, 0, sizeof(WsHeader), s) != cudaSuccess) return SSD_ERR_CUDA;
+    if (final_state &&
+        cudaMemsetAsync(final_state, 0, sizeof(float) * (size_t)b.nseq * b.H * b.P * b.N, s) !=
+            cudaSuccess)
+        return SSD_ERR_CUDA;
+    if (b.T == 0) return SSD_OK;
+    Launch L;
+    L.stream = s;
+    cudaError_t e = b.tc ? tc_forward(b, a, L) : simt_forward(b, a, L);
+    g_last_launches = L.count;
+    return e == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
+}
+
+ssd_status_t ssd_backward(const ssd_problem_t* prob, const void* x, const float* raw_dt,
+                          const void* B, const void* C, const int32_t* cu_seqlens,
+                          const void* dy, void* dx, float* d_raw_dt, void* dB, void* dC,
+                          void* workspace, size_t workspace_bytes, void* stream) {
+    g_last_launches = 0;
+    Prob b;
+    Layout l;
+    ssd_status_t st = check_common(prob, cu_seqlens, workspace, workspace_bytes, true, &b, &l);
+    if (st != SSD_OK) return st;
+    if (!x || !raw_dt || !B || !C || !dy || !dx || !d_raw_dt || !dB || !dC)
+        return SSD_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(raw_dt) || !aligned16(B) || !aligned16(C) ||
+        !aligned16(dy) || !aligned16(dx) || !aligned16(d_raw_dt) || !aligned16(dB) ||
+        !aligned16(dC))
+        return SSD_ERR_ALIGNMENT;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    Args a = make_args(b, l, workspace);
+    a.x = x;
+    a.raw = raw_dt;
+    a.B = B;
+    a.C = C;
+    a.cu = cu_seqlens;
+    a.dy = dy;
+    a.dx = dx;
+    a.draw = d_raw_dt;
+    a.dB = dB;
+    a.dC = dC;
+    if (cudaMemsetAsync(a.hdr, 0, sizeof(WsHeader), s) != cudaSuccess) return SSD_ERR_CUDA;
+    if (b.T == 0) return SSD_OK;
+    const size_t nbc = sizeof(float) * (size_t)b.T * b.G * b.N;
+    if (cudaMemsetAsync(a.dbacc, 0, nbc, s) != cudaSuccess ||
+        cudaMemsetAsync(a.dcacc, 0, nbc, s) != cudaSuccess)
+        return SSD_ERR_CUDA;
+    Launch L;
+    L.stream = s;
+    cudaError_t e = b.tc ? tc_backward(b, a, L) : simt_backward(b, a, L);
+    g_last_launches = L.count;
+    return e == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
+}
+
+ssd_status_t ssd_device_status(const void* workspace, void* stream, int32_t* device_status) {
+    if (!workspace || !device_status) return SSD_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int v = 0;
+    if (cudaMemcpyAsync(&v, workspace, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return SSD_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return SSD_ERR_CUDA;
+    *device_status = v;
+    return SSD_OK;
+}
+
+ssd_status_t ssd_profiler_enable(int on) {
+    if (!on && g_prof_on) prof_flush();
+    g_prof_on = on != 0;
+    return SSD_OK;
+}
+
+void ssd_profiler_reset(void) {
+    prof_flush();
+    g_prof_totals.clear();
+}
+
+int ssd_profiler_count(void) {
+    prof_flush();
+    return (int)g_prof_totals.size();
+}
+
+ssd_status_t ssd_profiler_entry(int index, const char** name, int64_t* launches,
+                                double* total_ms) {
+    prof_flush();
+    if (index < 0 || index >= (int)g_prof_totals.size()) return SSD_ERR_INVALID_ARG;
+    const ProfTotal& t = g_prof_totals[index];
+    if (name) *name = t.name.c_str();
+    if (launches) *launches = t.launches;
+    if (total_ms) *total_ms = t.ms;
+    return SSD_OK;
+}
+
+}  // extern "C"

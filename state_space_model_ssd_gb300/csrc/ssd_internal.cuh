@@ -1,0 +1,104 @@
+// Internal declarations shared by the C-ABI layer and the kernel files.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "ssd.h"
+
+namespace ssd {
+
+// One entry per segment: a run of whole chunks of one sequence.  Segments
+// never straddle a sequence boundary, so the state only restarts at a
+// segment's first token.
+struct SegInfo {
+    long long start;   // first token (packed index)
+    int len;           // tokens in the segment (<= segment length)
+    int seq;           // sequence (or dense row) index
+    int flags;         // SEG_FIRST | SEG_LAST
+    int pad[3];
+};
+static_assert(sizeof(SegInfo) == 32, "SegInfo layout");
+enum { SEG_FIRST = 1, SEG_LAST = 2 };
+
+// Header at the start of the workspace.
+struct WsHeader {
+    int status;   // first device-side error code (0 = none)
+    int nseg;     // segments actually present
+    int pad[62];
+};
+static_assert(sizeof(WsHeader) == 256, "WsHeader layout");
+
+// A validated problem with derived sizes.
+struct Prob {
+    long long T;        // total tokens
+    long long rowlen;   // tokens per dense row (0 for packed input)
+    int nseq;           // sequences (dense rows or packed sequences)
+    bool varlen;
+    int H, P, N, G, Q;
+    float delta_init;
+    int dtype;
+    int Ls;             // segment length in tokens (a multiple of Q)
+    long long nseg_max; // upper bound on the number of segments
+    bool tc;            // tensor-core path
+};
+
+// Byte offsets of the workspace regions.
+struct Layout {
+    size_t header, segtab, A, lam, adj, rq, rqsuf, dbacc, dcacc, total;
+};
+
+// Everything a kernel needs; passed by value.
+struct Args {
+    const void* x;
+    const float* raw;
+    const void* B;
+    const void* C;
+    const int* cu;
+    const void* dy;
+    void* y;
+    float* final_state;
+    void* dx;
+    float* draw;
+    void* dB;
+    void* dC;
+    WsHeader* hdr;
+    SegInfo* segtab;
+    float* A;       // [nseg_max][H][P][N]: segment aggregates, then the state entering each segment
+    float* lam;     // [nseg_max][H]: segment log-decay, sum of -delta
+    float* adj;     // [nseg_max][H][P][N]: adjoint aggregates, then the adjoint leaving each segment
+    float* rq;      // [nseg_max][H]
+    float* rqsuf;   // [nseg_max][H]
+    float* dbacc;   // [T][G][N] fp32
+    float* dcacc;   // [T][G][N] fp32
+    long long T, rowlen;
+    long long nseg_max;
+    int nseq, H, P, N, G, Q, Ls;
+    float delta_init;
+};
+
+// Launch bookkeeping: counts kernels and, when profiling is on, brackets
+// each launch with events on the launch stream.
+struct Launch {
+    cudaStream_t stream;
+    int count = 0;
+    void begin(const char* name);
+    cudaError_t end();
+};
+
+// SIMT path (any supported shape, f32 or bf16).
+cudaError_t simt_forward(const Prob& pb, const Args& a, Launch& L);
+cudaError_t simt_backward(const Prob& pb, const Args& a, Launch& L);
+// Tensor-core path (bf16, P = 64, N in {64, 128}, Q = 64).
+cudaError_t tc_forward(const Prob& pb, const Args& a, Launch& L);
+cudaError_t tc_backward(const Prob& pb, const Args& a, Launch& L);
+bool tc_supported(int dtype, int P, int N, int Q);
+
+// Shared small kernels (segment table, state scans, gradient epilogues).
+cudaError_t launch_seg_table(const Prob& pb, const Args& a, Launch& L);
+cudaError_t launch_state_scan(const Prob& pb, const Args& a, Launch& L, bool write_final);
+cudaError_t launch_adjoint_scan(const Prob& pb, const Args& a, Launch& L);
+cudaError_t launch_bwd_epilogue(const Prob& pb, const Args& a, Launch& L);
+
+}  // namespace ssd

@@ -1,0 +1,265 @@
+// Segment table, the state scans between segments, and the gradient
+// epilogues.  These kernels are shared by the SIMT and tensor-core paths.
+//
+// The scan between segments is the one-GPU form of the state hand-off that
+// page "揭秘MindSpeed-LLM多潜在注意力（MLA）与Mamba上下文并行实现原理" §三.2
+// performs across devices (every part computes a local decay and a local
+// state, then the prefix states are combined): here each segment contributes
+// (decay_j, A_j) and the state entering segment j is
+//     H_in[j] = decay_{j-1} * H_in[j-1] + A_{j-1},   H_in[first of a sequence] = 0,
+// an associative combine (a1, S1) o (a2, S2) = (a1 a2, a2 S1 + S2).
+#include "ssd_device.cuh"
+
+namespace ssd {
+
+namespace {
+
+constexpr int kTableThreads = 1024;
+
+// Builds the segment table from cu_seqlens (or the dense row length): every
+// sequence is cut into segments of Ls tokens from its own start.  Checks the
+// boundaries on the device and records SSD_ERR_DEVICE if they are malformed.
+__global__ void __launch_bounds__(kTableThreads) seg_table_kernel(Args a) {
+    __shared__ int warp_sums[32];
+    __shared__ long long base_s;
+    __shared__ int bad;
+    const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+    if (tid == 0) {
+        base_s = 0;
+        bad = 0;
+        if (a.cu && (a.cu[0] != 0 || (long long)a.cu[a.nseq] != a.T)) bad = 1;
+    }
+    __syncthreads();
+    if (a.cu)
+        for (int s = tid; s < a.nseq; s += blockDim.x)
+            if (a.cu[s + 1] < a.cu[s]) bad = 1;
+    __syncthreads();
+    if (bad) {
+        if (tid == 0) {
+            set_status(a.hdr, SSD_ERR_DEVICE);
+            a.hdr->nseg = 0;
+        }
+        return;
+    }
+    for (int s0 = 0; s0 < a.nseq; s0 += blockDim.x) {
+        const int s = s0 + tid;
+        long long start = 0;
+        int len = 0, cnt = 0;
+        if (s < a.nseq) {
+            start = a.cu ? (long long)a.cu[s] : (long long)s * a.rowlen;
+            len = a.cu ? a.cu[s + 1] - a.cu[s] : (int)a.rowlen;
+            cnt = (len + a.Ls - 1) / a.Ls;
+        }
+        int v = cnt;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int n = __shfl_up_sync(0xffffffffu, v, o);
+            if (lane >= o) v += n;
+        }
+        if (lane == 31) warp_sums[w] = v;
+        __syncthreads();
+        if (w == 0) {
+            int ws = (lane < (int)(blockDim.x >> 5)) ? warp_sums[lane] : 0;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int n = __shfl_up_sync(0xffffffffu, ws, o);
+                if (lane >= o) ws += n;
+            }
+            warp_sums[lane] = ws;
+        }
+        __syncthreads();
+        const int excl = v - cnt + (w > 0 ? warp_sums[w - 1] : 0);
+        const long long base = base_s + excl;
+        for (int k = 0; k < cnt; ++k) {
+            const long long idx = base + k;
+            if (idx < a.nseg_max) {
+                SegInfo e;
+                e.start = start + (long long)k * a.Ls;
+                e.len = min(a.Ls, len - k * a.Ls);
+                e.seq = s;
+                e.flags = (k == 0 ? SEG_FIRST : 0) | (k == cnt - 1 ? SEG_LAST : 0);
+                e.pad[0] = e.pad[1] = e.pad[2] = 0;
+                a.segtab[idx] = e;
+            } else {
+                set_status(a.hdr, SSD_ERR_DEVICE);
+            }
+        }
+        __syncthreads();
+        if (tid == (int)blockDim.x - 1) base_s += excl + cnt;
+        __syncthreads();
+    }
+    if (tid == 0) a.hdr->nseg = (int)(base_s < a.nseg_max ? base_s : a.nseg_max);
+}
+
+constexpr int kScanThreads = 128;
+constexpr int kScanUnroll = 8;
+
+// Forward scan over segments, per head and per state element (4 per thread).
+// On entry a.A holds the segment aggregates; on exit the state entering each
+// segment.  Optionally writes the state after the last segment of every
+// sequence to final_state.
+__global__ void __launch_bounds__(kScanThreads) state_scan_kernel(Args a, int write_final) {
+    const int h = blockIdx.y;
+    const int PN4 = (a.P * a.N) >> 2;
+    const int e4 = blockIdx.x * blockDim.x + threadIdx.x;
+    if (e4 >= PN4) return;
+    const int nseg = a.hdr->nseg;
+    float4* A4 = reinterpret_cast<float4*>(a.A);
+    float4 carry = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s0 = 0; s0 < nseg; s0 += kScanUnroll) {
+        float4 agg[kScanUnroll];
+        float dec[kScanUnroll];
+        int flags[kScanUnroll], seq[kScanUnroll];
+#pragma unroll
+        for (int u = 0; u < kScanUnroll; ++u) {
+            const int s = s0 + u;
+            if (s < nseg) {
+                agg[u] = A4[((long long)s * a.H + h) * PN4 + e4];
+                dec[u] = expf(a.lam[(long long)s * a.H + h]);
+                flags[u] = a.segtab[s].flags;
+                seq[u] = a.segtab[s].seq;
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kScanUnroll; ++u) {
+            const int s = s0 + u;
+            if (s >= nseg) break;
+            if (flags[u] & SEG_FIRST) carry = make_float4(0.f, 0.f, 0.f, 0.f);
+            A4[((long long)s * a.H + h) * PN4 + e4] = carry;
+            carry.x = fmaf(dec[u], carry.x, agg[u].x);
+            carry.y = fmaf(dec[u], carry.y, agg[u].y);
+            carry.z = fmaf(dec[u], carry.z, agg[u].z);
+            carry.w = fmaf(dec[u], carry.w, agg[u].w);
+            if (write_final && (flags[u] & SEG_LAST))
+                reinterpret_cast<float4*>(a.final_state)[((long long)seq[u] * a.H + h) * PN4 + e4] =
+                    carry;
+        }
+    }
+}
+
+// Reverse scan of the adjoint over segments.  On entry a.adj holds, per
+// segment, sum_u exp(Lambda_u - Lambda_before) dy_u C_u^T; on exit the adjoint
+// arriving at the segment's last token from later tokens of its sequence.
+__global__ void __launch_bounds__(kScanThreads) adjoint_scan_kernel(Args a) {
+    const int h = blockIdx.y;
+    const int PN4 = (a.P * a.N) >> 2;
+    const int e4 = blockIdx.x * blockDim.x + threadIdx.x;
+    if (e4 >= PN4) return;
+    const int nseg = a.hdr->nseg;
+    float4* G4 = reinterpret_cast<float4*>(a.adj);
+    float4 carry = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s0 = nseg - 1; s0 >= 0; s0 -= kScanUnroll) {
+        float4 agg[kScanUnroll];
+        float dec[kScanUnroll];
+        int flags[kScanUnroll];
+#pragma unroll
+        for (int u = 0; u < kScanUnroll; ++u) {
+            const int s = s0 - u;
+            if (s >= 0) {
+                agg[u] = G4[((long long)s * a.H + h) * PN4 + e4];
+                dec[u] = expf(a.lam[(long long)s * a.H + h]);
+                flags[u] = a.segtab[s].flags;
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kScanUnroll; ++u) {
+            const int s = s0 - u;
+            if (s < 0) break;
+            if (flags[u] & SEG_LAST) carry = make_float4(0.f, 0.f, 0.f, 0.f);
+            G4[((long long)s * a.H + h) * PN4 + e4] = carry;
+            carry.x = fmaf(dec[u], carry.x, agg[u].x);
+            carry.y = fmaf(dec[u], carry.y, agg[u].y);
+            carry.z = fmaf(dec[u], carry.z, agg[u].z);
+            carry.w = fmaf(dec[u], carry.w, agg[u].w);
+        }
+    }
+}
+
+// Sum of (r - q) over the later segments of the same sequence, per head.
+__global__ void rq_suffix_kernel(Args a) {
+    const int h = blockIdx.x * blockDim.x + threadIdx.x;
+    if (h >= a.H) return;
+    const int nseg = a.hdr->nseg;
+    float suf = 0.f;
+    for (int s = nseg - 1; s >= 0; --s) {
+        if (a.segtab[s].flags & SEG_LAST) suf = 0.f;
+        a.rqsuf[(long long)s * a.H + h] = suf;
+        suf += a.rq[(long long)s * a.H + h];
+    }
+}
+
+// d_raw = (partial - later segments' sum of (r - q)) * sigmoid(raw + delta_init).
+// On entry d_raw holds, per token, x.(G B) minus the in-segment suffix sum.
+__global__ void ddt_finalize_kernel(Args a) {
+    const int seg = blockIdx.x;
+    if (seg >= a.hdr->nseg) return;
+    const SegInfo si = a.segtab[seg];
+    const long long base = si.start * a.H;
+    const int cnt = si.len * a.H;
+    for (int i = threadIdx.x; i < cnt; i += blockDim.x) {
+        const int h = i % a.H;
+        const float z = a.raw[base + i] + a.delta_init;
+        a.draw[base + i] =
+            (a.draw[base + i] - a.rqsuf[(long long)seg * a.H + h]) * sigmoid_f(z);
+    }
+}
+
+template <typename TO>
+__global__ void dbc_convert_kernel(Args a) {
+    const long long n = a.T * a.G * a.N;
+    TO* dB = static_cast<TO*>(a.dB);
+    TO* dC = static_cast<TO*>(a.dC);
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
+         i += (long long)gridDim.x * blockDim.x) {
+        st_out(dB, i, a.dbacc[i]);
+        st_out(dC, i, a.dcacc[i]);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_seg_table(const Prob& pb, const Args& a, Launch& L) {
+    (void)pb;
+    L.begin("seg_table");
+    seg_table_kernel<<<1, kTableThreads, 0, L.stream>>>(a);
+    return L.end();
+}
+
+cudaError_t launch_state_scan(const Prob& pb, const Args& a, Launch& L, bool write_final) {
+    const int PN4 = (pb.P * pb.N) / 4;
+    dim3 grid((PN4 + kScanThreads - 1) / kScanThreads, pb.H);
+    L.begin("state_scan");
+    state_scan_kernel<<<grid, kScanThreads, 0, L.stream>>>(a, write_final ? 1 : 0);
+    return L.end();
+}
+
+cudaError_t launch_adjoint_scan(const Prob& pb, const Args& a, Launch& L) {
+    const int PN4 = (pb.P * pb.N) / 4;
+    dim3 grid((PN4 + kScanThreads - 1) / kScanThreads, pb.H);
+    L.begin("adjoint_scan");
+    adjoint_scan_kernel<<<grid, kScanThreads, 0, L.stream>>>(a);
+    return L.end();
+}
+
+cudaError_t launch_bwd_epilogue(const Prob& pb, const Args& a, Launch& L) {
+    L.begin("rq_suffix");
+    rq_suffix_kernel<<<(pb.H + 127) / 128, 128, 0, L.stream>>>(a);
+    cudaError_t e = L.end();
+    if (e != cudaSuccess) return e;
+    L.begin("ddt_finalize");
+    ddt_finalize_kernel<<<(unsigned)pb.nseg_max, 256, 0, L.stream>>>(a);
+    e = L.end();
+    if (e != cudaSuccess) return e;
+    const long long n = pb.T * pb.G * pb.N;
+    long long blocks = (n + 255) / 256;
+    if (blocks > 152 * 16) blocks = 152 * 16;
+    if (blocks < 1) blocks = 1;
+    L.begin("dbc_convert");
+    if (pb.dtype == SSD_DTYPE_BF16)
+        dbc_convert_kernel<__nv_bfloat16><<<(unsigned)blocks, 256, 0, L.stream>>>(a);
+    else
+        dbc_convert_kernel<float><<<(unsigned)blocks, 256, 0, L.stream>>>(a);
+    return L.end();
+}
+
+}  // namespace ssd
