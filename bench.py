@@ -1,0 +1,414 @@
+"""Benchmark of the SSD scan on GB300: one JSON line on stdout (rank 0).
+
+A step is one pass of the whole hot path on one batch: ssd_forward followed by
+ssd_backward (chunk cumsum, chunk state, state passing, chunk scan and their
+backward) on the mamba-2.8b-layer training workload: batch 1, L = 32768,
+80 heads x P = 64, N = 128, chunk 64, bf16 x/B/C/dy, fp32 raw_dt.  Inputs are
+synthetic and seeded (state_space_model_ssd_gb300.inputs); they are larger
+than L2, so no flush is needed between steps.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+--impl reference times the fp64 CPU oracle on the host cores (a bounded
+sample of the same workload per step).  Under torchrun every rank runs its
+own replica (weak scaling); only the barrier and the max-over-ranks timing
+cross ranks.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from state_space_model_ssd_gb300.inputs import WORKLOADS, make_inputs  # noqa: E402
+
+METRIC = "SSD scan tokens/s (fwd, fwd+bwd) on 1 GB300; % of HBM/tensor roofline"
+DEFAULT_WORKLOAD = "mamba2.8b_32k"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+SM_COUNT = 152
+FP32_LANES_PER_SM = 128
+
+
+def describe(w) -> str:
+    kind = "fwd+bwd" if w.backward else "fwd"
+    return ("%s %s: batch %d, L=%d, %d heads x P=%d, N=%d, chunk %d, %s x/B/C%s, fp32 raw_dt, "
+            "delta_init %.1f" % (w.name, kind, w.batch, w.seqlen, w.nheads, w.headdim, w.dstate,
+                                 w.chunk_size, w.dtype, "/dy" if w.backward else "",
+                                 w.delta_init))
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def algorithmic(w):
+    """Compulsory bytes and the chunked algorithm's flops per step (forward, backward)."""
+    T, H, P, N, G, Q = w.total_tokens, w.nheads, w.headdim, w.dstate, w.ngroups, w.chunk_size
+    e = 2 if w.dtype == "bf16" else 4
+    nseq = w.batch
+    fwd_bytes = 2 * T * H * P * e + 2 * T * G * N * e + T * H * 4 + nseq * H * P * N * 4
+    bwd_bytes = 3 * T * H * P * e + 4 * T * G * N * e + 2 * T * H * 4
+    fwd_flops = T * (H * (4 * P * N + 2 * Q * P) + 2 * Q * N * G)
+    bwd_flops = T * (H * (4 * Q * P + 4 * Q * N + 10 * P * N) + 2 * Q * N * G)
+    return fwd_bytes, bwd_bytes, fwd_flops, bwd_flops
+
+
+def kernel_model(name, w):
+    """(bound, algorithmic amount per launch, unit) for a kernel of the path.
+
+    SIMT kernels are bound by fp32 ALU work: flops counted per state element
+    and token-head (multiply and add counted separately).  Tensor-core and
+    streaming kernels are bound by their compulsory HBM bytes."""
+    T, H, P, N, G = w.total_tokens, w.nheads, w.headdim, w.dstate, w.ngroups
+    e = 2 if w.dtype == "bf16" else 4
+    per_elem = {"simt_seg_state": 3, "simt_seg_walk": 5, "simt_adj_state": 3,
+                "simt_bwd_walk": 12}
+    if name in per_elem:
+        return "alu", float(per_elem[name] * T * H * P * N), "flop"
+    xbytes = T * H * P * e
+    bc = T * G * N * e
+    raw = T * H * 4
+    table = {
+        "tc_fwd_state": xbytes + bc + raw,
+        "tc_fwd_walk": 2 * xbytes + 2 * bc + raw,
+        "tc_bwd_adjoint": xbytes + bc + raw,
+        "tc_bwd_walk": 3 * xbytes + 2 * bc + 2 * raw,
+    }
+    if name in table:
+        return "hbm", float(table[name]), "byte"
+    return None, None, None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.fh, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for nm, v in zip(names, parts[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(nm)
+        os.unlink(self.path)
+        return {"sm_mhz": float(np.median(sm)) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+def oracle_sample(w, d, heads: int, tokens: int, threads: int):
+    """One bounded oracle step: forward + backward on `heads` heads over the
+    first `tokens` tokens of the workload.  Returns (seconds, token-equivalents)."""
+    import oracle
+    sl = lambda a: np.ascontiguousarray(a[:, :tokens, :heads])  # noqa: E731
+    x, raw, dy = sl(d["x"]), sl(d["raw_dt"]), sl(d["dy"]) if "dy" in d else None
+    B = np.ascontiguousarray(d["B"][:, :tokens])
+    C = np.ascontiguousarray(d["C"][:, :tokens])
+    t0 = time.perf_counter()
+    oracle.forward(x, raw, B, C, w.delta_init, threads=threads)
+    if w.backward:
+        oracle.backward(x, raw, B, C, dy, w.delta_init, threads=threads)
+    dt = time.perf_counter() - t0
+    return dt, tokens * w.batch * heads / float(w.nheads)
+
+
+def reference_arm(args, w, rank, world):
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    d = make_inputs(w, seed=0, tokens=min(w.seqlen, 8192))
+    cores = os.cpu_count() or 1
+    heads = min(w.nheads, cores)
+    tokens = min(w.seqlen, 4096)
+    for _ in range(args.warmup):
+        oracle_sample(w, d, heads, tokens, cores)
+    total_t, total_tok = 0.0, 0.0
+    for _ in range(args.steps):
+        dt, tok = oracle_sample(w, d, heads, tokens, cores)
+        total_t += dt
+        total_tok += tok
+    value = total_tok / total_t
+    sample = "%d of %d heads x first %d tokens per step, fwd%s" % (
+        heads, w.nheads, tokens, "+bwd" if w.backward else "")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * total_t / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": describe(w), "sample": sample},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": oracle.max_threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def gpu_arm(args, w, rank, world, dist):
+    import torch
+
+    import state_space_model_ssd_gb300 as ssd
+    from state_space_model_ssd_gb300 import build as ssd_build
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    ssd_build.build()
+    d = make_inputs(w, seed=rank)
+    tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    host = {k: torch.from_numpy(d[k]).to(tdt).pin_memory() for k in ("x", "B", "C")}
+    host["raw_dt"] = torch.from_numpy(d["raw_dt"]).pin_memory()
+    if w.backward:
+        host["dy"] = torch.from_numpy(d["dy"]).to(tdt).pin_memory()
+    dv = {k: v.to(dev) for k, v in host.items()}
+    cu = None
+    if d["cu_seqlens"] is not None:
+        cu = torch.from_numpy(d["cu_seqlens"]).to(dev)
+    prob = ssd.make_problem(dv["x"], dv["B"], w.delta_init, w.chunk_size, cu)
+    path = ssd.dispatch_path(prob)
+    ws = torch.empty(max(ssd.workspace_size(prob, False), ssd.workspace_size(prob, True)),
+                     dtype=torch.uint8, device=dev)
+    y = torch.empty_like(dv["x"])
+    grads = None
+    if w.backward:
+        grads = {"dx": torch.empty_like(dv["x"]), "d_raw_dt": torch.empty_like(dv["raw_dt"]),
+                 "dB": torch.empty_like(dv["B"]), "dC": torch.empty_like(dv["C"])}
+    stream = torch.cuda.current_stream()
+
+    def step(mid=None):
+        _, fs = ssd.forward(dv["x"], dv["raw_dt"], dv["B"], dv["C"], w.delta_init,
+                            w.chunk_size, cu, final_state=True, out=y, workspace=ws)
+        n = ssd.last_launch_count()
+        if mid is not None:
+            mid.record(stream)
+        if w.backward:
+            ssd.backward(dv["x"], dv["raw_dt"], dv["B"], dv["C"], dv["dy"], w.delta_init,
+                         w.chunk_size, cu, out=grads, workspace=ws)
+            n += ssd.last_launch_count()
+        return n
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    for _ in range(args.warmup):
+        step()
+    # ---- timed region: whole steps, device events on the launch stream
+    sampler = ClockSampler(local)
+    sampler.start()
+    ssd.profiler.reset()
+    ssd.profiler.enable(True)
+    barrier()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    launches = 0
+    marks = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+             for _ in range(args.steps)]
+    ev0.record(stream)
+    for i in range(args.steps):
+        marks[i][0].record(stream)
+        launches += step(marks[i][1])
+    ev1.record(stream)
+    barrier()
+    ssd.profiler.enable(False)
+    clocks = sampler.stop()
+    ms = ev0.elapsed_time(ev1) / args.steps
+    ms_fwd = float(np.mean([a.elapsed_time(b) for a, b in marks]))
+    prof = ssd.profiler.read()
+    ms_max = ms
+    if dist is not None:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_max = float(t.item())
+    tokens_per_step = w.total_tokens
+    value = world * tokens_per_step / (ms_max * 1e-3)
+
+    # ---- end to end through the public API: pinned host in, host out
+    out_host = {"y": torch.empty_like(host["x"]).pin_memory()}
+    if w.backward:
+        for k in ("dx", "d_raw_dt", "dB", "dC"):
+            out_host[k] = torch.empty(grads[k].shape, dtype=grads[k].dtype).pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    d2h = sum(v.numel() * v.element_size() for v in out_host.values())
+
+    def e2e_step():
+        for k, v in host.items():
+            dv[k].copy_(v, non_blocking=True)
+        step()
+        out_host["y"].copy_(y, non_blocking=True)
+        if w.backward:
+            for k in ("dx", "d_raw_dt", "dB", "dC"):
+                out_host[k].copy_(grads[k], non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        e2e_step()
+    barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    barrier()
+    e2e_ms = e0.elapsed_time(e1) / args.steps
+    if dist is not None:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+
+    if rank != 0:
+        return
+    peaks, peak_kind = load_peaks()
+    fwd_b, bwd_b, fwd_f, bwd_f = algorithmic(w)
+    kernels = {k: {"launches": n, "total_ms": t, "avg_ms": t / max(n, 1),
+                   "share": t / max(sum(v[1] for v in prof.values()), 1e-12)}
+               for k, (n, t) in prof.items()}
+    dom = max(kernels.items(), key=lambda kv: kv[1]["total_ms"])[0] if kernels else None
+    roof = None
+    if dom is not None:
+        bound, amount, unit = kernel_model(dom, w)
+        avg_s = kernels[dom]["avg_ms"] * 1e-3
+        if bound == "hbm":
+            ach = amount / avg_s / 1e9
+            peak = peaks["hbm_gbs"]
+            roof = {"kernel": dom, "bound": "hbm", "achieved": ach, "peak": peak, "unit": "GB/s",
+                    "frac": ach / peak, "traffic": None,
+                    "peak_source": "%s hbm_gbs (copy)" % peak_kind}
+        elif bound == "alu":
+            clk = (clocks.get("sm_max_mhz") or peaks.get("sm_max_mhz") or 2070.0) * 1e6
+            peak = SM_COUNT * FP32_LANES_PER_SM * 2 * clk / 1e12
+            ach = amount / avg_s / 1e12
+            roof = {"kernel": dom, "bound": "alu", "achieved": ach, "peak": peak,
+                    "unit": "TFLOP/s", "frac": ach / peak, "traffic": None,
+                    "peak_source": "fp32 FMA: 152 SMs x 128 lanes x 2 flops x max SM clock"}
+    step_bytes = fwd_b + (bwd_b if w.backward else 0)
+    step_flops = fwd_f + (bwd_f if w.backward else 0)
+    t_bind = max(step_bytes / (peaks["hbm_gbs"] * 1e9), step_flops / (peaks["bf16_tflops"] * 1e12))
+    # CPU baseline: the oracle as it stands on this host, one bounded sample
+    cpu = None
+    if not args.no_cpu_baseline:
+        import oracle
+        oracle.build()
+        cores = os.cpu_count() or 1
+        heads = min(w.nheads, cores)
+        tokens = min(w.seqlen, 4096)
+        dt, tok = oracle_sample(w, d, heads, tokens, cores)
+        cpu = {"value": tok / dt, "unit": "tokens/s", "cores": oracle.max_threads(),
+               "kind": "oracle",
+               "sample": "%d of %d heads x first %d tokens, fwd%s, %.1f s" % (
+                   heads, w.nheads, tokens, "+bwd" if w.backward else "", dt)}
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if path == "tensor-core" else "f32",
+        "data": "synthetic",
+        "config": {"workload": describe(w), "path": path,
+                   "l2": "inputs larger than L2 (x alone %.0f MB), no flush" % (
+                       dv["x"].numel() * dv["x"].element_size() / 1e6),
+                   "parallelism": "replicas" if world > 1 else "single GPU",
+                   "global_batch": w.batch * world, "seq_len": w.seqlen},
+        "fwd": {"ms": ms_fwd, "tokens_per_s": tokens_per_step / (ms_fwd * 1e-3)
+                if ms_fwd > 0 else None},
+        "path_roofline": {"bytes": step_bytes, "flops": step_flops,
+                          "binding_ms": t_bind * 1e3, "frac": t_bind * 1e3 / ms_max,
+                          "peaks": "%s hbm %.1f GB/s, bf16 %.1f TFLOP/s" % (
+                              peak_kind, peaks["hbm_gbs"], peaks["bf16_tflops"])},
+        "roofline": roof,
+        "kernels": kernels,
+        "cpu_baseline": cpu,
+        "e2e": {"value": world * tokens_per_step / (e2e_ms * 1e-3), "unit": "tokens/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": launches,
+        "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    w = WORKLOADS[args.workload]
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        reference_arm(args, w, rank, world)
+        return
+    dist = None
+    if world > 1:
+        import torch
+        import torch.distributed as tdist
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+        tdist.init_process_group("nccl")
+        dist = tdist
+    try:
+        gpu_arm(args, w, rank, world, dist)
+    finally:
+        if dist is not None:
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,179 @@
+"""GPU parity: the CUDA path against the fp64 oracle on identical seeded inputs.
+
+Bar (per output tensor): max|gpu - oracle| / max|oracle| <= 1e-4 for fp32
+inputs and <= 1e-2 for bf16 inputs (fp32 accumulation), gradients included.
+Sizes here span several chunks and segments and end in a ragged tail; the
+full-size workloads are checked in test_fullsize_gpu.py.
+"""
+
+import numpy as np
+import pytest
+
+from helpers import TOL, rel_err, to_device, to_np
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def ssd():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import state_space_model_ssd_gb300 as m
+    from state_space_model_ssd_gb300 import build
+    build.build()
+    return m
+
+
+def _draw(seed, bsz, L, H, P, N, G=1, dtype="f32", cu=None, raw_shift=0.0):
+    from state_space_model_ssd_gb300.inputs import bf16_round
+    rng = np.random.default_rng(seed)
+    rnd = (lambda a: bf16_round(a)) if dtype == "bf16" else (lambda a: a)
+    d = {
+        "x": rnd(rng.standard_normal((bsz, L, H, P), dtype=np.float32)),
+        "B": rnd(rng.standard_normal((bsz, L, G, N), dtype=np.float32) / np.float32(np.sqrt(N))),
+        "C": rnd(rng.standard_normal((bsz, L, G, N), dtype=np.float32) / np.float32(np.sqrt(N))),
+        "raw_dt": (rng.standard_normal((bsz, L, H), dtype=np.float32) * np.float32(0.5)
+                   + np.float32(raw_shift)),
+        "dy": rnd(rng.standard_normal((bsz, L, H, P), dtype=np.float32)),
+        "cu_seqlens": None if cu is None else np.asarray(cu, dtype=np.int32),
+    }
+    return d
+
+
+def _fwd_check(ssd, oracle, d, dtype, dinit, Q=64, tol=None):
+    tol = TOL[dtype] if tol is None else tol
+    t = to_device(d, dtype)
+    y, fs = ssd.forward(t["x"], t["raw_dt"], t["B"], t["C"], delta_init=dinit, chunk_size=Q,
+                        cu_seqlens=t["cu_seqlens"])
+    yr, fr = oracle.forward(d["x"], d["raw_dt"], d["B"], d["C"], dinit,
+                            cu_seqlens=d["cu_seqlens"])
+    ey, ef = rel_err(to_np(y), yr), rel_err(to_np(fs), fr)
+    assert ey <= tol, "y rel err %g" % ey
+    assert ef <= tol, "final_state rel err %g" % ef
+    return to_np(y), to_np(fs)
+
+
+def _bwd_check(ssd, oracle, d, dtype, dinit, Q=64, tol=None):
+    tol = TOL[dtype] if tol is None else tol
+    t = to_device(d, dtype)
+    g = ssd.backward(t["x"], t["raw_dt"], t["B"], t["C"], t["dy"], delta_init=dinit,
+                     chunk_size=Q, cu_seqlens=t["cu_seqlens"])
+    r = oracle.backward(d["x"], d["raw_dt"], d["B"], d["C"], d["dy"], dinit,
+                        cu_seqlens=d["cu_seqlens"])
+    for k in ("dx", "d_raw_dt", "dB", "dC"):
+        e = rel_err(to_np(g[k]), r[k])
+        assert e <= tol, "%s rel err %g" % (k, e)
+
+
+def test_tiny_f32_workload(ssd, oracle_mod):
+    """The tiny fp32 workload exactly as specified (seeded recipe, seed 0)."""
+    from state_space_model_ssd_gb300.inputs import WORKLOADS, make_inputs
+    w = WORKLOADS["tiny_f32"]
+    d = make_inputs(w, seed=0)
+    _fwd_check(ssd, oracle_mod, d, "f32", w.delta_init)
+
+
+@pytest.mark.parametrize("P,N", [(16, 16), (8, 128), (64, 64), (32, 8), (128, 32)])
+def test_f32_forward_shapes(ssd, oracle_mod, P, N):
+    d = _draw(1, 2, 333, 3, P, N)
+    _fwd_check(ssd, oracle_mod, d, "f32", -4.6)
+
+
+@pytest.mark.parametrize("P,N", [(16, 32), (64, 128)])
+def test_f32_backward(ssd, oracle_mod, P, N):
+    d = _draw(2, 1, 461, 3, P, N, raw_shift=1.0)
+    _bwd_check(ssd, oracle_mod, d, "f32", -3.0)
+
+
+@pytest.mark.parametrize("N", [64, 128])
+def test_bf16_forward_backward(ssd, oracle_mod, N):
+    d = _draw(3, 2, 650, 6, 64, N, dtype="bf16")
+    _fwd_check(ssd, oracle_mod, d, "bf16", -4.6)
+    _bwd_check(ssd, oracle_mod, d, "bf16", -4.6)
+
+
+def test_bf16_larger_delta(ssd, oracle_mod):
+    """delta near 1 per token: strong decay inside every chunk."""
+    d = _draw(4, 1, 517, 4, 64, 128, dtype="bf16", raw_shift=4.0)
+    _fwd_check(ssd, oracle_mod, d, "bf16", -4.0)
+    _bwd_check(ssd, oracle_mod, d, "bf16", -4.0)
+
+
+@pytest.mark.parametrize("dtype,P,N", [("f32", 16, 32), ("bf16", 64, 128)])
+def test_packed_sequences(ssd, oracle_mod, dtype, P, N):
+    lens = [1, 64, 130, 0, 257, 7, 128, 3]
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    d = _draw(5, 1, int(cu[-1]), 3, P, N, dtype=dtype, cu=cu)
+    _fwd_check(ssd, oracle_mod, d, dtype, -4.6)
+    _bwd_check(ssd, oracle_mod, d, dtype, -4.6)
+
+
+def test_groups(ssd, oracle_mod):
+    d = _draw(6, 1, 300, 4, 16, 16, G=2)
+    _fwd_check(ssd, oracle_mod, d, "f32", -2.0)
+    _bwd_check(ssd, oracle_mod, d, "f32", -2.0)
+
+
+def test_chunk_size_invariance(ssd, oracle_mod):
+    """The chunked form is exact: every chunk length gives the oracle's result."""
+    d = _draw(7, 1, 700, 2, 16, 32)
+    ys = []
+    for Q in (16, 32, 64, 128, 256):
+        y, _ = _fwd_check(ssd, oracle_mod, d, "f32", -4.6, Q=Q)
+        ys.append(y)
+    for y in ys[1:]:
+        assert rel_err(y, ys[0]) <= 1e-4
+
+
+def test_single_token_and_exact_chunks(ssd, oracle_mod):
+    for L in (1, 64, 128):
+        d = _draw(8, 1, L, 2, 64, 64, dtype="bf16")
+        _fwd_check(ssd, oracle_mod, d, "bf16", -4.6)
+        _bwd_check(ssd, oracle_mod, d, "bf16", -4.6)
+
+
+def test_empty_input(ssd):
+    import torch
+    x = torch.zeros(1, 0, 2, 16, device="cuda")
+    B = torch.zeros(1, 0, 1, 16, device="cuda")
+    y, fs = ssd.forward(x, torch.zeros(1, 0, 2, device="cuda"), B, B, delta_init=-4.6)
+    assert y.shape == x.shape and torch.all(fs == 0)
+
+
+def test_deterministic_forward(ssd):
+    d = _draw(9, 1, 1000, 4, 64, 128, dtype="bf16")
+    t = to_device(d, "bf16")
+    y1, f1 = ssd.forward(t["x"], t["raw_dt"], t["B"], t["C"], delta_init=-4.6)
+    y2, f2 = ssd.forward(t["x"], t["raw_dt"], t["B"], t["C"], delta_init=-4.6)
+    assert bool((y1 == y2).all()) and bool((f1 == f2).all())
+
+
+def test_bad_cu_seqlens_reports_device_status(ssd):
+    """A non-monotone cu_seqlens is caught on the device; the call returns, no hang."""
+    import torch
+    d = _draw(10, 1, 100, 2, 16, 16, cu=[0, 60, 40, 100])
+    t = to_device(d, "f32")
+    prob = ssd.make_problem(t["x"], t["B"], -4.6, 64, t["cu_seqlens"])
+    ws = torch.empty(ssd.workspace_size(prob, False), dtype=torch.uint8, device="cuda")
+    ssd.forward(t["x"], t["raw_dt"], t["B"], t["C"], delta_init=-4.6,
+                cu_seqlens=t["cu_seqlens"], workspace=ws)
+    assert ssd.device_status(ws) == 7
+    good = torch.tensor([0, 40, 60, 100], dtype=torch.int32, device="cuda")
+    ssd.forward(t["x"], t["raw_dt"], t["B"], t["C"], delta_init=-4.6, cu_seqlens=good,
+                workspace=ws)
+    assert ssd.device_status(ws) == 0
+
+
+def test_launch_count_and_profiler(ssd):
+    d = _draw(11, 1, 500, 2, 64, 128, dtype="bf16")
+    t = to_device(d, "bf16")
+    ssd.profiler.reset()
+    ssd.profiler.enable(True)
+    ssd.forward(t["x"], t["raw_dt"], t["B"], t["C"], delta_init=-4.6)
+    n = ssd.last_launch_count()
+    ssd.profiler.enable(False)
+    prof = ssd.profiler.read()
+    assert n >= 3
+    assert sum(v[0] for v in prof.values()) == n
+    assert all(v[1] > 0 for v in prof.values())
