@@ -109,7 +109,8 @@ ssd_status_t make_prob(const ssd_problem_t* p, Prob* out) {
     b.dtype = p->dtype;
     b.tc = tc_supported(p->dtype, p->headdim, p->dstate, p->chunk_size);
     b.Ls = choose_segment_length(T, b.nseq, b.H, b.Q);
-    b.nseg_max = (T + b.Ls - 1) / b.Ls + (b.varlen ? b.nseq : 0);
+    // every sequence (dense row) may end in a partial segment
+    b.nseg_max = (T + b.Ls - 1) / b.Ls + b.nseq;
     if (b.nseg_max < 1) b.nseg_max = 1;
     if (b.nseg_max > 0x7fffffffLL) return SSD_ERR_UNSUPPORTED;
     return SSD_OK;
@@ -261,11 +262,18 @@ ssd_status_t ssd_forward(const ssd_problem_t* prob, const void* x, const float* 
     Layout l;
     ssd_status_t st = check_common(prob, cu_seqlens, workspace, workspace_bytes, false, &b, &l);
     if (st != SSD_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (b.T == 0) {  // nothing to read: only the (zero) final states are written
+        if (final_state &&
+            cudaMemsetAsync(final_state, 0, sizeof(float) * (size_t)b.nseq * b.H * b.P * b.N,
+                            s) != cudaSuccess)
+            return SSD_ERR_CUDA;
+        return SSD_OK;
+    }
     if (!x || !raw_dt || !B || !C || !y) return SSD_ERR_INVALID_ARG;
     if (!aligned16(x) || !aligned16(raw_dt) || !aligned16(B) || !aligned16(C) || !aligned16(y) ||
         (final_state && !aligned16(final_state)))
         return SSD_ERR_ALIGNMENT;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
     Args a = make_args(b, l, workspace);
     a.x = x;
     a.raw = raw_dt;
@@ -279,7 +287,6 @@ ssd_status_t ssd_forward(const ssd_problem_t* prob, const void* x, const float* 
         cudaMemsetAsync(final_state, 0, sizeof(float) * (size_t)b.nseq * b.H * b.P * b.N, s) !=
             cudaSuccess)
         return SSD_ERR_CUDA;
-    if (b.T == 0) return SSD_OK;
     Launch L;
     L.stream = s;
     cudaError_t e = b.tc ? tc_forward(b, a, L) : simt_forward(b, a, L);
@@ -296,6 +303,7 @@ ssd_status_t ssd_backward(const ssd_problem_t* prob, const void* x, const float*
     Layout l;
     ssd_status_t st = check_common(prob, cu_seqlens, workspace, workspace_bytes, true, &b, &l);
     if (st != SSD_OK) return st;
+    if (b.T == 0) return SSD_OK;  // no tokens: every gradient is empty
     if (!x || !raw_dt || !B || !C || !dy || !dx || !d_raw_dt || !dB || !dC)
         return SSD_ERR_INVALID_ARG;
     if (!aligned16(x) || !aligned16(raw_dt) || !aligned16(B) || !aligned16(C) ||
@@ -315,7 +323,6 @@ ssd_status_t ssd_backward(const ssd_problem_t* prob, const void* x, const float*
     a.dB = dB;
     a.dC = dC;
     if (cudaMemsetAsync(a.hdr, 0, sizeof(WsHeader), s) != cudaSuccess) return SSD_ERR_CUDA;
-    if (b.T == 0) return SSD_OK;
     const size_t nbc = sizeof(float) * (size_t)b.T * b.G * b.N;
     if (cudaMemsetAsync(a.dbacc, 0, nbc, s) != cudaSuccess ||
         cudaMemsetAsync(a.dcacc, 0, nbc, s) != cudaSuccess)
