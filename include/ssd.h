@@ -107,6 +107,34 @@ ssd_status_t ssd_backward(const ssd_problem_t* prob, const void* x, const float*
                           const void* dy, void* dx, float* d_raw_dt, void* dB, void* dC,
                           void* workspace, size_t workspace_bytes, void* stream);
 
+/* Size of the device scratch array that ssd_forward_noalloc works in. */
+#define SSD_NOALLOC_SCRATCH_BYTES (64u << 20)
+
+/* ssd_forward for callers that cannot allocate device memory.  The pages have
+ * no counterpart to this call: it exists for host applications whose device
+ * memory is owned by someone else -- a plugin or callback inside a framework
+ * that hands out no workspace, or code on a latency-critical path where
+ * cudaMalloc / cudaFree (which may synchronise the device) are not allowed.
+ * Such a caller passes only inputs and outputs; the scratch that ssd_forward
+ * takes as `workspace` comes instead from one SSD_NOALLOC_SCRATCH_BYTES array
+ * that the library declares in device memory.  Every GPU on which the library
+ * is loaded holds that array until the process exits (with CUDA's default lazy
+ * module loading, from the first call on that GPU).
+ *  - Same arguments, layouts and results as ssd_forward, minus the workspace.
+ *  - Problems whose forward workspace (ssd_workspace_size(prob, 0)) exceeds
+ *    SSD_NOALLOC_SCRATCH_BYTES are rejected with SSD_ERR_WORKSPACE before any
+ *    launch.
+ *  - The first call on a device looks up the array's device address for that
+ *    device (the current one); make that first call before any stream capture.
+ *  - Every call on a device uses the same array, which keeps the previous
+ *    call's contents (the call clears what it needs cleared); calls that may
+ *    overlap on the GPU, from any stream or thread, race and must be ordered
+ *    by the caller.
+ *  - Allocates nothing: no cudaMalloc, cudaFree or allocating library call. */
+ssd_status_t ssd_forward_noalloc(const ssd_problem_t* prob, const void* x, const float* raw_dt,
+                                 const void* B, const void* C, const int32_t* cu_seqlens,
+                                 void* y, float* final_state, void* stream);
+
 /* Synchronises `stream` and returns in *device_status the status word that
  * the last call using `workspace` left (SSD_OK, SSD_ERR_DEVICE, SSD_ERR_TIMEOUT).
  * Returns SSD_ERR_CUDA if the synchronisation itself failed. */
