@@ -107,7 +107,7 @@ ssd_status_t make_prob(const ssd_problem_t* p, Prob* out) {
     b.Q = p->chunk_size;
     b.delta_init = p->delta_init;
     b.dtype = p->dtype;
-    b.tc = tc_supported(p->dtype, p->headdim, p->dstate, p->chunk_size);
+    b.tc = tc_supported(p->dtype, p->headdim, p->dstate, p->chunk_size, p->nheads, p->ngroups);
     b.Ls = choose_segment_length(T, b.nseq, b.H, b.Q);
     // every sequence (dense row) may end in a partial segment
     b.nseg_max = (T + b.Ls - 1) / b.Ls + b.nseq;

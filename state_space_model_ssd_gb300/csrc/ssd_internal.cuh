@@ -90,10 +90,10 @@ struct Launch {
 // SIMT path (any supported shape, f32 or bf16).
 cudaError_t simt_forward(const Prob& pb, const Args& a, Launch& L);
 cudaError_t simt_backward(const Prob& pb, const Args& a, Launch& L);
-// Tensor-core path (bf16, P = 64, N in {64, 128}, Q = 64).
+// Tensor-core path (bf16, P = 64, N in {64, 128}, Q = 64, an even number of heads per group).
 cudaError_t tc_forward(const Prob& pb, const Args& a, Launch& L);
 cudaError_t tc_backward(const Prob& pb, const Args& a, Launch& L);
-bool tc_supported(int dtype, int P, int N, int Q);
+bool tc_supported(int dtype, int P, int N, int Q, int H, int G);
 
 // Shared small kernels (segment table, state scans, gradient epilogues).
 cudaError_t launch_seg_table(const Prob& pb, const Args& a, Launch& L);

@@ -100,11 +100,12 @@ def test_bf16_larger_delta(ssd, oracle_mod):
     _bwd_check(ssd, oracle_mod, d, "bf16", -4.0)
 
 
-@pytest.mark.parametrize("dtype,P,N", [("f32", 16, 32), ("bf16", 64, 128)])
-def test_packed_sequences(ssd, oracle_mod, dtype, P, N):
-    lens = [1, 64, 130, 0, 257, 7, 128, 3]
+@pytest.mark.parametrize("dtype,P,N,H", [("f32", 16, 32, 3), ("bf16", 64, 128, 4),
+                                         ("bf16", 64, 64, 2), ("bf16", 64, 128, 3)])
+def test_packed_sequences(ssd, oracle_mod, dtype, P, N, H):
+    lens = [1, 64, 130, 0, 257, 7, 128, 3, 1100, 65]
     cu = np.concatenate([[0], np.cumsum(lens)])
-    d = _draw(5, 1, int(cu[-1]), 3, P, N, dtype=dtype, cu=cu)
+    d = _draw(5, 1, int(cu[-1]), H, P, N, dtype=dtype, cu=cu)
     _fwd_check(ssd, oracle_mod, d, dtype, -4.6)
     _bwd_check(ssd, oracle_mod, d, dtype, -4.6)
 
@@ -131,6 +132,22 @@ def test_single_token_and_exact_chunks(ssd, oracle_mod):
         d = _draw(8, 1, L, 2, 64, 64, dtype="bf16")
         _fwd_check(ssd, oracle_mod, d, "bf16", -4.6)
         _bwd_check(ssd, oracle_mod, d, "bf16", -4.6)
+
+
+@pytest.mark.parametrize("H,N,expect", [(2, 128, "tensor-core"), (24, 64, "tensor-core"),
+                                         (3, 128, "simt")])
+def test_dispatch_path(ssd, H, N, expect):
+    """bf16, P = 64, chunk 64 and an even number of heads per group take the tensor cores."""
+    import torch
+    x = torch.empty(1, 8, H, 64, dtype=torch.bfloat16, device="cuda")
+    B = torch.empty(1, 8, 1, N, dtype=torch.bfloat16, device="cuda")
+    assert ssd.dispatch_path(ssd.make_problem(x, B, -4.6)) == expect
+
+
+def test_long_segments_bf16(ssd, oracle_mod):
+    """Several full 16-chunk segments per head plus a ragged tail (tensor-core path)."""
+    d = _draw(12, 1, 4 * 1024 + 100, 2, 64, 128, dtype="bf16")
+    _fwd_check(ssd, oracle_mod, d, "bf16", -4.6)
 
 
 def test_empty_input(ssd):
