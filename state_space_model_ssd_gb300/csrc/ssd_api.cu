@@ -1,6 +1,7 @@
 // C ABI of the SSD scan library: argument checks, workspace layout, path
 // dispatch and launch bookkeeping.  No kernel arithmetic lives here.
 #include <math.h>
+#include <stdlib.h>
 #include <string.h>
 
 #include <string>
@@ -74,6 +75,13 @@ bool is_pow2_in(int v, int lo, int hi) {
 // fill the GPU several times over; at most 16 chunks so that the states kept
 // between segments stay small next to the activations.
 int choose_segment_length(long long T, int nseq, int H, int Q) {
+    // SSD_SEGMENT_CHUNKS (1..16) fixes the number of chunks per segment; the
+    // result does not depend on it (tests use it to cover multi-chunk segments
+    // at small sizes).
+    if (const char* env = getenv("SSD_SEGMENT_CHUNKS")) {
+        const int k = atoi(env);
+        if (k >= 1 && k <= 16) return k * Q;
+    }
     const long long target_units = 8LL * 152;
     const long long chunks = (T + Q - 1) / Q;
     int k = 16;
@@ -128,7 +136,7 @@ Layout make_layout(const Prob& b, bool bwd) {
     off = align_up(off + sizeof(float) * (size_t)b.nseg_max * b.H * PN);
     l.lam = off;
     off = align_up(off + sizeof(float) * (size_t)b.nseg_max * b.H);
-    l.adj = l.rq = l.rqsuf = l.dbacc = l.dcacc = 0;
+    l.adj = l.rq = l.rqsuf = l.dbacc = l.dcacc = l.rtok = 0;
     if (bwd) {
         l.adj = off;
         off = align_up(off + sizeof(float) * (size_t)b.nseg_max * b.H * PN);
@@ -140,6 +148,8 @@ Layout make_layout(const Prob& b, bool bwd) {
         off = align_up(off + sizeof(float) * (size_t)b.T * b.G * b.N);
         l.dcacc = off;
         off = align_up(off + sizeof(float) * (size_t)b.T * b.G * b.N);
+        l.rtok = off;
+        off = align_up(off + sizeof(float) * (size_t)b.T * b.H);
     }
     l.total = off;
     return l;
@@ -161,6 +171,7 @@ Args make_args(const Prob& b, const Layout& l, void* ws) {
         a.rqsuf = reinterpret_cast<float*>(base + l.rqsuf);
         a.dbacc = reinterpret_cast<float*>(base + l.dbacc);
         a.dcacc = reinterpret_cast<float*>(base + l.dcacc);
+        a.rtok = reinterpret_cast<float*>(base + l.rtok);
     }
     a.T = b.T;
     a.rowlen = b.rowlen;

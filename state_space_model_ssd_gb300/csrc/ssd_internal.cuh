@@ -46,7 +46,7 @@ struct Prob {
 
 // Byte offsets of the workspace regions.
 struct Layout {
-    size_t header, segtab, A, lam, adj, rq, rqsuf, dbacc, dcacc, total;
+    size_t header, segtab, A, lam, adj, rq, rqsuf, dbacc, dcacc, rtok, total;
 };
 
 // Everything a kernel needs; passed by value.
@@ -72,6 +72,7 @@ struct Args {
     float* rqsuf;   // [nseg_max][H]
     float* dbacc;   // [T][G][N] fp32
     float* dcacc;   // [T][G][N] fp32
+    float* rtok;    // [T][H] fp32: dy_t . y_t per token and head (tensor-core backward)
     long long T, rowlen;
     long long nseg_max;
     int nseq, H, P, N, G, Q, Ls;
@@ -100,5 +101,6 @@ cudaError_t launch_seg_table(const Prob& pb, const Args& a, Launch& L);
 cudaError_t launch_state_scan(const Prob& pb, const Args& a, Launch& L, bool write_final);
 cudaError_t launch_adjoint_scan(const Prob& pb, const Args& a, Launch& L);
 cudaError_t launch_bwd_epilogue(const Prob& pb, const Args& a, Launch& L);
+cudaError_t launch_dbc_convert(const Prob& pb, const Args& a, Launch& L);
 
 }  // namespace ssd

@@ -250,6 +250,10 @@ cudaError_t launch_bwd_epilogue(const Prob& pb, const Args& a, Launch& L) {
     ddt_finalize_kernel<<<(unsigned)pb.nseg_max, 256, 0, L.stream>>>(a);
     e = L.end();
     if (e != cudaSuccess) return e;
+    return launch_dbc_convert(pb, a, L);
+}
+
+cudaError_t launch_dbc_convert(const Prob& pb, const Args& a, Launch& L) {
     const long long n = pb.T * pb.G * pb.N;
     long long blocks = (n + 255) / 256;
     if (blocks > 152 * 16) blocks = 152 * 16;

@@ -25,108 +25,18 @@
 // entering it.
 #include <mutex>
 
-#include "ssd_device.cuh"
-#include "tc_ptx.cuh"
+#include "tc_common.cuh"
 
 namespace ssd {
 
 using namespace tc;
+using namespace tcc;
 
 namespace {
 
-constexpr int kQ = 64;                 // chunk length
-constexpr int kP = 64;                 // head dimension
-constexpr float kMaxChunkDecay = 160.f;
-constexpr uint64_t kWaitNs = 2000000000ull;
-
-// ---------------------------------------------------------------- host: tensor maps
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-    static EncodeTiledFn fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void* p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
-                                             cudaEnableDefault, &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(p);
-    });
-    return fn;
-}
-
-// 3-D bf16 map over a [T][D1][D0] tensor, dims ordered (D0, D1, T), box
-// (64, 1, 64): one 64 x 64 tile of one head (or group) per copy.
-bool make_map(CUtensorMap* m, const void* base, long long T, int D1, int D0) {
-    EncodeTiledFn enc = encode_fn();
-    if (!enc) return false;
-    cuuint64_t dims[3] = {(cuuint64_t)D0, (cuuint64_t)D1, (cuuint64_t)T};
-    cuuint64_t strides[2] = {(cuuint64_t)D0 * 2, (cuuint64_t)D1 * D0 * 2};
-    cuuint32_t box[3] = {64, 1, 64};
-    cuuint32_t es[3] = {1, 1, 1};
-    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
-               box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-// ---------------------------------------------------------------- device helpers
-__device__ __forceinline__ void named_sync(int id, int nthreads) {
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
-}
-
-// Bounded wait that also gives up as soon as another thread has aborted.
-__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity,
-                                              volatile int* abort_flag, WsHeader* hdr) {
-    if (*abort_flag) return false;
-    if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = globaltimer_ns();
-    while (true) {
-        for (int i = 0; i < 32; ++i)
-            if (mbar_try_wait(bar, parity)) return true;
-        if (*abort_flag) return false;
-        if (globaltimer_ns() - t0 > kWaitNs) {
-            *abort_flag = 1;
-            set_status(hdr, SSD_ERR_TIMEOUT);
-            return false;
-        }
-    }
-}
-
-__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
-    __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
-    return *reinterpret_cast<uint32_t*>(&v);
-}
-
-// Multiplies the 8 bf16 values of a 16-byte chunk by s.
-__device__ __forceinline__ uint4 scale_chunk(uint4 v, float s) {
-    uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        __nv_bfloat162 b = *reinterpret_cast<__nv_bfloat162*>(&w[i]);
-        float2 f = __bfloat1622float2(b);
-        w[i] = pack_bf16(f.x * s, f.y * s);
-    }
-    return make_uint4(w[0], w[1], w[2], w[3]);
-}
-
-// Inclusive prefix sum within a warp.
-__device__ __forceinline__ float warp_scan(float v, int lane) {
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const float n = __shfl_up_sync(0xffffffffu, v, o);
-        if (lane >= o) v += n;
-    }
-    return v;
-}
-
 // ================================================================ segment aggregates
 // Warps: 0 = TMA producer, 1 = MMA issuer (and TMEM owner), 2..5 = compute.
-constexpr int kStateStages = 4;
+constexpr int kStateStages = 3;
 constexpr int kStateThreads = 192;
 constexpr int kMaxSeg = 1024;  // segment length bound for the per-token weights
 
@@ -135,9 +45,16 @@ struct StateSmem {
     static constexpr int stage_bytes(int N) { return 16384 + N * 128; }
 };
 
-template <int N>
-__global__ void __launch_bounds__(kStateThreads, 1)
-    tc_fwd_state_kernel(const __grid_constant__ CUtensorMap map_x,
+// MODE 0: forward aggregates  A_j  = sum_t exp(Lambda_end - Lambda_t) delta_t x_t B_t^T
+//         (operands x, B; also writes the segment log-decay).
+// MODE 1: adjoint aggregates Ad_j = sum_u exp(Lambda_u - Lambda_before) dy_u C_u^T
+//         (operands dy, C).
+constexpr int kWPad = kMaxSeg + kMaxSeg / 16;  // per-head weight row, padded against bank conflicts
+__device__ __forceinline__ int widx(int t) { return t + (t >> 4); }
+
+template <int N, int MODE>
+__global__ void __launch_bounds__(kStateThreads, 2)
+    tc_seg_state_kernel(const __grid_constant__ CUtensorMap map_x,
                         const __grid_constant__ CUtensorMap map_b, Args a) {
     const int seg = blockIdx.x;
     const int h0 = blockIdx.y * 2;
@@ -151,8 +68,8 @@ __global__ void __launch_bounds__(kStateThreads, 1)
     unsigned char* sm = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smraw) + 1023) & ~(uintptr_t)1023);
     unsigned char* stages = sm;
-    float* wts = reinterpret_cast<float*>(sm + kStateStages * SB);   // [2][kMaxSeg]
-    float* red = wts + 2 * kMaxSeg;                                 // [8]
+    float* wts = reinterpret_cast<float*>(sm + kStateStages * SB);   // [2][kWPad]
+    float* red = wts + 2 * kWPad;                                   // [8]
     uint64_t* full = reinterpret_cast<uint64_t*>(red + 8);
     uint64_t* empty = full + kStateStages;
     uint64_t* ready = empty + kStateStages;
@@ -222,14 +139,26 @@ __global__ void __launch_bounds__(kStateThreads, 1)
         const int j = ct & 63;              // 64 threads per head
         const int per = (si.len + 63) / 64; // consecutive tokens per thread
         const int t_lo = j * per;
+        {
+            // delta for the whole segment, loads issued together (2 heads x len tokens)
+            float v[2 * kMaxSeg / 128];
+#pragma unroll
+            for (int k = 0; k < 2 * kMaxSeg / 128; ++k) {
+                const int i = ct + 128 * k, t = i >> 1;
+                v[k] = (t < si.len) ? a.raw[(si.start + t) * a.H + h0 + (i & 1)] : 0.f;
+            }
+#pragma unroll
+            for (int k = 0; k < 2 * kMaxSeg / 128; ++k) {
+                const int i = ct + 128 * k, t = i >> 1;
+                wts[(i & 1) * kWPad + widx(t)] =
+                    (t < si.len) ? softplus_f(v[k] + a.delta_init) : 0.f;
+            }
+        }
+        named_sync(1, 128);
         float loc = 0.f;
         for (int i = 0; i < per; ++i) {
             const int t = t_lo + i;
-            float d = 0.f;
-            if (t < si.len)
-                d = softplus_f(a.raw[(si.start + t) * a.H + h0 + head] + a.delta_init);
-            loc += d;
-            if (t < kMaxSeg) wts[head * kMaxSeg + t] = d;
+            if (t < kMaxSeg) loc += wts[head * kWPad + widx(t)];
         }
         // exclusive prefix of the per-thread sums across the head's 64 threads
         float inc = warp_scan(loc, lane);
@@ -238,19 +167,20 @@ __global__ void __launch_bounds__(kStateThreads, 1)
         named_sync(1, 128);
         float excl = inc - loc + (hw ? red[head * 2] : 0.f);
         const float total = red[head * 2] + red[head * 2 + 1];
-        // w_t = delta_t exp(-(sum of delta over (t, end]))
+        // MODE 0: w_t = delta_t exp(-(sum of delta over (t, end]));
+        // MODE 1: w_t = exp(-(sum of delta over [start, t]))
         float run = excl;
         for (int i = 0; i < per; ++i) {
             const int t = t_lo + i;
             if (t < si.len) {
-                const float d = wts[head * kMaxSeg + t];
+                const float d = wts[head * kWPad + widx(t)];
                 run += d;
-                wts[head * kMaxSeg + t] = d * expf(run - total);
+                wts[head * kWPad + widx(t)] = MODE == 0 ? d * expf(run - total) : expf(-run);
             } else if (t < kMaxSeg) {
-                wts[head * kMaxSeg + t] = 0.f;
+                wts[head * kWPad + widx(t)] = 0.f;
             }
         }
-        if (j == 0) a.lam[(long long)seg * a.H + h0 + head] = -total;
+        if (MODE == 0 && j == 0) a.lam[(long long)seg * a.H + h0 + head] = -total;
         named_sync(1, 128);
         // ---- scale x by the weights in place, chunk by chunk
         for (int c = 0; c < nchunks; ++c) {
@@ -263,7 +193,7 @@ __global__ void __launch_bounds__(kStateThreads, 1)
                 const int hh = idx >> 9;
                 const int row = (idx & 511) >> 3;
                 const int t = c * kQ + row;
-                const float w = (t < si.len) ? wts[hh * kMaxSeg + t] : 0.f;
+                const float w = (t < si.len) ? wts[hh * kWPad + widx(t)] : 0.f;
                 xs[idx] = scale_chunk(xs[idx], w);
             }
             fence_proxy_async();
@@ -274,7 +204,8 @@ __global__ void __launch_bounds__(kStateThreads, 1)
         tc_fence_after();
         const int q = warp & 3;
         const int r = 32 * q + lane;  // accumulator row = (head, p)
-        float* Arow = a.A + (((long long)seg * a.H + h0 + (r >> 6)) * kP + (r & 63)) * N;
+        float* Arow = (MODE == 0 ? a.A : a.adj) +
+                      (((long long)seg * a.H + h0 + (r >> 6)) * kP + (r & 63)) * N;
 #pragma unroll
         for (int c0 = 0; c0 < N; c0 += 16) {
             uint32_t v[16];
@@ -471,71 +402,79 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
         const int rh = r >> 6, rp = r & 63;
         constexpr int NH = N / 2;       // state columns per warpgroup
         const int n0 = wg * NH;
-        float H[NH];
+        const uint32_t trow = tmem + ((uint32_t)(32 * q) << 16);
+        // The state is kept pre-scaled for its next chunk: Hs_c = exp(m_c) H_c, so that
+        //   Hs_{c+1} = exp(m_{c+1} + s_end_c / 2) (Hs_c + S_c)      (m_c = s_end_c / 2)
+        // and Hs_c is directly the bf16 operand of G3.
+        float Hs[NH];
+        // byte offsets of this thread's y elements inside a staging tile, by t % 8
+        uint32_t yoff[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+            yoff[k] = rh * 8192 + ((((rp >> 3) ^ k) & 7) << 4) + (rp & 7) * 2;
 
-        // chunk factors for chunk cc into buffer cc & 1 (threads 0..127 compute)
-        auto factors = [&](int cc) {
+        auto load_raw = [&](int cc) -> float {
+            const int head = ct >> 6, t = ct & 63;
+            if (ct >= 128 || cc >= nchunks || t >= si.len - cc * kQ) return 0.f;
+            return a.raw[(si.start + (long long)cc * kQ + t) * a.H + h0 + head];
+        };
+        // chunk factors for chunk cc into buffer cc & 1 (threads 0..127 compute):
+        // f(t) = exp(s_t - m), g(t) = delta_t exp(m - s_t), half = -m = (sum of delta) / 2
+        auto factors = [&](int cc, float rawv) {
             named_sync(1, kCT);
             if (ct < 128) {
                 const int head = ct >> 6, t = ct & 63;
                 const int vc = min(kQ, si.len - cc * kQ);
                 float d = 0.f;
-                if (t < vc)
-                    d = softplus_f(a.raw[(si.start + (long long)cc * kQ + t) * a.H + h0 + head] +
-                                   a.delta_init);
+                if (t < vc) d = softplus_f(rawv + a.delta_init);
                 float inc = warp_scan(d, lane);
                 const int hw = (ct >> 5) & 1;
                 if (lane == 31) red[head * 2 + hw] = inc;
-                // wait for both warps of the head (64 threads per head, ids 2 and 3)
                 named_sync(2 + head, 64);
                 if (hw) inc += red[head * 2];
                 const float send = red[head * 2] + red[head * 2 + 1];  // sum of delta
-                const float sc = -inc;            // s_t
-                const float mid = -0.5f * send;   // reference point
+                const float half = 0.5f * send;
                 const int b = cc & 1;
-                fbuf[(b * 2 + head) * 64 + t] = expf(sc - mid);
-                gbuf[(b * 2 + head) * 64 + t] = d * expf(mid - sc);
+                fbuf[(b * 2 + head) * 64 + t] = expf(half - inc);
+                gbuf[(b * 2 + head) * 64 + t] = d * expf(inc - half);
                 if (t == 0) {
-                    scal[(b * 2 + head) * 4 + 0] = expf(-send);        // exp(s_end)
-                    scal[(b * 2 + head) * 4 + 1] = expf(-send - mid);  // exp(s_end - m)
-                    scal[(b * 2 + head) * 4 + 2] = expf(mid);          // exp(m)
+                    scal[(b * 2 + head) * 4 + 0] = half;
                     if (send > kMaxChunkDecay) set_status(a.hdr, SSD_ERR_DEVICE);
                 }
             }
             named_sync(1, kCT);
         };
-
-        // writes bf16(H * exp(m_cc)) into the H operand buffer for chunk cc
+        // bf16(Hs) -> the G3 operand buffer for chunk cc (K-major, 128-byte swizzle)
         auto write_h = [&](int cc) {
-            const int b = cc & 1;
-            const float hsc = scal[(b * 2 + rh) * 4 + 2];
-            unsigned char* hb = sm + Lay::OFF_H + b * Lay::HBUF;
+            unsigned char* hb = sm + Lay::OFF_H + (cc & 1) * Lay::HBUF + r * 128;
 #pragma unroll
             for (int c8 = 0; c8 < NH; c8 += 8) {
                 const int n = n0 + c8;
-                uint4 v = make_uint4(pack_bf16(H[c8] * hsc, H[c8 + 1] * hsc),
-                                     pack_bf16(H[c8 + 2] * hsc, H[c8 + 3] * hsc),
-                                     pack_bf16(H[c8 + 4] * hsc, H[c8 + 5] * hsc),
-                                     pack_bf16(H[c8 + 6] * hsc, H[c8 + 7] * hsc));
-                *reinterpret_cast<uint4*>(hb + (n >> 6) * 16384 + sw128_offset(r, n & 63)) = v;
+                const uint4 v = make_uint4(pack_bf16(Hs[c8], Hs[c8 + 1]),
+                                           pack_bf16(Hs[c8 + 2], Hs[c8 + 3]),
+                                           pack_bf16(Hs[c8 + 4], Hs[c8 + 5]),
+                                           pack_bf16(Hs[c8 + 6], Hs[c8 + 7]));
+                *reinterpret_cast<uint4*>(hb + (n >> 6) * 16384 +
+                                          (((((n & 63) >> 3) ^ r) & 7) << 4)) = v;
             }
             fence_proxy_async();
-            mbar_arrive(&h_ready[b]);
+            mbar_arrive(&h_ready[cc & 1]);
         };
 
         // prologue: state entering the segment, factors of chunk 0
+        factors(0, load_raw(0));
         {
+            const float sc0 = expf(-scal[(0 * 2 + rh) * 4 + 0]);  // exp(m_0)
             const float* Hin = a.A + (((long long)seg * a.H + h0 + rh) * kP + rp) * N + n0;
 #pragma unroll
             for (int i = 0; i < NH; i += 4) {
                 const float4 v = *reinterpret_cast<const float4*>(Hin + i);
-                H[i] = v.x;
-                H[i + 1] = v.y;
-                H[i + 2] = v.z;
-                H[i + 3] = v.w;
+                Hs[i] = v.x * sc0;
+                Hs[i + 1] = v.y * sc0;
+                Hs[i + 2] = v.z * sc0;
+                Hs[i + 3] = v.w * sc0;
             }
         }
-        factors(0);
         write_h(0);
 
         for (int c = 0; c < nchunks; ++c) {
@@ -544,16 +483,16 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
             const int vc = min(kQ, si.len - c * kQ);
             const long long tok0 = si.start + (long long)c * kQ;
             unsigned char* st = sm + Lay::OFF_STAGE + s * Lay::STAGE;
+            const float raw_next = load_raw(c + 1);  // consumed by factors(c + 1) below
             // A: x -> g(s) x in place (the operand of G2 and G4)
             const bool have = wait_or_abort(&full[s], ph, abort_flag, a.hdr);
             if (have) {
                 uint4* xs = reinterpret_cast<uint4*>(st);
+                const float* gv = gbuf + s * 128;
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
-                    const int idx = ct + kCT * i;  // 0..1023
-                    const int hh = idx >> 9;
-                    const int row = (idx & 511) >> 3;
-                    xs[idx] = scale_chunk(xs[idx], gbuf[(s * 2 + hh) * 64 + row]);
+                    const int idx = ct + kCT * i;  // 0..1023: head = idx / 512, row = (idx / 8) % 64
+                    xs[idx] = scale_chunk(xs[idx], gv[((idx >> 9) << 6) + ((idx >> 3) & 63)]);
                 }
             }
             fence_proxy_async();
@@ -563,81 +502,84 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
                 const bool ok = wait_or_abort(&d1_full[s], ph, abort_flag, a.hdr);
                 tc_fence_after();
                 const int t = 16 * q + lane;
-                unsigned char* l0 = sm + Lay::OFF_L0 + s * 8192;
+                unsigned char* l0 = sm + Lay::OFF_L0 + s * 8192 + t * 128;
+                uint32_t v[64];
+                tmem_ld16(trow + col_d1(s) + 0, *reinterpret_cast<uint32_t(*)[16]>(&v[0]));
+                tmem_ld16(trow + col_d1(s) + 16, *reinterpret_cast<uint32_t(*)[16]>(&v[16]));
+                tmem_ld16(trow + col_d1(s) + 32, *reinterpret_cast<uint32_t(*)[16]>(&v[32]));
+                tmem_ld16(trow + col_d1(s) + 48, *reinterpret_cast<uint32_t(*)[16]>(&v[48]));
+                tmem_wait_ld();
+                if (lane < 16 && ok) {
 #pragma unroll
-                for (int c0 = 0; c0 < 64; c0 += 16) {
-                    uint32_t v[16];
-                    tmem_ld16(tmem + ((uint32_t)(32 * q) << 16) + col_d1(s) + c0, v);
-                    tmem_wait_ld();
-                    if (lane < 16 && ok) {
+                    for (int e = 0; e < 64; e += 8) {
+                        float f[8];
 #pragma unroll
-                        for (int e = 0; e < 16; e += 8) {
-                            float f[8];
-#pragma unroll
-                            for (int u = 0; u < 8; ++u)
-                                f[u] = (c0 + e + u <= t) ? __uint_as_float(v[e + u]) : 0.f;
-                            *reinterpret_cast<uint4*>(l0 + sw128_offset(t, c0 + e)) =
-                                make_uint4(pack_bf16(f[0], f[1]), pack_bf16(f[2], f[3]),
-                                           pack_bf16(f[4], f[5]), pack_bf16(f[6], f[7]));
-                        }
+                        for (int u = 0; u < 8; ++u)
+                            f[u] = (e + u <= t) ? __uint_as_float(v[e + u]) : 0.f;
+                        *reinterpret_cast<uint4*>(l0 + ((((e >> 3) ^ t) & 7) << 4)) =
+                            make_uint4(pack_bf16(f[0], f[1]), pack_bf16(f[2], f[3]),
+                                       pack_bf16(f[4], f[5]), pack_bf16(f[6], f[7]));
                     }
                 }
                 fence_proxy_async();
                 if (lane < 16) mbar_arrive(&l0_ready[s]);
             }
-            // C: state update H <- exp(s_end) H + exp(s_end - m) S
+            // C: factors of the next chunk, state update, H operand of the next chunk
             if (!last) {
+                factors(c + 1, raw_next);
                 const bool ok = wait_or_abort(&s_full[s], ph, abort_flag, a.hdr);
                 tc_fence_after();
-                const float e_end = scal[(s * 2 + rh) * 4 + 0];
-                const float kk = scal[(s * 2 + rh) * 4 + 1];
+                const float gam = expf(-(scal[(s * 2 + rh) * 4 + 0] +
+                                         scal[((s ^ 1) * 2 + rh) * 4 + 0]));
 #pragma unroll
-                for (int c0 = 0; c0 < NH; c0 += 16) {
-                    uint32_t v[16];
-                    tmem_ld16(tmem + ((uint32_t)(32 * q) << 16) + col_s<N>(s) + n0 + c0, v);
+                for (int c0 = 0; c0 < NH; c0 += 32) {
+                    uint32_t v[32];
+                    tmem_ld16(trow + col_s<N>(s) + n0 + c0, *reinterpret_cast<uint32_t(*)[16]>(&v[0]));
+                    tmem_ld16(trow + col_s<N>(s) + n0 + c0 + 16,
+                              *reinterpret_cast<uint32_t(*)[16]>(&v[16]));
                     tmem_wait_ld();
                     if (ok) {
 #pragma unroll
-                        for (int u = 0; u < 16; ++u)
-                            H[c0 + u] = fmaf(e_end, H[c0 + u], kk * __uint_as_float(v[u]));
+                        for (int u = 0; u < 32; ++u)
+                            Hs[c0 + u] = gam * (Hs[c0 + u] + __uint_as_float(v[u]));
                     }
                 }
                 tc_fence_before();
                 mbar_arrive(&s_free[s]);
-                // E, F: factors of the next chunk, then its H operand
-                factors(c + 1);
                 write_h(c + 1);
             }
-            // D: y = f(t) Y  -> staging tile -> TMA store (or direct stores on a partial chunk)
+            // D: y = f(t) Y -> staging tile -> TMA store (or direct stores on a partial chunk)
             {
                 const bool ok = wait_or_abort(&y_full[s], ph, abort_flag, a.hdr);
                 tc_fence_after();
                 if (ct == 0) tma_store_wait_read<1>();
                 named_sync(1, kCT);
-                unsigned char* yst = sm + Lay::OFF_Y + s * 16384 + rh * 8192;
-                const float* fv = fbuf + (s * 2 + rh) * 64;
+                unsigned char* yst = sm + Lay::OFF_Y + s * 16384;
+                const float* fv = fbuf + (s * 2 + rh) * 64 + wg * 32;
+                uint32_t v[32];
+                tmem_ld16(trow + col_y(s) + wg * 32, *reinterpret_cast<uint32_t(*)[16]>(&v[0]));
+                tmem_ld16(trow + col_y(s) + wg * 32 + 16, *reinterpret_cast<uint32_t(*)[16]>(&v[16]));
+                tmem_wait_ld();
+                tc_fence_before();
+                mbar_arrive(&y_free[s]);
+                if (ok) {
+                    if (vc == kQ) {
+                        unsigned char* yb = yst + wg * 32 * 128;
 #pragma unroll
-                for (int c0 = 0; c0 < 32; c0 += 16) {
-                    const int tb = wg * 32 + c0;
-                    uint32_t v[16];
-                    tmem_ld16(tmem + ((uint32_t)(32 * q) << 16) + col_y(s) + tb, v);
-                    tmem_wait_ld();
-                    if (ok) {
+                        for (int u = 0; u < 32; ++u)
+                            *reinterpret_cast<__nv_bfloat16*>(yb + u * 128 + yoff[u & 7]) =
+                                __float2bfloat16_rn(__uint_as_float(v[u]) * fv[u]);
+                    } else {
 #pragma unroll
-                        for (int u = 0; u < 16; ++u) {
-                            const int t = tb + u;
-                            const __nv_bfloat16 yv =
-                                __float2bfloat16_rn(__uint_as_float(v[u]) * fv[t]);
-                            if (vc == kQ)
-                                *reinterpret_cast<__nv_bfloat16*>(yst + sw128_offset(t, rp)) = yv;
-                            else if (t < vc)
+                        for (int u = 0; u < 32; ++u) {
+                            const int t = wg * 32 + u;
+                            if (t < vc)
                                 static_cast<__nv_bfloat16*>(a.y)[((tok0 + t) * a.H + h0 + rh) * kP +
-                                                                 rp] = yv;
+                                                                 rp] =
+                                    __float2bfloat16_rn(__uint_as_float(v[u]) * fv[u]);
                         }
                     }
                 }
-                tc_fence_before();
-                mbar_arrive(&y_free[s]);
                 fence_proxy_async();
                 named_sync(1, kCT);
                 if (ct == 0 && vc == kQ && ok) {
@@ -654,6 +596,781 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
     if (warp == 1) tmem_dealloc(tmem, 512);
 }
 
+// ================================================================ backward walks
+// Both backward kernels walk a segment chunk by chunk for one pair of heads,
+// with the same warp roles as the forward walk (0 = TMA, 1 = MMA, 2..9 =
+// compute).  Per chunk: f(t) = exp(s_t - m), g(t) = delta_t exp(m - s_t) as in
+// the forward; dyf = f dy and xg = g x are scaled in place in the stage.
+//
+// tc_bwd_dc (chunks in order, state Hs_c = exp(m_c) H_c as in the forward walk):
+//   P1_h[t, s] = dyf_t . xg_s                                  (M=64, N=64, K=P)
+//   W_h        = P1_h masked to s <= t                           (epilogue, bf16)
+//   dC_h[t, .] = W_h B + dyf_h Hs_h   = H_t^T dy_t for head h    (M=64, N=N, K=64 + 64)
+//   r_t,h      = C_t . dC_h[t, .]     = dy_t . y_t
+//   dC         = sum over the pair, added into the fp32 accumulator
+// tc_bwd_dxdb (chunks in reverse, adjoint Gs_c = exp(s_end - m) G_c where G_c
+// arrives at the chunk end from later tokens; Gs_{c-1} = gamma (Gs_c + S'_c)):
+//   S'[(h,p), n] = sum_u dyf_u[(h,p)] C_u[n]                     (M=128, N=N, K=64)
+//   L0T[t, u]    = (B_t . C_u) [u >= t]                          (M=64, N=64, K=N)
+//   DX[t,(h,p)]  = sum_u L0T[t,u] dyf_u[(h,p)] + B_t . Gs[(h,p)]   (M=64, N=128)
+//   dx_t         = g(t) DX[t, .],  q_t = x_t . dx_t
+//   P2_h[t, u]   = xg_t . dyf_u masked to u >= t                 (M=64, N=64, K=P)
+//   dB[t, .]     = sum_h P2_h C + xg_h Gs_h                      (M=64, N=N)
+//   d_raw_t = sigmoid(z_t) (q_t / delta_t - sum_{u >= t in the segment} (r_u - q_u) - <G_seg, H_end>)
+constexpr int kBwdThreads = 320;
+
+template <int N>
+struct BwdLayout {
+    static constexpr int STAGE = 32768 + 2 * N * 128;      // x h0|h1, dy h0|h1, B, C
+    static constexpr int OFF_STAGE = 0;
+    static constexpr int OFF_T0 = 2 * STAGE;               // two 8K operand tiles (W / P2m)
+    static constexpr int OFF_T1 = OFF_T0 + 16384;          // 8K (L0T)
+    static constexpr int OFF_S = OFF_T1 + 8192;            // state operand (N/64) x 16K
+    static constexpr int SBUF = (N / 64) * 16384;
+    static constexpr int OFF_F = OFF_S + SBUF;             // f, g, delta: [2 buf][2 head][64] each
+    static constexpr int OFF_SC = OFF_F + 3 * 2 * 2 * 64 * 4;  // half: [2 buf][2 head][4]
+    static constexpr int OFF_RQ = OFF_SC + 2 * 2 * 4 * 4;      // [2 wg][2 head][64]
+    static constexpr int OFF_RED = OFF_RQ + 2 * 2 * 64 * 4;    // [8]
+    static constexpr int OFF_BAR = OFF_RED + 64;
+    static constexpr int NBAR = 16;
+    static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+    static constexpr int TOTAL = OFF_MISC + 16 + 1024;
+};
+
+__device__ __forceinline__ uint64_t kdesc(uint32_t base, int k16, uint32_t kblock) {
+    return sw128_desc(base + (k16 >> 2) * kblock + (k16 & 3) * 32, 16, 1024);
+}
+__device__ __forceinline__ uint64_t mdesc(uint32_t base, int k16, uint32_t lbo) {
+    return sw128_desc(base + k16 * 2048, lbo, 1024);
+}
+
+// Per-chunk factors shared by both backward kernels (threads ct < 128 compute;
+// all kCT compute threads must call).
+struct ChunkFactors {
+    float* fbuf;  // [2][2][64]
+    float* gbuf;
+    float* dbuf;
+    float* scal;  // [2][2][4]: half
+    float* red;
+};
+
+__device__ __forceinline__ void bwd_factors(const ChunkFactors& F, const SegInfo& si,
+                                            const Args& a, int h0, int cc, float rawv, int ct,
+                                            int lane) {
+    named_sync(1, kCT);
+    if (ct < 128) {
+        const int head = ct >> 6, t = ct & 63;
+        const int vc = min(kQ, si.len - cc * kQ);
+        float d = 0.f;
+        if (t < vc) d = softplus_f(rawv + a.delta_init);
+        float inc = warp_scan(d, lane);
+        const int hw = (ct >> 5) & 1;
+        if (lane == 31) F.red[head * 2 + hw] = inc;
+        named_sync(2 + head, 64);
+        if (hw) inc += F.red[head * 2];
+        const float send = F.red[head * 2] + F.red[head * 2 + 1];
+        const float half = 0.5f * send;
+        const int b = cc & 1;
+        // rows past the chunk's valid tokens (another sequence, or past T) get zero
+        // weight on both sides: f for dy, g (through delta = 0) for x
+        F.fbuf[(b * 2 + head) * 64 + t] = (t < vc) ? expf(half - inc) : 0.f;
+        F.gbuf[(b * 2 + head) * 64 + t] = d * expf(inc - half);
+        F.dbuf[(b * 2 + head) * 64 + t] = d;
+        if (t == 0) {
+            F.scal[(b * 2 + head) * 4 + 0] = half;
+            if (send > kMaxChunkDecay) set_status(a.hdr, SSD_ERR_DEVICE);
+        }
+    }
+    named_sync(1, kCT);
+}
+
+__device__ __forceinline__ float bwd_load_raw(const Args& a, const SegInfo& si, int h0, int cc,
+                                              int nchunks, int ct) {
+    const int head = ct >> 6, t = ct & 63;
+    if (ct >= 128 || cc < 0 || cc >= nchunks || t >= si.len - cc * kQ) return 0.f;
+    return a.raw[(si.start + (long long)cc * kQ + t) * a.H + h0 + head];
+}
+
+// x -> g x and dy -> f dy in place (the 4 bf16 tiles at the start of a stage).
+__device__ __forceinline__ void bwd_scale_stage(unsigned char* st, const float* gv,
+                                                const float* fv, int ct) {
+    uint4* xs = reinterpret_cast<uint4*>(st);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int idx = ct + kCT * i;  // 0..2047: [x h0 | x h1 | dy h0 | dy h1] 16-byte chunks
+        const int tile = idx >> 9;
+        const int hh = tile & 1;
+        const int row = (idx >> 3) & 63;
+        const float sc = (tile < 2) ? gv[hh * 64 + row] : fv[hh * 64 + row];
+        xs[idx] = scale_chunk(xs[idx], sc);
+    }
+}
+
+// Masked copy of a 64 x 64 M=64 accumulator (rows t in lanes 0..15 of each
+// quadrant) into a K-major bf16 tile; keep (t, u) when (lower ? u <= t : u >= t).
+__device__ __forceinline__ void masked_tile(uint32_t taddr_row, unsigned char* tile, int t,
+                                            bool active, bool lower) {
+    uint32_t v[64];
+    tmem_ld16(taddr_row + 0, *reinterpret_cast<uint32_t(*)[16]>(&v[0]));
+    tmem_ld16(taddr_row + 16, *reinterpret_cast<uint32_t(*)[16]>(&v[16]));
+    tmem_ld16(taddr_row + 32, *reinterpret_cast<uint32_t(*)[16]>(&v[32]));
+    tmem_ld16(taddr_row + 48, *reinterpret_cast<uint32_t(*)[16]>(&v[48]));
+    tmem_wait_ld();
+    if (!active) return;
+    unsigned char* row = tile + t * 128;
+#pragma unroll
+    for (int e = 0; e < 64; e += 8) {
+        float f[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const bool keep = lower ? (e + u <= t) : (e + u >= t);
+            f[u] = keep ? __uint_as_float(v[e + u]) : 0.f;
+        }
+        *reinterpret_cast<uint4*>(row + ((((e >> 3) ^ t) & 7) << 4)) =
+            make_uint4(pack_bf16(f[0], f[1]), pack_bf16(f[2], f[3]), pack_bf16(f[4], f[5]),
+                       pack_bf16(f[6], f[7]));
+    }
+}
+
+// bf16(S) of this thread's row (h,p) and column half into the state operand buffer.
+template <int NH>
+__device__ __forceinline__ void write_state(unsigned char* sb, const float (&S)[NH], int r,
+                                            int n0) {
+    unsigned char* row = sb + r * 128;
+#pragma unroll
+    for (int c8 = 0; c8 < NH; c8 += 8) {
+        const int n = n0 + c8;
+        const uint4 v = make_uint4(pack_bf16(S[c8], S[c8 + 1]), pack_bf16(S[c8 + 2], S[c8 + 3]),
+                                   pack_bf16(S[c8 + 4], S[c8 + 5]),
+                                   pack_bf16(S[c8 + 6], S[c8 + 7]));
+        *reinterpret_cast<uint4*>(row + (n >> 6) * 16384 + (((((n & 63) >> 3) ^ r) & 7) << 4)) = v;
+    }
+}
+
+// ---------------------------------------------------------------- dC walk
+template <int N>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    tc_bwd_dc_kernel(const __grid_constant__ CUtensorMap map_x,
+                     const __grid_constant__ CUtensorMap map_dy,
+                     const __grid_constant__ CUtensorMap map_b,
+                     const __grid_constant__ CUtensorMap map_c, Args a) {
+    using Lay = BwdLayout<N>;
+    const int seg = blockIdx.x;
+    const int h0 = blockIdx.y * 2;
+    if (seg >= a.hdr->nseg) return;
+    const SegInfo si = a.segtab[seg];
+    const int g = h0 / (a.H / a.G);
+    const int nchunks = (si.len + kQ - 1) / kQ;
+
+    extern __shared__ __align__(1024) unsigned char smraw[];
+    unsigned char* sm = reinterpret_cast<unsigned char*>(
+        (reinterpret_cast<uintptr_t>(smraw) + 1023) & ~(uintptr_t)1023);
+    ChunkFactors F;
+    F.fbuf = reinterpret_cast<float*>(sm + Lay::OFF_F);
+    F.gbuf = F.fbuf + 256;
+    F.dbuf = F.gbuf + 256;
+    F.scal = reinterpret_cast<float*>(sm + Lay::OFF_SC);
+    F.red = reinterpret_cast<float*>(sm + Lay::OFF_RED);
+    float* rpart = reinterpret_cast<float*>(sm + Lay::OFF_RQ);  // [2 wg][2 head][64]
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + Lay::OFF_BAR);
+    uint64_t* full = bars + 0;      // [2]
+    uint64_t* empty = bars + 2;     // [2] (compute threads arrive after the chunk's epilogue)
+    uint64_t* xg_ready = bars + 4;
+    uint64_t* s_full = bars + 5;
+    uint64_t* s_free = bars + 6;
+    uint64_t* p1_full = bars + 7;
+    uint64_t* w_ready = bars + 8;
+    uint64_t* h_ready = bars + 9;
+    uint64_t* dc_full = bars + 10;
+    uint64_t* dc_free = bars + 11;
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + Lay::OFF_MISC);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tslot + 1);
+    const uint32_t T_S = 0, T_P1 = 128, T_DC = 256;  // TMEM columns
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    if (tid == 0) {
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], kCT);
+        }
+        mbar_init(xg_ready, kCT);
+        mbar_init(s_full, 1);
+        mbar_init(s_free, kCT);
+        mbar_init(p1_full, 1);
+        mbar_init(w_ready, kCT);
+        mbar_init(h_ready, kCT);
+        mbar_init(dc_full, 1);
+        mbar_init(dc_free, kCT);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(tslot, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tslot;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            for (int c = 0; c < nchunks; ++c) {
+                const int s = c & 1;
+                if (c >= 2 && !wait_or_abort(&empty[s], ((c >> 1) - 1) & 1, abort_flag, a.hdr))
+                    break;
+                unsigned char* st = sm + Lay::OFF_STAGE + s * Lay::STAGE;
+                const int tok = (int)(si.start + (long long)c * kQ);
+                mbar_expect_tx(&full[s], Lay::STAGE);
+                tma_load_3d(st, &map_x, &full[s], 0, h0, tok);
+                tma_load_3d(st + 8192, &map_x, &full[s], 0, h0 + 1, tok);
+                tma_load_3d(st + 16384, &map_dy, &full[s], 0, h0, tok);
+                tma_load_3d(st + 24576, &map_dy, &full[s], 0, h0 + 1, tok);
+                for (int nb = 0; nb < N / 64; ++nb) {
+                    tma_load_3d(st + 32768 + nb * 8192, &map_b, &full[s], nb * 64, g, tok);
+                    tma_load_3d(st + 32768 + N * 128 + nb * 8192, &map_c, &full[s], nb * 64, g,
+                                tok);
+                }
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            const uint32_t id_s = idesc_bf16(128, N, 1, 1);
+            const uint32_t id_p = idesc_bf16(64, 64, 0, 0);
+            const uint32_t id_c = idesc_bf16(64, N, 0, 1);
+            for (int c = 0; c < nchunks; ++c) {
+                const int s = c & 1, ph = (c >> 1) & 1, pc = c & 1;
+                if (!wait_or_abort(&full[s], ph, abort_flag, a.hdr)) break;
+                if (!wait_or_abort(xg_ready, pc, abort_flag, a.hdr)) break;
+                if (c >= 1 && !wait_or_abort(s_free, pc ^ 1, abort_flag, a.hdr)) break;
+                tc_fence_after();
+                const uint32_t xs = smem_u32(sm + Lay::OFF_STAGE + s * Lay::STAGE);
+                const uint32_t ys = xs + 16384, bs = xs + 32768, cs = bs + N * 128;
+                if (c < nchunks - 1) {  // chunk state, needed only for later chunks
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        mma_bf16(tmem + T_S, mdesc(xs, k, 8192), mdesc(bs, k, 8192), id_s,
+                                 k > 0 ? 1u : 0u);
+                }
+                mma_commit(s_full);
+#pragma unroll
+                for (int h = 0; h < 2; ++h)
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        mma_bf16(tmem + T_P1 + h * 64, kdesc(ys + h * 8192, k, 0),
+                                 kdesc(xs + h * 8192, k, 0), id_p, k > 0 ? 1u : 0u);
+                mma_commit(p1_full);
+                if (!wait_or_abort(w_ready, pc, abort_flag, a.hdr)) break;
+                if (!wait_or_abort(h_ready, pc, abort_flag, a.hdr)) break;
+                if (c >= 1 && !wait_or_abort(dc_free, pc ^ 1, abort_flag, a.hdr)) break;
+                tc_fence_after();
+                const uint32_t wt = smem_u32(sm + Lay::OFF_T0);
+                const uint32_t hb = smem_u32(sm + Lay::OFF_S);
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        mma_bf16(tmem + T_DC + h * N, kdesc(wt + h * 8192, k, 0),
+                                 mdesc(bs, k, 8192), id_c, k > 0 ? 1u : 0u);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        mma_bf16(tmem + T_DC + h * N, kdesc(ys + h * 8192, k, 0),
+                                 mdesc(hb + h * 8192, k, 16384), id_c, 1u);
+                }
+                mma_commit(dc_full);
+            }
+        }
+    } else {
+        const int ct = tid - 64;
+        const int wg = ct >> 7;
+        const int q = warp & 3;
+        const int r = 32 * q + lane;        // M=128 row (h, p)
+        const int rh = r >> 6, rp = r & 63;
+        const int t = 16 * q + lane;        // M=64 row (token), valid for lane < 16
+        const bool trow = lane < 16;
+        constexpr int NH = N / 2;
+        const int n0 = wg * NH;
+        const uint32_t tq = tmem + ((uint32_t)(32 * q) << 16);
+        float Hs[NH];
+
+        bwd_factors(F, si, a, h0, 0, bwd_load_raw(a, si, h0, 0, nchunks, ct), ct, lane);
+        {
+            const float sc0 = expf(-F.scal[(0 * 2 + rh) * 4 + 0]);
+            const float* Hin = a.A + (((long long)seg * a.H + h0 + rh) * kP + rp) * N + n0;
+#pragma unroll
+            for (int i = 0; i < NH; i += 4) {
+                const float4 v = *reinterpret_cast<const float4*>(Hin + i);
+                Hs[i] = v.x * sc0;
+                Hs[i + 1] = v.y * sc0;
+                Hs[i + 2] = v.z * sc0;
+                Hs[i + 3] = v.w * sc0;
+            }
+        }
+        write_state<NH>(sm + Lay::OFF_S, Hs, r, n0);
+        fence_proxy_async();
+        mbar_arrive(h_ready);
+
+        for (int c = 0; c < nchunks; ++c) {
+            const int s = c & 1, ph = (c >> 1) & 1, pc = c & 1;
+            const bool last = (c == nchunks - 1);
+            const int vc = min(kQ, si.len - c * kQ);
+            const long long tok0 = si.start + (long long)c * kQ;
+            unsigned char* st = sm + Lay::OFF_STAGE + s * Lay::STAGE;
+            const float raw_next = bwd_load_raw(a, si, h0, c + 1, nchunks, ct);
+            // A: scale x and dy in place
+            if (wait_or_abort(&full[s], ph, abort_flag, a.hdr))
+                bwd_scale_stage(st, F.gbuf + s * 128, F.fbuf + s * 128, ct);
+            fence_proxy_async();
+            mbar_arrive(xg_ready);
+            // B: W_h = P1_h masked to s <= t (warpgroup h handles head h)
+            {
+                const bool ok = wait_or_abort(p1_full, pc, abort_flag, a.hdr);
+                tc_fence_after();
+                masked_tile(tq + T_P1 + wg * 64, sm + Lay::OFF_T0 + wg * 8192, t, ok && trow, true);
+                fence_proxy_async();
+                mbar_arrive(w_ready);
+            }
+            // C: chunk state -> Hs for the next chunk (kept in registers until dC is done)
+            if (!last) {
+                bwd_factors(F, si, a, h0, c + 1, raw_next, ct, lane);
+                const bool ok = wait_or_abort(s_full, pc, abort_flag, a.hdr);
+                tc_fence_after();
+                const float gam = expf(-(F.scal[(s * 2 + rh) * 4] + F.scal[((s ^ 1) * 2 + rh) * 4]));
+#pragma unroll
+                for (int c0 = 0; c0 < NH; c0 += 32) {
+                    uint32_t v[32];
+                    tmem_ld16(tq + T_S + n0 + c0, *reinterpret_cast<uint32_t(*)[16]>(&v[0]));
+                    tmem_ld16(tq + T_S + n0 + c0 + 16, *reinterpret_cast<uint32_t(*)[16]>(&v[16]));
+                    tmem_wait_ld();
+                    if (ok) {
+#pragma unroll
+                        for (int u = 0; u < 32; ++u) Hs[c0 + u] = gam * (Hs[c0 + u] + __uint_as_float(v[u]));
+                    }
+                }
+                tc_fence_before();
+                mbar_arrive(s_free);
+            } else {
+                mbar_arrive(s_free);
+            }
+            // D: dC rows (both heads, this warpgroup's column half), r partials
+            {
+                const bool ok = wait_or_abort(dc_full, pc, abort_flag, a.hdr) && trow;
+                tc_fence_after();
+                const unsigned char* cst = st + 32768 + N * 128;
+                float rp0 = 0.f, rp1 = 0.f;
+                float* dcrow = a.dcacc + ((tok0 + t) * a.G + g) * (long long)N;
+#pragma unroll
+                for (int c0 = 0; c0 < NH; c0 += 16) {
+                    const int n = n0 + c0;
+                    uint32_t v0[16], v1[16];
+                    tmem_ld16(tq + T_DC + n, v0);
+                    tmem_ld16(tq + T_DC + N + n, v1);
+                    tmem_wait_ld();
+                    if (ok) {
+                        const unsigned char* crow = cst + (n >> 6) * 8192 + t * 128;
+                        float cv[16];
+#pragma unroll
+                        for (int e = 0; e < 16; e += 8) {
+                            const uint4 w = *reinterpret_cast<const uint4*>(
+                                crow + (((((n & 63) + e) >> 3) ^ t) & 7) * 16);
+                            const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                const float2 f2 = __bfloat1622float2(
+                                    *reinterpret_cast<const __nv_bfloat162*>(&ww[i]));
+                                cv[e + 2 * i] = f2.x;
+                                cv[e + 2 * i + 1] = f2.y;
+                            }
+                        }
+#pragma unroll
+                        for (int u = 0; u < 16; ++u) {
+                            const float d0 = __uint_as_float(v0[u]), d1 = __uint_as_float(v1[u]);
+                            rp0 = fmaf(cv[u], d0, rp0);
+                            rp1 = fmaf(cv[u], d1, rp1);
+                        }
+                        if (t < vc) {
+#pragma unroll
+                            for (int u = 0; u < 16; ++u)
+                                atomicAdd(dcrow + n + u,
+                                          __uint_as_float(v0[u]) + __uint_as_float(v1[u]));
+                        }
+                    }
+                }
+                tc_fence_before();
+                mbar_arrive(dc_free);
+                if (trow) {
+                    rpart[(wg * 2 + 0) * 64 + t] = rp0;
+                    rpart[(wg * 2 + 1) * 64 + t] = rp1;
+                }
+                named_sync(1, kCT);
+                if (wg == 0 && trow && t < vc && ok) {
+                    a.rtok[(tok0 + t) * a.H + h0] = rpart[0 * 64 + t] + rpart[2 * 64 + t];
+                    a.rtok[(tok0 + t) * a.H + h0 + 1] = rpart[1 * 64 + t] + rpart[3 * 64 + t];
+                }
+                mbar_arrive(&empty[s]);
+            }
+            // E: the next chunk's state operand (dC of this chunk no longer reads it)
+            if (!last) {
+                write_state<NH>(sm + Lay::OFF_S, Hs, r, n0);
+                fence_proxy_async();
+                mbar_arrive(h_ready);
+            }
+            named_sync(1, kCT);  // rpart reuse
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) tmem_dealloc(tmem, 512);
+}
+
+// ---------------------------------------------------------------- dX / dB walk
+template <int N>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    tc_bwd_dxdb_kernel(const __grid_constant__ CUtensorMap map_x,
+                       const __grid_constant__ CUtensorMap map_dy,
+                       const __grid_constant__ CUtensorMap map_b,
+                       const __grid_constant__ CUtensorMap map_c, Args a) {
+    using Lay = BwdLayout<N>;
+    const int seg = blockIdx.x;
+    const int h0 = blockIdx.y * 2;
+    if (seg >= a.hdr->nseg) return;
+    const SegInfo si = a.segtab[seg];
+    const int g = h0 / (a.H / a.G);
+    const int nchunks = (si.len + kQ - 1) / kQ;
+
+    extern __shared__ __align__(1024) unsigned char smraw[];
+    unsigned char* sm = reinterpret_cast<unsigned char*>(
+        (reinterpret_cast<uintptr_t>(smraw) + 1023) & ~(uintptr_t)1023);
+    ChunkFactors F;
+    F.fbuf = reinterpret_cast<float*>(sm + Lay::OFF_F);
+    F.gbuf = F.fbuf + 256;
+    F.dbuf = F.gbuf + 256;
+    F.scal = reinterpret_cast<float*>(sm + Lay::OFF_SC);
+    F.red = reinterpret_cast<float*>(sm + Lay::OFF_RED);
+    float* rqs = reinterpret_cast<float*>(sm + Lay::OFF_RQ);  // [2 head][64]: r - q of the chunk
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + Lay::OFF_BAR);
+    uint64_t* full = bars + 0;      // [2]
+    uint64_t* empty = bars + 2;     // [2]
+    uint64_t* xg_ready = bars + 4;
+    uint64_t* d1_full = bars + 5;
+    uint64_t* p2_full = bars + 6;
+    uint64_t* e_ready = bars + 7;   // L0T and P2m tiles written, D1/P2 TMEM read
+    uint64_t* s_full = bars + 8;
+    uint64_t* s_free = bars + 9;
+    uint64_t* g_ready = bars + 10;
+    uint64_t* o_full = bars + 11;   // DX and dB accumulated
+    uint64_t* o_free = bars + 12;
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + Lay::OFF_MISC);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tslot + 1);
+    // TMEM columns: D1 0..63, P2 64..191, (S' aliases 0..N-1 once D1/P2 are read), DX 192..319,
+    // dB 320..320+N-1
+    const uint32_t T_D1 = 0, T_P2 = 64, T_SP = 0, T_DX = 192, T_DB = 320;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    if (tid == 0) {
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], kCT);
+        }
+        mbar_init(xg_ready, kCT);
+        mbar_init(d1_full, 1);
+        mbar_init(p2_full, 1);
+        mbar_init(e_ready, kCT);
+        mbar_init(s_full, 1);
+        mbar_init(s_free, kCT);
+        mbar_init(g_ready, kCT);
+        mbar_init(o_full, 1);
+        mbar_init(o_free, kCT);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(tslot, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tslot;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            for (int it = 0; it < nchunks; ++it) {
+                const int c = nchunks - 1 - it, s = it & 1;
+                if (it >= 2 && !wait_or_abort(&empty[s], ((it >> 1) - 1) & 1, abort_flag, a.hdr))
+                    break;
+                unsigned char* st = sm + Lay::OFF_STAGE + s * Lay::STAGE;
+                const int tok = (int)(si.start + (long long)c * kQ);
+                mbar_expect_tx(&full[s], Lay::STAGE);
+                tma_load_3d(st, &map_x, &full[s], 0, h0, tok);
+                tma_load_3d(st + 8192, &map_x, &full[s], 0, h0 + 1, tok);
+                tma_load_3d(st + 16384, &map_dy, &full[s], 0, h0, tok);
+                tma_load_3d(st + 24576, &map_dy, &full[s], 0, h0 + 1, tok);
+                for (int nb = 0; nb < N / 64; ++nb) {
+                    tma_load_3d(st + 32768 + nb * 8192, &map_b, &full[s], nb * 64, g, tok);
+                    tma_load_3d(st + 32768 + N * 128 + nb * 8192, &map_c, &full[s], nb * 64, g,
+                                tok);
+                }
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            const uint32_t id_cb = idesc_bf16(64, 64, 0, 0);
+            const uint32_t id_sp = idesc_bf16(128, N, 1, 1);
+            const uint32_t id_dx1 = idesc_bf16(64, 128, 0, 1);
+            const uint32_t id_dx2 = idesc_bf16(64, 128, 0, 0);
+            const uint32_t id_db = idesc_bf16(64, N, 0, 1);
+            for (int it = 0; it < nchunks; ++it) {
+                const int s = it & 1, ph = (it >> 1) & 1, pi = it & 1;
+                if (!wait_or_abort(&full[s], ph, abort_flag, a.hdr)) break;
+                if (it >= 1 && !wait_or_abort(s_free, pi ^ 1, abort_flag, a.hdr)) break;
+                tc_fence_after();
+                const uint32_t xs = smem_u32(sm + Lay::OFF_STAGE + s * Lay::STAGE);
+                const uint32_t ys = xs + 16384, bs = xs + 32768, cs = bs + N * 128;
+                // L0T[t, u] = B_t . C_u
+#pragma unroll
+                for (int k = 0; k < N / 16; ++k)
+                    mma_bf16(tmem + T_D1, kdesc(bs, k, 8192), kdesc(cs, k, 8192), id_cb,
+                             k > 0 ? 1u : 0u);
+                mma_commit(d1_full);
+                if (!wait_or_abort(xg_ready, pi, abort_flag, a.hdr)) break;
+                tc_fence_after();
+#pragma unroll
+                for (int h = 0; h < 2; ++h)
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        mma_bf16(tmem + T_P2 + h * 64, kdesc(xs + h * 8192, k, 0),
+                                 kdesc(ys + h * 8192, k, 0), id_cb, k > 0 ? 1u : 0u);
+                mma_commit(p2_full);
+                if (!wait_or_abort(e_ready, pi, abort_flag, a.hdr)) break;
+                tc_fence_after();
+                // S' = dyf^T C (adjoint contribution of the chunk), into the freed D1/P2 columns
+                if (it < nchunks - 1) {
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        mma_bf16(tmem + T_SP, mdesc(ys, k, 8192), mdesc(cs, k, 8192), id_sp,
+                                 k > 0 ? 1u : 0u);
+                }
+                mma_commit(s_full);
+                if (!wait_or_abort(g_ready, pi, abort_flag, a.hdr)) break;
+                if (it >= 1 && !wait_or_abort(o_free, pi ^ 1, abort_flag, a.hdr)) break;
+                tc_fence_after();
+                const uint32_t l0 = smem_u32(sm + Lay::OFF_T1);
+                const uint32_t p2m = smem_u32(sm + Lay::OFF_T0);
+                const uint32_t gb = smem_u32(sm + Lay::OFF_S);
+                // DX = L0T dyf + B Gs^T
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    mma_bf16(tmem + T_DX, kdesc(l0, k, 0), mdesc(ys, k, 8192), id_dx1,
+                             k > 0 ? 1u : 0u);
+#pragma unroll
+                for (int k = 0; k < N / 16; ++k)
+                    mma_bf16(tmem + T_DX, kdesc(bs, k, 8192), kdesc(gb, k, 16384), id_dx2, 1u);
+                // dB = sum_h P2m_h C + xg_h Gs_h
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        mma_bf16(tmem + T_DB, kdesc(p2m + h * 8192, k, 0), mdesc(cs, k, 8192),
+                                 id_db, (h > 0 || k > 0) ? 1u : 0u);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        mma_bf16(tmem + T_DB, kdesc(xs + h * 8192, k, 0),
+                                 mdesc(gb + h * 8192, k, 16384), id_db, 1u);
+                }
+                mma_commit(o_full);
+            }
+        }
+    } else {
+        const int ct = tid - 64;
+        const int wg = ct >> 7;
+        const int q = warp & 3;
+        const int r = 32 * q + lane;
+        const int rh = r >> 6, rp = r & 63;
+        const int t = 16 * q + lane;
+        const bool trow = lane < 16;
+        constexpr int NH = N / 2;
+        const int n0 = wg * NH;
+        const uint32_t tq = tmem + ((uint32_t)(32 * q) << 16);
+        float Gs[NH];
+        float carry = 0.f;  // sum of (r - q) over the later chunks of the segment, head wg
+
+        // prologue: adjoint arriving at the segment end, factors of the last chunk, and
+        // kseg = <G_seg, H_end>: the pairs (s, u) of the quadratic form with s in or
+        // before this segment and u after it, which equals the sum over later tokens of
+        // r_u - q_u (both states come from the fp32 scans)
+        const int clast = nchunks - 1;
+        if (ct == 0) {
+            F.red[4] = 0.f;
+            F.red[5] = 0.f;
+        }
+        bwd_factors(F, si, a, h0, clast, bwd_load_raw(a, si, h0, clast, nchunks, ct), ct, lane);
+        {
+            const float sc = expf(-F.scal[((clast & 1) * 2 + rh) * 4 + 0]);
+            const float* Gin = a.adj + (((long long)seg * a.H + h0 + rh) * kP + rp) * N + n0;
+            const bool more = !(si.flags & SEG_LAST);
+            const float* Hend = a.A + (((long long)(seg + 1) * a.H + h0 + rh) * kP + rp) * N + n0;
+            float kp = 0.f;
+#pragma unroll
+            for (int i = 0; i < NH; i += 4) {
+                const float4 v = *reinterpret_cast<const float4*>(Gin + i);
+                if (more) {
+                    const float4 w = *reinterpret_cast<const float4*>(Hend + i);
+                    kp += v.x * w.x + v.y * w.y + v.z * w.z + v.w * w.w;
+                }
+                Gs[i] = v.x * sc;
+                Gs[i + 1] = v.y * sc;
+                Gs[i + 2] = v.z * sc;
+                Gs[i + 3] = v.w * sc;
+            }
+            kp = warp_sum(kp);
+            if (lane == 0) atomicAdd(&F.red[4 + rh], kp);
+        }
+        named_sync(1, kCT);
+        const float kseg = F.red[4 + wg];  // for head wg (the head this warpgroup's dx rows belong to)
+        write_state<NH>(sm + Lay::OFF_S, Gs, r, n0);
+        fence_proxy_async();
+        mbar_arrive(g_ready);
+
+        for (int it = 0; it < nchunks; ++it) {
+            const int c = nchunks - 1 - it;
+            const int s = it & 1, ph = (it >> 1) & 1, pi = it & 1, fb = c & 1;
+            const int vc = min(kQ, si.len - c * kQ);
+            const long long tok0 = si.start + (long long)c * kQ;
+            unsigned char* st = sm + Lay::OFF_STAGE + s * Lay::STAGE;
+            const float raw_next = bwd_load_raw(a, si, h0, c - 1, nchunks, ct);
+            const float rv = (trow && t < vc) ? a.rtok[(tok0 + t) * a.H + h0 + wg] : 0.f;
+            // A: scale x and dy in place
+            if (wait_or_abort(&full[s], ph, abort_flag, a.hdr))
+                bwd_scale_stage(st, F.gbuf + fb * 128, F.fbuf + fb * 128, ct);
+            fence_proxy_async();
+            mbar_arrive(xg_ready);
+            // B: L0T (warpgroup 0) and the masked P2 tiles (warpgroup 1, both heads)
+            if (wg == 0) {
+                const bool ok = wait_or_abort(d1_full, pi, abort_flag, a.hdr);
+                tc_fence_after();
+                masked_tile(tq + T_D1, sm + Lay::OFF_T1, t, ok && trow, false);
+            } else {
+                const bool ok = wait_or_abort(p2_full, pi, abort_flag, a.hdr);
+                tc_fence_after();
+                masked_tile(tq + T_P2, sm + Lay::OFF_T0, t, ok && trow, false);
+                masked_tile(tq + T_P2 + 64, sm + Lay::OFF_T0 + 8192, t, ok && trow, false);
+            }
+            tc_fence_before();
+            fence_proxy_async();
+            mbar_arrive(e_ready);
+            // C: adjoint chain, Gs for the previous chunk (kept in registers until DX/dB are done)
+            if (c > 0) {
+                bwd_factors(F, si, a, h0, c - 1, raw_next, ct, lane);
+                const bool ok = wait_or_abort(s_full, pi, abort_flag, a.hdr);
+                tc_fence_after();
+                const float gam = expf(-(F.scal[(fb * 2 + rh) * 4] + F.scal[((fb ^ 1) * 2 + rh) * 4]));
+#pragma unroll
+                for (int c0 = 0; c0 < NH; c0 += 32) {
+                    uint32_t v[32];
+                    tmem_ld16(tq + T_SP + n0 + c0, *reinterpret_cast<uint32_t(*)[16]>(&v[0]));
+                    tmem_ld16(tq + T_SP + n0 + c0 + 16, *reinterpret_cast<uint32_t(*)[16]>(&v[16]));
+                    tmem_wait_ld();
+                    if (ok) {
+#pragma unroll
+                        for (int u = 0; u < 32; ++u) Gs[c0 + u] = gam * (Gs[c0 + u] + __uint_as_float(v[u]));
+                    }
+                }
+                tc_fence_before();
+            }
+            mbar_arrive(s_free);
+            // D: dx (head wg), q, dB (columns of this warpgroup), partial d_raw
+            {
+                const bool ok = wait_or_abort(o_full, pi, abort_flag, a.hdr) && trow;
+                tc_fence_after();
+                const float gt = F.gbuf[(fb * 2 + wg) * 64 + (t & 63)];
+                const float dt = F.dbuf[(fb * 2 + wg) * 64 + (t & 63)];
+                const unsigned char* xrow = st + wg * 8192 + (t & 63) * 128;  // xg of head wg, row t
+                __nv_bfloat16* dxrow =
+                    static_cast<__nv_bfloat16*>(a.dx) + ((tok0 + t) * a.H + h0 + wg) * kP;
+                float qv = 0.f;
+#pragma unroll
+                for (int c0 = 0; c0 < 64; c0 += 16) {
+                    uint32_t v[16];
+                    tmem_ld16(tq + T_DX + wg * 64 + c0, v);
+                    tmem_wait_ld();
+                    if (ok) {
+#pragma unroll
+                        for (int e = 0; e < 16; e += 8) {
+                            const uint4 w = *reinterpret_cast<const uint4*>(
+                                xrow + ((((c0 + e) >> 3) ^ t) & 7) * 16);
+                            const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                const float2 xf = __bfloat1622float2(
+                                    *reinterpret_cast<const __nv_bfloat162*>(&ww[i]));
+                                qv = fmaf(xf.x, __uint_as_float(v[e + 2 * i]), qv);
+                                qv = fmaf(xf.y, __uint_as_float(v[e + 2 * i + 1]), qv);
+                            }
+                        }
+                        if (t < vc) {
+#pragma unroll
+                            for (int e = 0; e < 16; e += 8)
+                                *reinterpret_cast<uint4*>(dxrow + c0 + e) = make_uint4(
+                                    pack_bf16(gt * __uint_as_float(v[e]), gt * __uint_as_float(v[e + 1])),
+                                    pack_bf16(gt * __uint_as_float(v[e + 2]), gt * __uint_as_float(v[e + 3])),
+                                    pack_bf16(gt * __uint_as_float(v[e + 4]), gt * __uint_as_float(v[e + 5])),
+                                    pack_bf16(gt * __uint_as_float(v[e + 6]), gt * __uint_as_float(v[e + 7])));
+                        }
+                    }
+                }
+                float* dbrow = a.dbacc + ((tok0 + t) * a.G + g) * (long long)N;
+#pragma unroll
+                for (int c0 = 0; c0 < NH; c0 += 16) {
+                    uint32_t v[16];
+                    tmem_ld16(tq + T_DB + n0 + c0, v);
+                    tmem_wait_ld();
+                    if (ok && t < vc) {
+#pragma unroll
+                        for (int u = 0; u < 16; ++u) atomicAdd(dbrow + n0 + c0 + u, __uint_as_float(v[u]));
+                    }
+                }
+                tc_fence_before();
+                mbar_arrive(o_free);
+                // q = xg . DX (xg = g x, so q = x . dx); x.(G B) = q / delta
+                const float xgb = (dt > 1e-30f) ? qv / dt : 0.f;
+                if (trow) rqs[wg * 64 + t] = (t < vc) ? (rv - qv) : 0.f;
+                named_sync(1, kCT);
+                float suf = 0.f;
+                for (int u = 63; u >= 0; --u) {
+                    const float w = rqs[wg * 64 + u];
+                    if (u >= t) suf += w;
+                }
+                const float tot = suf + [&] {
+                    float s0 = 0.f;
+                    for (int u = 0; u < t; ++u) s0 += rqs[wg * 64 + u];
+                    return s0;
+                }();
+                // d raw = sigmoid(raw + delta_init) d delta, sigmoid = 1 - exp(-delta)
+                if (ok && t < vc)
+                    a.draw[(tok0 + t) * a.H + h0 + wg] = -expm1f(-dt) * (xgb - (carry + suf + kseg));
+                carry += tot;
+                mbar_arrive(&empty[s]);
+            }
+            // E: state operand for the previous chunk
+            if (c > 0) {
+                write_state<NH>(sm + Lay::OFF_S, Gs, r, n0);
+                fence_proxy_async();
+                mbar_arrive(g_ready);
+            }
+            named_sync(1, kCT);  // rqs reuse
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) tmem_dealloc(tmem, 512);
+}
+
+constexpr int state_smem_bytes(int N) {
+    return kStateStages * StateSmem::stage_bytes(N) + 2 * kWPad * 4 + 32 + 3 * kStateStages * 8 +
+           8 + 16 + 1024;
+}
+
 template <typename K>
 cudaError_t set_smem(K kernel, int bytes) {
     return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
@@ -668,12 +1385,10 @@ cudaError_t forward_n(const Prob& pb, const Args& a, Launch& L) {
     cudaError_t e = launch_seg_table(pb, a, L);
     if (e != cudaSuccess) return e;
     const dim3 grid((unsigned)pb.nseg_max, pb.H / 2);
-    const int smem_state = kStateStages * StateSmem::stage_bytes(N) + 2 * kMaxSeg * 4 + 32 +
-                           3 * kStateStages * 8 + 8 + 16 + 1024;
-    e = set_smem(tc_fwd_state_kernel<N>, smem_state);
+    e = set_smem(tc_seg_state_kernel<N, 0>, state_smem_bytes(N));
     if (e != cudaSuccess) return e;
     L.begin("tc_fwd_state");
-    tc_fwd_state_kernel<N><<<grid, kStateThreads, smem_state, L.stream>>>(mx, mb, a);
+    tc_seg_state_kernel<N, 0><<<grid, kStateThreads, state_smem_bytes(N), L.stream>>>(mx, mb, a);
     e = L.end();
     if (e != cudaSuccess) return e;
     e = launch_state_scan(pb, a, L, a.final_state != nullptr);
@@ -684,6 +1399,41 @@ cudaError_t forward_n(const Prob& pb, const Args& a, Launch& L) {
     tc_fwd_walk_kernel<N><<<grid, kWalkThreads, WalkLayout<N>::TOTAL, L.stream>>>(mx, mb, mc, my,
                                                                                   a);
     return L.end();
+}
+
+template <int N>
+cudaError_t backward_n(const Prob& pb, const Args& a, Launch& L) {
+    CUtensorMap mx, mdy, mb, mc;
+    if (!make_map(&mx, a.x, pb.T, pb.H, kP) || !make_map(&mdy, a.dy, pb.T, pb.H, kP) ||
+        !make_map(&mb, a.B, pb.T, pb.G, N) || !make_map(&mc, a.C, pb.T, pb.G, N))
+        return cudaErrorInvalidValue;
+    cudaError_t e = launch_seg_table(pb, a, L);
+    if (e != cudaSuccess) return e;
+    const dim3 grid((unsigned)pb.nseg_max, pb.H / 2);
+    e = set_smem(tc_seg_state_kernel<N, 0>, state_smem_bytes(N));
+    if (e != cudaSuccess) return e;
+    L.begin("tc_fwd_state");
+    tc_seg_state_kernel<N, 0><<<grid, kStateThreads, state_smem_bytes(N), L.stream>>>(mx, mb, a);
+    if ((e = L.end()) != cudaSuccess) return e;
+    if ((e = launch_state_scan(pb, a, L, false)) != cudaSuccess) return e;
+    e = set_smem(tc_seg_state_kernel<N, 1>, state_smem_bytes(N));
+    if (e != cudaSuccess) return e;
+    L.begin("tc_bwd_adj_state");
+    tc_seg_state_kernel<N, 1><<<grid, kStateThreads, state_smem_bytes(N), L.stream>>>(mdy, mc, a);
+    if ((e = L.end()) != cudaSuccess) return e;
+    if ((e = launch_adjoint_scan(pb, a, L)) != cudaSuccess) return e;
+    e = set_smem(tc_bwd_dc_kernel<N>, BwdLayout<N>::TOTAL);
+    if (e != cudaSuccess) return e;
+    L.begin("tc_bwd_dc");
+    tc_bwd_dc_kernel<N><<<grid, kBwdThreads, BwdLayout<N>::TOTAL, L.stream>>>(mx, mdy, mb, mc, a);
+    if ((e = L.end()) != cudaSuccess) return e;
+    e = set_smem(tc_bwd_dxdb_kernel<N>, BwdLayout<N>::TOTAL);
+    if (e != cudaSuccess) return e;
+    L.begin("tc_bwd_dxdb");
+    tc_bwd_dxdb_kernel<N><<<grid, kBwdThreads, BwdLayout<N>::TOTAL, L.stream>>>(mx, mdy, mb, mc,
+                                                                               a);
+    if ((e = L.end()) != cudaSuccess) return e;
+    return launch_dbc_convert(pb, a, L);
 }
 
 }  // namespace
@@ -698,7 +1448,7 @@ cudaError_t tc_forward(const Prob& pb, const Args& a, Launch& L) {
 }
 
 cudaError_t tc_backward(const Prob& pb, const Args& a, Launch& L) {
-    return simt_backward(pb, a, L);
+    return pb.N == 128 ? backward_n<128>(pb, a, L) : backward_n<64>(pb, a, L);
 }
 
 }  // namespace ssd
