@@ -18,6 +18,7 @@ cross ranks.
 from __future__ import annotations
 
 import argparse
+import dataclasses  # noqa: F401
 import json
 import math
 import os
@@ -73,27 +74,54 @@ def algorithmic(w):
 def kernel_model(name, w):
     """(bound, algorithmic amount per launch, unit) for a kernel of the path.
 
-    SIMT kernels are bound by fp32 ALU work: flops counted per state element
-    and token-head (multiply and add counted separately).  Tensor-core and
-    streaming kernels are bound by their compulsory HBM bytes."""
+    Tensor-core kernels are HBM-bound at these shapes (arithmetic intensity
+    ~100-155 flop/byte, below the bf16 ridge of ~285): their algorithmic
+    amount is the compulsory bytes of the tensors the kernel must read or
+    write once (x, dy, dx, y: T*H*P*e; B, C, dB, dC: T*G*N*e; raw_dt, d_raw_dt:
+    T*H*4).  SIMT kernels are bound by fp32 ALU work: flops per state element
+    and token-head (multiply and add counted separately)."""
     T, H, P, N, G = w.total_tokens, w.nheads, w.headdim, w.dstate, w.ngroups
     e = 2 if w.dtype == "bf16" else 4
     per_elem = {"simt_seg_state": 3, "simt_seg_walk": 5, "simt_adj_state": 3,
                 "simt_bwd_walk": 12}
     if name in per_elem:
         return "alu", float(per_elem[name] * T * H * P * N), "flop"
-    xbytes = T * H * P * e
-    bc = T * G * N * e
+    xb = T * H * P * e      # one [T][H][P] activation
+    bc = T * G * N * e      # one [T][G][N] tensor
     raw = T * H * 4
     table = {
-        "tc_fwd_state": xbytes + bc + raw,
-        "tc_fwd_walk": 2 * xbytes + 2 * bc + raw,
-        "tc_bwd_adjoint": xbytes + bc + raw,
-        "tc_bwd_walk": 3 * xbytes + 2 * bc + 2 * raw,
+        "tc_fwd_state": xb + bc + raw,                        # x, B, raw_dt
+        "tc_fwd_walk": 2 * xb + 2 * bc + raw,                 # x, B, C, raw_dt -> y
+        "tc_bwd_adj_state": xb + bc + raw,                    # dy, C, raw_dt
+        "tc_bwd_dc": 2 * xb + 3 * bc + raw,                   # x, dy, B, C, raw_dt -> dC
+        "tc_bwd_dxdb": 3 * xb + 3 * bc + 2 * raw,             # x, dy, B, C, raw_dt -> dx, dB, d_raw
     }
     if name in table:
         return "hbm", float(table[name]), "byte"
     return None, None, None
+
+
+def measured_traffic(name, w):
+    """DRAM bytes per launch of `name` at workload `w`, from the committed ncu
+    summary profiles/traffic.txt, or None when there is none or the kernel source
+    changed since it was taken (the summary records the source file's sha256)."""
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    if not os.path.exists(path):
+        return None
+    import hashlib
+    for line in open(path):
+        parts = line.split()
+        if len(parts) < 4 or line.startswith("#") or parts[0] != name:
+            continue
+        per_token, src, sha = float(parts[1]), parts[2], parts[3]
+        srcp = os.path.join(ROOT, src)
+        if not os.path.exists(srcp):
+            return None
+        if hashlib.sha256(open(srcp, "rb").read()).hexdigest() != sha:
+            return None
+        heads_scale = w.nheads / float(parts[4]) if len(parts) > 4 else 1.0
+        return per_token * w.total_tokens * heads_scale
+    return None
 
 
 class ClockSampler:
@@ -174,7 +202,7 @@ def reference_arm(args, w, rank, world):
     d = make_inputs(w, seed=0, tokens=min(w.seqlen, 8192))
     cores = os.cpu_count() or 1
     heads = min(w.nheads, cores)
-    tokens = min(w.seqlen, 4096)
+    tokens = min(w.seqlen, 8192)
     for _ in range(args.warmup):
         oracle_sample(w, d, heads, tokens, cores)
     total_t, total_tok = 0.0, 0.0
@@ -328,7 +356,8 @@ def gpu_arm(args, w, rank, world, dist):
             ach = amount / avg_s / 1e9
             peak = peaks["hbm_gbs"]
             roof = {"kernel": dom, "bound": "hbm", "achieved": ach, "peak": peak, "unit": "GB/s",
-                    "frac": ach / peak, "traffic": None,
+                    "frac": ach / peak, "traffic": measured_traffic(dom, w),
+                    "algorithmic_bytes": amount,
                     "peak_source": "%s hbm_gbs (copy)" % peak_kind}
         elif bound == "alu":
             clk = (clocks.get("sm_max_mhz") or peaks.get("sm_max_mhz") or 2070.0) * 1e6
@@ -346,13 +375,11 @@ def gpu_arm(args, w, rank, world, dist):
         import oracle
         oracle.build()
         cores = os.cpu_count() or 1
-        heads = min(w.nheads, cores)
-        tokens = min(w.seqlen, 4096)
-        dt, tok = oracle_sample(w, d, heads, tokens, cores)
+        dt, tok = oracle_sample(w, d, w.nheads, w.seqlen, cores)
         cpu = {"value": tok / dt, "unit": "tokens/s", "cores": oracle.max_threads(),
                "kind": "oracle",
-               "sample": "%d of %d heads x first %d tokens, fwd%s, %.1f s" % (
-                   heads, w.nheads, tokens, "+bwd" if w.backward else "", dt)}
+               "sample": "the whole workload once (all %d heads x %d tokens), fwd%s, %.1f s" % (
+                   w.nheads, w.seqlen, "+bwd" if w.backward else "", dt)}
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,
@@ -389,8 +416,13 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--tokens", type=int, default=0,
+                    help="run the workload at this row length instead (profiling a smaller case)")
     args = ap.parse_args()
     w = WORKLOADS[args.workload]
+    if args.tokens > 0:
+        import dataclasses
+        w = dataclasses.replace(w, seqlen=args.tokens, name=w.name + "@%d" % args.tokens)
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     if args.impl == "reference":
