@@ -475,13 +475,59 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
                 Hs[i + 3] = v.w * sc0;
             }
         }
+        // y epilogue of chunk cc: y = f(t) Y -> staging tile -> TMA store (or direct stores
+        // on a partial chunk).  Runs one chunk behind, so the state MMA of the current
+        // chunk overlaps it.
+        auto drain_y = [&](int cc) {
+            const int s = cc & 1, ph = (cc >> 1) & 1;
+            const int vc = min(kQ, si.len - cc * kQ);
+            const long long tok0 = si.start + (long long)cc * kQ;
+                {
+                    const bool ok = wait_or_abort(&y_full[s], ph, abort_flag, a.hdr);
+                    tc_fence_after();
+                    if (ct == 0) tma_store_wait_read<1>();
+                    named_sync(1, kCT);
+                    unsigned char* yst = sm + Lay::OFF_Y + s * 16384;
+                    const float* fv = fbuf + (s * 2 + rh) * 64 + wg * 32;
+                    uint32_t v[32];
+                    tmem_ld16(trow + col_y(s) + wg * 32, *reinterpret_cast<uint32_t(*)[16]>(&v[0]));
+                    tmem_ld16(trow + col_y(s) + wg * 32 + 16, *reinterpret_cast<uint32_t(*)[16]>(&v[16]));
+                    tmem_wait_ld();
+                    tc_fence_before();
+                    mbar_arrive(&y_free[s]);
+                    if (ok) {
+                        if (vc == kQ) {
+                            unsigned char* yb = yst + wg * 32 * 128;
+    #pragma unroll
+                            for (int u = 0; u < 32; ++u)
+                                *reinterpret_cast<__nv_bfloat16*>(yb + u * 128 + yoff[u & 7]) =
+                                    __float2bfloat16_rn(__uint_as_float(v[u]) * fv[u]);
+                        } else {
+    #pragma unroll
+                            for (int u = 0; u < 32; ++u) {
+                                const int t = wg * 32 + u;
+                                if (t < vc)
+                                    static_cast<__nv_bfloat16*>(a.y)[((tok0 + t) * a.H + h0 + rh) * kP +
+                                                                     rp] =
+                                        __float2bfloat16_rn(__uint_as_float(v[u]) * fv[u]);
+                            }
+                        }
+                    }
+                    fence_proxy_async();
+                    named_sync(1, kCT);
+                    if (ct == 0 && vc == kQ && ok) {
+                        tma_store_3d(&map_y, sm + Lay::OFF_Y + s * 16384, 0, h0, (int)tok0);
+                        tma_store_3d(&map_y, sm + Lay::OFF_Y + s * 16384 + 8192, 0, h0 + 1, (int)tok0);
+                        tma_store_commit();
+                    }
+                }
+        };
+
         write_h(0);
 
         for (int c = 0; c < nchunks; ++c) {
             const int s = c & 1, ph = (c >> 1) & 1;
             const bool last = (c == nchunks - 1);
-            const int vc = min(kQ, si.len - c * kQ);
-            const long long tok0 = si.start + (long long)c * kQ;
             unsigned char* st = sm + Lay::OFF_STAGE + s * Lay::STAGE;
             const float raw_next = load_raw(c + 1);  // consumed by factors(c + 1) below
             // A: x -> g(s) x in place (the operand of G2 and G4)
@@ -524,6 +570,8 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
                 fence_proxy_async();
                 if (lane < 16) mbar_arrive(&l0_ready[s]);
             }
+            // y of the previous chunk (it reads the factor buffer factors(c + 1) rewrites)
+            if (c > 0) drain_y(c - 1);
             // C: factors of the next chunk, state update, H operand of the next chunk
             if (!last) {
                 factors(c + 1, raw_next);
@@ -548,47 +596,8 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
                 mbar_arrive(&s_free[s]);
                 write_h(c + 1);
             }
-            // D: y = f(t) Y -> staging tile -> TMA store (or direct stores on a partial chunk)
-            {
-                const bool ok = wait_or_abort(&y_full[s], ph, abort_flag, a.hdr);
-                tc_fence_after();
-                if (ct == 0) tma_store_wait_read<1>();
-                named_sync(1, kCT);
-                unsigned char* yst = sm + Lay::OFF_Y + s * 16384;
-                const float* fv = fbuf + (s * 2 + rh) * 64 + wg * 32;
-                uint32_t v[32];
-                tmem_ld16(trow + col_y(s) + wg * 32, *reinterpret_cast<uint32_t(*)[16]>(&v[0]));
-                tmem_ld16(trow + col_y(s) + wg * 32 + 16, *reinterpret_cast<uint32_t(*)[16]>(&v[16]));
-                tmem_wait_ld();
-                tc_fence_before();
-                mbar_arrive(&y_free[s]);
-                if (ok) {
-                    if (vc == kQ) {
-                        unsigned char* yb = yst + wg * 32 * 128;
-#pragma unroll
-                        for (int u = 0; u < 32; ++u)
-                            *reinterpret_cast<__nv_bfloat16*>(yb + u * 128 + yoff[u & 7]) =
-                                __float2bfloat16_rn(__uint_as_float(v[u]) * fv[u]);
-                    } else {
-#pragma unroll
-                        for (int u = 0; u < 32; ++u) {
-                            const int t = wg * 32 + u;
-                            if (t < vc)
-                                static_cast<__nv_bfloat16*>(a.y)[((tok0 + t) * a.H + h0 + rh) * kP +
-                                                                 rp] =
-                                    __float2bfloat16_rn(__uint_as_float(v[u]) * fv[u]);
-                        }
-                    }
-                }
-                fence_proxy_async();
-                named_sync(1, kCT);
-                if (ct == 0 && vc == kQ && ok) {
-                    tma_store_3d(&map_y, sm + Lay::OFF_Y + s * 16384, 0, h0, (int)tok0);
-                    tma_store_3d(&map_y, sm + Lay::OFF_Y + s * 16384 + 8192, 0, h0 + 1, (int)tok0);
-                    tma_store_commit();
-                }
-            }
         }
+        drain_y(nchunks - 1);
         if (ct == 0) tma_store_wait_all<0>();
     }
     tc_fence_before();
@@ -627,7 +636,8 @@ struct BwdLayout {
     static constexpr int OFF_T1 = OFF_T0 + 16384;          // 8K (L0T)
     static constexpr int OFF_S = OFF_T1 + 8192;            // state operand (N/64) x 16K
     static constexpr int SBUF = (N / 64) * 16384;
-    static constexpr int OFF_F = OFF_S + SBUF;             // f, g, delta: [2 buf][2 head][64] each
+    static constexpr int OFF_R = OFF_S + SBUF;             // fp32 partial dB / dC tiles: (N/32) x 8K
+    static constexpr int OFF_F = OFF_R + (N / 32) * 8192;  // f, g, delta: [2 buf][2 head][64] each
     static constexpr int OFF_SC = OFF_F + 3 * 2 * 2 * 64 * 4;  // half: [2 buf][2 head][4]
     static constexpr int OFF_RQ = OFF_SC + 2 * 2 * 4 * 4;      // [2 wg][2 head][64]
     static constexpr int OFF_RED = OFF_RQ + 2 * 2 * 64 * 4;    // [8]
@@ -747,13 +757,26 @@ __device__ __forceinline__ void write_state(unsigned char* sb, const float (&S)[
     }
 }
 
+// Writes 16 fp32 values (columns n .. n+15 of row t) into the (N/32) x [64 x 32]
+// fp32 staging tiles (128-byte swizzle, 16-byte chunk index XOR t % 8).
+__device__ __forceinline__ void stage_row16(unsigned char* tiles, int t, int n, const float* v) {
+    unsigned char* tile = tiles + (n >> 5) * 8192 + t * 128;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const int chunk = ((n & 31) >> 2) + k;
+        *reinterpret_cast<float4*>(tile + (((chunk ^ t) & 7) << 4)) =
+            make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
+    }
+}
+
 // ---------------------------------------------------------------- dC walk
 template <int N>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     tc_bwd_dc_kernel(const __grid_constant__ CUtensorMap map_x,
                      const __grid_constant__ CUtensorMap map_dy,
                      const __grid_constant__ CUtensorMap map_b,
-                     const __grid_constant__ CUtensorMap map_c, Args a) {
+                     const __grid_constant__ CUtensorMap map_c,
+                     const __grid_constant__ CUtensorMap map_acc, Args a) {
     using Lay = BwdLayout<N>;
     const int seg = blockIdx.x;
     const int h0 = blockIdx.y * 2;
@@ -958,7 +981,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 tc_fence_after();
                 const unsigned char* cst = st + 32768 + N * 128;
                 float rp0 = 0.f, rp1 = 0.f;
-                float* dcrow = a.dcacc + ((tok0 + t) * a.G + g) * (long long)N;
+                unsigned char* rtiles = sm + Lay::OFF_R;
+                if (ct == 0) tma_store_wait_read<0>();  // previous chunk's reduce has read the tiles
+                named_sync(1, kCT);
 #pragma unroll
                 for (int c0 = 0; c0 < NH; c0 += 16) {
                     const int n = n0 + c0;
@@ -988,16 +1013,25 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                             rp0 = fmaf(cv[u], d0, rp0);
                             rp1 = fmaf(cv[u], d1, rp1);
                         }
-                        if (t < vc) {
+                    }
+                    if (trow) {  // partial dC (both heads); rows past the chunk's tokens add zero
+                        float sum[16];
 #pragma unroll
-                            for (int u = 0; u < 16; ++u)
-                                atomicAdd(dcrow + n + u,
-                                          __uint_as_float(v0[u]) + __uint_as_float(v1[u]));
-                        }
+                        for (int u = 0; u < 16; ++u)
+                            sum[u] = (ok && t < vc) ? __uint_as_float(v0[u]) + __uint_as_float(v1[u])
+                                                    : 0.f;
+                        stage_row16(rtiles, t, n, sum);
                     }
                 }
                 tc_fence_before();
                 mbar_arrive(dc_free);
+                fence_proxy_async();
+                named_sync(1, kCT);
+                if (ct == 0) {
+                    for (int j = 0; j < N / 32; ++j)
+                        tma_reduce_add_3d(&map_acc, rtiles + j * 8192, j * 32, g, (int)tok0);
+                    tma_store_commit();
+                }
                 if (trow) {
                     rpart[(wg * 2 + 0) * 64 + t] = rp0;
                     rpart[(wg * 2 + 1) * 64 + t] = rp1;
@@ -1017,6 +1051,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             }
             named_sync(1, kCT);  // rpart reuse
         }
+        if (ct == 0) tma_store_wait_all<0>();
     }
     tc_fence_before();
     __syncthreads();
@@ -1029,7 +1064,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     tc_bwd_dxdb_kernel(const __grid_constant__ CUtensorMap map_x,
                        const __grid_constant__ CUtensorMap map_dy,
                        const __grid_constant__ CUtensorMap map_b,
-                       const __grid_constant__ CUtensorMap map_c, Args a) {
+                       const __grid_constant__ CUtensorMap map_c,
+                       const __grid_constant__ CUtensorMap map_acc, Args a) {
     using Lay = BwdLayout<N>;
     const int seg = blockIdx.x;
     const int h0 = blockIdx.y * 2;
@@ -1319,19 +1355,30 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                         }
                     }
                 }
-                float* dbrow = a.dbacc + ((tok0 + t) * a.G + g) * (long long)N;
+                unsigned char* rtiles = sm + Lay::OFF_R;
+                if (ct == 0) tma_store_wait_read<0>();  // previous chunk's reduce has read the tiles
+                named_sync(1, kCT);
 #pragma unroll
                 for (int c0 = 0; c0 < NH; c0 += 16) {
                     uint32_t v[16];
                     tmem_ld16(tq + T_DB + n0 + c0, v);
                     tmem_wait_ld();
-                    if (ok && t < vc) {
+                    if (trow) {  // partial dB; rows past the chunk's tokens add zero
+                        float val[16];
 #pragma unroll
-                        for (int u = 0; u < 16; ++u) atomicAdd(dbrow + n0 + c0 + u, __uint_as_float(v[u]));
+                        for (int u = 0; u < 16; ++u) val[u] = (ok && t < vc) ? __uint_as_float(v[u]) : 0.f;
+                        stage_row16(rtiles, t, n0 + c0, val);
                     }
                 }
                 tc_fence_before();
                 mbar_arrive(o_free);
+                fence_proxy_async();
+                named_sync(1, kCT);
+                if (ct == 0) {
+                    for (int j = 0; j < N / 32; ++j)
+                        tma_reduce_add_3d(&map_acc, rtiles + j * 8192, j * 32, g, (int)tok0);
+                    tma_store_commit();
+                }
                 // q = xg . DX (xg = g x, so q = x . dx); x.(G B) = q / delta
                 const float xgb = (dt > 1e-30f) ? qv / dt : 0.f;
                 if (trow) rqs[wg * 64 + t] = (t < vc) ? (rv - qv) : 0.f;
@@ -1360,6 +1407,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             }
             named_sync(1, kCT);  // rqs reuse
         }
+        if (ct == 0) tma_store_wait_all<0>();
     }
     tc_fence_before();
     __syncthreads();
@@ -1403,9 +1451,10 @@ cudaError_t forward_n(const Prob& pb, const Args& a, Launch& L) {
 
 template <int N>
 cudaError_t backward_n(const Prob& pb, const Args& a, Launch& L) {
-    CUtensorMap mx, mdy, mb, mc;
+    CUtensorMap mx, mdy, mb, mc, mdb, mdc;
     if (!make_map(&mx, a.x, pb.T, pb.H, kP) || !make_map(&mdy, a.dy, pb.T, pb.H, kP) ||
-        !make_map(&mb, a.B, pb.T, pb.G, N) || !make_map(&mc, a.C, pb.T, pb.G, N))
+        !make_map(&mb, a.B, pb.T, pb.G, N) || !make_map(&mc, a.C, pb.T, pb.G, N) ||
+        !make_map_f32(&mdb, a.dbacc, pb.T, pb.G, N) || !make_map_f32(&mdc, a.dcacc, pb.T, pb.G, N))
         return cudaErrorInvalidValue;
     cudaError_t e = launch_seg_table(pb, a, L);
     if (e != cudaSuccess) return e;
@@ -1425,13 +1474,14 @@ cudaError_t backward_n(const Prob& pb, const Args& a, Launch& L) {
     e = set_smem(tc_bwd_dc_kernel<N>, BwdLayout<N>::TOTAL);
     if (e != cudaSuccess) return e;
     L.begin("tc_bwd_dc");
-    tc_bwd_dc_kernel<N><<<grid, kBwdThreads, BwdLayout<N>::TOTAL, L.stream>>>(mx, mdy, mb, mc, a);
+    tc_bwd_dc_kernel<N><<<grid, kBwdThreads, BwdLayout<N>::TOTAL, L.stream>>>(mx, mdy, mb, mc, mdc,
+                                                                             a);
     if ((e = L.end()) != cudaSuccess) return e;
     e = set_smem(tc_bwd_dxdb_kernel<N>, BwdLayout<N>::TOTAL);
     if (e != cudaSuccess) return e;
     L.begin("tc_bwd_dxdb");
     tc_bwd_dxdb_kernel<N><<<grid, kBwdThreads, BwdLayout<N>::TOTAL, L.stream>>>(mx, mdy, mb, mc,
-                                                                               a);
+                                                                               mdb, a);
     if ((e = L.end()) != cudaSuccess) return e;
     return launch_dbc_convert(pb, a, L);
 }

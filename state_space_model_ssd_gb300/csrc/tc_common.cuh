@@ -52,6 +52,20 @@ inline bool make_map(CUtensorMap* m, const void* base, long long T, int D1, int 
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 3-D fp32 map over a [T][D1][D0] tensor, dims (D0, D1, T), box (32, 1, 64):
+// one 64-row x 128-byte tile (128-byte swizzle), used to add partial dB/dC tiles.
+inline bool make_map_f32(CUtensorMap* m, const void* base, long long T, int D1, int D0) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)D0, (cuuint64_t)D1, (cuuint64_t)T};
+    cuuint64_t strides[2] = {(cuuint64_t)D0 * 4, (cuuint64_t)D1 * D0 * 4};
+    cuuint32_t box[3] = {32, 1, 64};
+    cuuint32_t es[3] = {1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(base), dims, strides, box,
+               es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // ---------------------------------------------------------------- device helpers
 __device__ __forceinline__ void named_sync(int id, int nthreads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
