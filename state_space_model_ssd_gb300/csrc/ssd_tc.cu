@@ -634,10 +634,9 @@ struct BwdLayout {
     static constexpr int OFF_STAGE = 0;
     static constexpr int OFF_T0 = 2 * STAGE;               // two 8K operand tiles (W / P2m)
     static constexpr int OFF_T1 = OFF_T0 + 16384;          // 8K (L0T)
-    static constexpr int OFF_S = OFF_T1 + 8192;            // state operand (N/64) x 16K
+    static constexpr int OFF_S = OFF_T1 + 8192;            // state operand, 2 x (N/64) x 16K
     static constexpr int SBUF = (N / 64) * 16384;
-    static constexpr int OFF_R = OFF_S + SBUF;             // fp32 partial dB / dC tiles: (N/32) x 8K
-    static constexpr int OFF_F = OFF_R + (N / 32) * 8192;  // f, g, delta: [2 buf][2 head][64] each
+    static constexpr int OFF_F = OFF_S + 2 * SBUF;         // f, g, delta: [2 buf][2 head][64] each
     static constexpr int OFF_SC = OFF_F + 3 * 2 * 2 * 64 * 4;  // half: [2 buf][2 head][4]
     static constexpr int OFF_RQ = OFF_SC + 2 * 2 * 4 * 4;      // [2 wg][2 head][64]
     static constexpr int OFF_RED = OFF_RQ + 2 * 2 * 64 * 4;    // [8]
@@ -803,9 +802,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     uint64_t* s_free = bars + 6;
     uint64_t* p1_full = bars + 7;
     uint64_t* w_ready = bars + 8;
-    uint64_t* h_ready = bars + 9;
     uint64_t* dc_full = bars + 10;
     uint64_t* dc_free = bars + 11;
+    uint64_t* h_ready = bars + 12;  // [2], one per state operand buffer
     uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + Lay::OFF_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tslot + 1);
     const uint32_t T_S = 0, T_P1 = 128, T_DC = 256;  // TMEM columns
@@ -821,7 +820,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         mbar_init(s_free, kCT);
         mbar_init(p1_full, 1);
         mbar_init(w_ready, kCT);
-        mbar_init(h_ready, kCT);
+        mbar_init(&h_ready[0], kCT);
+        mbar_init(&h_ready[1], kCT);
         mbar_init(dc_full, 1);
         mbar_init(dc_free, kCT);
         *abort_flag = 0;
@@ -884,11 +884,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                                  kdesc(xs + h * 8192, k, 0), id_p, k > 0 ? 1u : 0u);
                 mma_commit(p1_full);
                 if (!wait_or_abort(w_ready, pc, abort_flag, a.hdr)) break;
-                if (!wait_or_abort(h_ready, pc, abort_flag, a.hdr)) break;
+                if (!wait_or_abort(&h_ready[s], ph, abort_flag, a.hdr)) break;
                 if (c >= 1 && !wait_or_abort(dc_free, pc ^ 1, abort_flag, a.hdr)) break;
                 tc_fence_after();
                 const uint32_t wt = smem_u32(sm + Lay::OFF_T0);
-                const uint32_t hb = smem_u32(sm + Lay::OFF_S);
+                const uint32_t hb = smem_u32(sm + Lay::OFF_S + s * Lay::SBUF);
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
 #pragma unroll
@@ -931,7 +931,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
         write_state<NH>(sm + Lay::OFF_S, Hs, r, n0);
         fence_proxy_async();
-        mbar_arrive(h_ready);
+        mbar_arrive(&h_ready[0]);
+        int pending_empty = -1;  // thread 0: stage whose reduce-add may still read shared memory
 
         for (int c = 0; c < nchunks; ++c) {
             const int s = c & 1, ph = (c >> 1) & 1, pc = c & 1;
@@ -972,6 +973,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 }
                 tc_fence_before();
                 mbar_arrive(s_free);
+                // the next chunk's state operand, in the other buffer (dC of chunk c - 1,
+                // its previous reader, completed before this iteration's epilogue)
+                write_state<NH>(sm + Lay::OFF_S + (s ^ 1) * Lay::SBUF, Hs, r, n0);
+                fence_proxy_async();
+                mbar_arrive(&h_ready[s ^ 1]);
             } else {
                 mbar_arrive(s_free);
             }
@@ -981,9 +987,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 tc_fence_after();
                 const unsigned char* cst = st + 32768 + N * 128;
                 float rp0 = 0.f, rp1 = 0.f;
-                unsigned char* rtiles = sm + Lay::OFF_R;
-                if (ct == 0) tma_store_wait_read<0>();  // previous chunk's reduce has read the tiles
-                named_sync(1, kCT);
+                // the partial dC tiles go into this stage's x / dy tiles, which every MMA of
+                // the chunk has finished reading
+                unsigned char* rtiles = st;
+                if (ct == 0 && pending_empty >= 0) {
+                    tma_store_wait_read<0>();
+                    mbar_arrive(&empty[pending_empty]);
+                    pending_empty = -1;
+                }
 #pragma unroll
                 for (int c0 = 0; c0 < NH; c0 += 16) {
                     const int n = n0 + c0;
@@ -1031,6 +1042,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     for (int j = 0; j < N / 32; ++j)
                         tma_reduce_add_3d(&map_acc, rtiles + j * 8192, j * 32, g, (int)tok0);
                     tma_store_commit();
+                    pending_empty = s;  // released once the reduce-add has read the tiles
                 }
                 if (trow) {
                     rpart[(wg * 2 + 0) * 64 + t] = rp0;
@@ -1041,13 +1053,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     a.rtok[(tok0 + t) * a.H + h0] = rpart[0 * 64 + t] + rpart[2 * 64 + t];
                     a.rtok[(tok0 + t) * a.H + h0 + 1] = rpart[1 * 64 + t] + rpart[3 * 64 + t];
                 }
-                mbar_arrive(&empty[s]);
-            }
-            // E: the next chunk's state operand (dC of this chunk no longer reads it)
-            if (!last) {
-                write_state<NH>(sm + Lay::OFF_S, Hs, r, n0);
-                fence_proxy_async();
-                mbar_arrive(h_ready);
+                if (ct != 0) mbar_arrive(&empty[s]);
             }
             named_sync(1, kCT);  // rpart reuse
         }
@@ -1093,9 +1099,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     uint64_t* e_ready = bars + 7;   // L0T and P2m tiles written, D1/P2 TMEM read
     uint64_t* s_full = bars + 8;
     uint64_t* s_free = bars + 9;
-    uint64_t* g_ready = bars + 10;
     uint64_t* o_full = bars + 11;   // DX and dB accumulated
     uint64_t* o_free = bars + 12;
+    uint64_t* g_ready = bars + 13;  // [2], one per state operand buffer
     uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + Lay::OFF_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tslot + 1);
     // TMEM columns: D1 0..63, P2 64..191, (S' aliases 0..N-1 once D1/P2 are read), DX 192..319,
@@ -1114,7 +1120,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         mbar_init(e_ready, kCT);
         mbar_init(s_full, 1);
         mbar_init(s_free, kCT);
-        mbar_init(g_ready, kCT);
+        mbar_init(&g_ready[0], kCT);
+        mbar_init(&g_ready[1], kCT);
         mbar_init(o_full, 1);
         mbar_init(o_free, kCT);
         *abort_flag = 0;
@@ -1188,12 +1195,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                                  k > 0 ? 1u : 0u);
                 }
                 mma_commit(s_full);
-                if (!wait_or_abort(g_ready, pi, abort_flag, a.hdr)) break;
+                const int cb = (nchunks - 1 - it) & 1;  // state operand buffer of this chunk
+                if (!wait_or_abort(&g_ready[cb], ph, abort_flag, a.hdr)) break;
                 if (it >= 1 && !wait_or_abort(o_free, pi ^ 1, abort_flag, a.hdr)) break;
                 tc_fence_after();
                 const uint32_t l0 = smem_u32(sm + Lay::OFF_T1);
                 const uint32_t p2m = smem_u32(sm + Lay::OFF_T0);
-                const uint32_t gb = smem_u32(sm + Lay::OFF_S);
+                const uint32_t gb = smem_u32(sm + Lay::OFF_S + cb * Lay::SBUF);
                 // DX = L0T dyf + B Gs^T
 #pragma unroll
                 for (int k = 0; k < 4; ++k)
@@ -1264,9 +1272,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
         named_sync(1, kCT);
         const float kseg = F.red[4 + wg];  // for head wg (the head this warpgroup's dx rows belong to)
-        write_state<NH>(sm + Lay::OFF_S, Gs, r, n0);
+        write_state<NH>(sm + Lay::OFF_S + (clast & 1) * Lay::SBUF, Gs, r, n0);
         fence_proxy_async();
-        mbar_arrive(g_ready);
+        mbar_arrive(&g_ready[clast & 1]);
+        int pending_empty = -1;  // thread 0: stage whose reduce-add may still read shared memory
 
         for (int it = 0; it < nchunks; ++it) {
             const int c = nchunks - 1 - it;
@@ -1315,6 +1324,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 tc_fence_before();
             }
             mbar_arrive(s_free);
+            // the previous chunk's state operand, in the other buffer (its previous reader,
+            // chunk c + 1's DX/dB, completed before the last epilogue)
+            if (c > 0) {
+                write_state<NH>(sm + Lay::OFF_S + ((c - 1) & 1) * Lay::SBUF, Gs, r, n0);
+                fence_proxy_async();
+                mbar_arrive(&g_ready[(c - 1) & 1]);
+            }
             // D: dx (head wg), q, dB (columns of this warpgroup), partial d_raw
             {
                 const bool ok = wait_or_abort(o_full, pi, abort_flag, a.hdr) && trow;
@@ -1355,8 +1371,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                         }
                     }
                 }
-                unsigned char* rtiles = sm + Lay::OFF_R;
-                if (ct == 0) tma_store_wait_read<0>();  // previous chunk's reduce has read the tiles
+                // the partial dB tiles go into this stage's x / dy tiles once every thread
+                // has read its x row for q above and every MMA of the chunk is done
+                unsigned char* rtiles = st;
+                if (ct == 0 && pending_empty >= 0) {
+                    tma_store_wait_read<0>();
+                    mbar_arrive(&empty[pending_empty]);
+                    pending_empty = -1;
+                }
                 named_sync(1, kCT);
 #pragma unroll
                 for (int c0 = 0; c0 < NH; c0 += 16) {
@@ -1378,32 +1400,33 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     for (int j = 0; j < N / 32; ++j)
                         tma_reduce_add_3d(&map_acc, rtiles + j * 8192, j * 32, g, (int)tok0);
                     tma_store_commit();
+                    pending_empty = s;  // released once the reduce-add has read the tiles
                 }
                 // q = xg . DX (xg = g x, so q = x . dx); x.(G B) = q / delta
                 const float xgb = (dt > 1e-30f) ? qv / dt : 0.f;
-                if (trow) rqs[wg * 64 + t] = (t < vc) ? (rv - qv) : 0.f;
-                named_sync(1, kCT);
-                float suf = 0.f;
-                for (int u = 63; u >= 0; --u) {
-                    const float w = rqs[wg * 64 + u];
-                    if (u >= t) suf += w;
+                // suffix sums of (r - q) over the chunk's rows u >= t: a reverse scan over
+                // the 16 rows of this quadrant, plus the totals of the later quadrants
+                float suf = (trow && t < vc) ? (rv - qv) : 0.f;
+#pragma unroll
+                for (int o = 1; o < 16; o <<= 1) {
+                    const float nb = __shfl_down_sync(0xffffffffu, suf, o, 16);
+                    if ((lane & 15) + o < 16) suf += nb;
                 }
-                const float tot = suf + [&] {
-                    float s0 = 0.f;
-                    for (int u = 0; u < t; ++u) s0 += rqs[wg * 64 + u];
-                    return s0;
-                }();
+                if (lane == 0) rqs[wg * 4 + q] = suf;
+                named_sync(1, kCT);
+                float later = 0.f, tot = 0.f;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const float x = rqs[wg * 4 + k];
+                    tot += x;
+                    if (k > q) later += x;
+                }
+                suf += later;
                 // d raw = sigmoid(raw + delta_init) d delta, sigmoid = 1 - exp(-delta)
                 if (ok && t < vc)
                     a.draw[(tok0 + t) * a.H + h0 + wg] = -expm1f(-dt) * (xgb - (carry + suf + kseg));
                 carry += tot;
-                mbar_arrive(&empty[s]);
-            }
-            // E: state operand for the previous chunk
-            if (c > 0) {
-                write_state<NH>(sm + Lay::OFF_S, Gs, r, n0);
-                fence_proxy_async();
-                mbar_arrive(g_ready);
+                if (ct != 0) mbar_arrive(&empty[s]);
             }
             named_sync(1, kCT);  // rqs reuse
         }
