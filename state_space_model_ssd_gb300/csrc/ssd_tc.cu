@@ -693,6 +693,33 @@ __device__ __forceinline__ void bwd_factors(const ChunkFactors& F, const SegInfo
     named_sync(1, kCT);
 }
 
+// The same factors computed by warpgroup 0 alone (threads ct < 128); the caller
+// orders the writes against later readers with a block-wide barrier.
+__device__ __forceinline__ void bwd_factors_wg0(const ChunkFactors& F, const SegInfo& si,
+                                                const Args& a, int h0, int cc, float rawv, int ct,
+                                                int lane) {
+    const int head = ct >> 6, t = ct & 63;
+    const int vc = min(kQ, si.len - cc * kQ);
+    float d = 0.f;
+    if (t < vc) d = softplus_f(rawv + a.delta_init);
+    float inc = warp_scan(d, lane);
+    const int hw = (ct >> 5) & 1;
+    if (lane == 31) F.red[head * 2 + hw] = inc;
+    named_sync(2 + head, 64);
+    if (hw) inc += F.red[head * 2];
+    const float send = F.red[head * 2] + F.red[head * 2 + 1];
+    const float half = 0.5f * send;
+    const int b = cc & 1;
+    F.fbuf[(b * 2 + head) * 64 + t] = (t < vc) ? expf(half - inc) : 0.f;
+    F.gbuf[(b * 2 + head) * 64 + t] = d * expf(inc - half);
+    F.dbuf[(b * 2 + head) * 64 + t] = d;
+    if (t == 0) {
+        F.scal[(b * 2 + head) * 4 + 0] = half;
+        if (send > kMaxChunkDecay) set_status(a.hdr, SSD_ERR_DEVICE);
+    }
+    named_sync(2 + head, 64);  // red is reused by the next call
+}
+
 __device__ __forceinline__ float bwd_load_raw(const Args& a, const SegInfo& si, int h0, int cc,
                                               int nchunks, int ct) {
     const int head = ct >> 6, t = ct & 63;
@@ -1277,36 +1304,53 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         mbar_arrive(&g_ready[clast & 1]);
         int pending_empty = -1;  // thread 0: stage whose reduce-add may still read shared memory
 
+        // stage x / dy scaling of chunk index `j` (processing order) into its stage
+        auto scale_chunk_tiles = [&](int j) {
+            const int cj = nchunks - 1 - j, sj = j & 1;
+            if (wait_or_abort(&full[sj], (j >> 1) & 1, abort_flag, a.hdr))
+                bwd_scale_stage(sm + Lay::OFF_STAGE + sj * Lay::STAGE, F.gbuf + (cj & 1) * 128,
+                                F.fbuf + (cj & 1) * 128, ct);
+            fence_proxy_async();
+            mbar_arrive(xg_ready);
+        };
+        scale_chunk_tiles(0);
+
         for (int it = 0; it < nchunks; ++it) {
             const int c = nchunks - 1 - it;
             const int s = it & 1, ph = (it >> 1) & 1, pi = it & 1, fb = c & 1;
             const int vc = min(kQ, si.len - c * kQ);
             const long long tok0 = si.start + (long long)c * kQ;
             unsigned char* st = sm + Lay::OFF_STAGE + s * Lay::STAGE;
+            // release the previous chunk's stage once its dB reduce-add has read it
+            if (ct == 0 && pending_empty >= 0) {
+                tma_store_wait_read<0>();
+                mbar_arrive(&empty[pending_empty]);
+                pending_empty = -1;
+            }
             const float raw_next = bwd_load_raw(a, si, h0, c - 1, nchunks, ct);
             const float rv = (trow && t < vc) ? a.rtok[(tok0 + t) * a.H + h0 + wg] : 0.f;
-            // A: scale x and dy in place
-            if (wait_or_abort(&full[s], ph, abort_flag, a.hdr))
-                bwd_scale_stage(st, F.gbuf + fb * 128, F.fbuf + fb * 128, ct);
-            fence_proxy_async();
-            mbar_arrive(xg_ready);
-            // B: L0T (warpgroup 0) and the masked P2 tiles (warpgroup 1, both heads)
+            // B: L0T and the factors of the next chunk (warpgroup 0), the masked P2 tiles
+            // (warpgroup 1, both heads)
             if (wg == 0) {
                 const bool ok = wait_or_abort(d1_full, pi, abort_flag, a.hdr);
                 tc_fence_after();
                 masked_tile(tq + T_D1, sm + Lay::OFF_T1, t, ok && trow, false);
+                tc_fence_before();
+                fence_proxy_async();
+                mbar_arrive(e_ready);
+                if (c > 0) bwd_factors_wg0(F, si, a, h0, c - 1, raw_next, ct, lane);
             } else {
                 const bool ok = wait_or_abort(p2_full, pi, abort_flag, a.hdr);
                 tc_fence_after();
                 masked_tile(tq + T_P2, sm + Lay::OFF_T0, t, ok && trow, false);
                 masked_tile(tq + T_P2 + 64, sm + Lay::OFF_T0 + 8192, t, ok && trow, false);
+                tc_fence_before();
+                fence_proxy_async();
+                mbar_arrive(e_ready);
             }
-            tc_fence_before();
-            fence_proxy_async();
-            mbar_arrive(e_ready);
-            // C: adjoint chain, Gs for the previous chunk (kept in registers until DX/dB are done)
+            named_sync(1, kCT);  // the next chunk's factors are visible
+            // C: adjoint chain, Gs for the previous chunk
             if (c > 0) {
-                bwd_factors(F, si, a, h0, c - 1, raw_next, ct, lane);
                 const bool ok = wait_or_abort(s_full, pi, abort_flag, a.hdr);
                 tc_fence_after();
                 const float gam = expf(-(F.scal[(fb * 2 + rh) * 4] + F.scal[((fb ^ 1) * 2 + rh) * 4]));
@@ -1331,6 +1375,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 fence_proxy_async();
                 mbar_arrive(&g_ready[(c - 1) & 1]);
             }
+            // A for the next chunk: its tiles are scaled while this chunk's DX/dB MMAs run
+            if (it + 1 < nchunks) scale_chunk_tiles(it + 1);
             // D: dx (head wg), q, dB (columns of this warpgroup), partial d_raw
             {
                 const bool ok = wait_or_abort(o_full, pi, abort_flag, a.hdr) && trow;
@@ -1342,13 +1388,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     static_cast<__nv_bfloat16*>(a.dx) + ((tok0 + t) * a.H + h0 + wg) * kP;
                 float qv = 0.f;
 #pragma unroll
-                for (int c0 = 0; c0 < 64; c0 += 16) {
-                    uint32_t v[16];
-                    tmem_ld16(tq + T_DX + wg * 64 + c0, v);
+                for (int c0 = 0; c0 < 64; c0 += 32) {
+                    uint32_t v[32];
+                    tmem_ld16(tq + T_DX + wg * 64 + c0, *reinterpret_cast<uint32_t(*)[16]>(&v[0]));
+                    tmem_ld16(tq + T_DX + wg * 64 + c0 + 16, *reinterpret_cast<uint32_t(*)[16]>(&v[16]));
                     tmem_wait_ld();
                     if (ok) {
 #pragma unroll
-                        for (int e = 0; e < 16; e += 8) {
+                        for (int e = 0; e < 32; e += 8) {
                             const uint4 w = *reinterpret_cast<const uint4*>(
                                 xrow + ((((c0 + e) >> 3) ^ t) & 7) * 16);
                             const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
@@ -1362,7 +1409,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                         }
                         if (t < vc) {
 #pragma unroll
-                            for (int e = 0; e < 16; e += 8)
+                            for (int e = 0; e < 32; e += 8)
                                 *reinterpret_cast<uint4*>(dxrow + c0 + e) = make_uint4(
                                     pack_bf16(gt * __uint_as_float(v[e]), gt * __uint_as_float(v[e + 1])),
                                     pack_bf16(gt * __uint_as_float(v[e + 2]), gt * __uint_as_float(v[e + 3])),
@@ -1374,22 +1421,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 // the partial dB tiles go into this stage's x / dy tiles once every thread
                 // has read its x row for q above and every MMA of the chunk is done
                 unsigned char* rtiles = st;
-                if (ct == 0 && pending_empty >= 0) {
-                    tma_store_wait_read<0>();
-                    mbar_arrive(&empty[pending_empty]);
-                    pending_empty = -1;
-                }
                 named_sync(1, kCT);
 #pragma unroll
-                for (int c0 = 0; c0 < NH; c0 += 16) {
-                    uint32_t v[16];
-                    tmem_ld16(tq + T_DB + n0 + c0, v);
+                for (int c0 = 0; c0 < NH; c0 += 32) {
+                    uint32_t v[32];
+                    tmem_ld16(tq + T_DB + n0 + c0, *reinterpret_cast<uint32_t(*)[16]>(&v[0]));
+                    tmem_ld16(tq + T_DB + n0 + c0 + 16, *reinterpret_cast<uint32_t(*)[16]>(&v[16]));
                     tmem_wait_ld();
                     if (trow) {  // partial dB; rows past the chunk's tokens add zero
-                        float val[16];
+                        float val[32];
 #pragma unroll
-                        for (int u = 0; u < 16; ++u) val[u] = (ok && t < vc) ? __uint_as_float(v[u]) : 0.f;
+                        for (int u = 0; u < 32; ++u) val[u] = (ok && t < vc) ? __uint_as_float(v[u]) : 0.f;
                         stage_row16(rtiles, t, n0 + c0, val);
+                        stage_row16(rtiles, t, n0 + c0 + 16, val + 16);
                     }
                 }
                 tc_fence_before();
