@@ -35,9 +35,9 @@ using namespace tcc;
 namespace {
 
 // ================================================================ segment aggregates
-// Warps: 0 = TMA producer, 1 = MMA issuer (and TMEM owner), 2..5 = compute.
+// Warps: 0 = TMA producer, 1 = MMA issuer (and TMEM owner), 2..9 = compute.
 constexpr int kStateStages = 3;
-constexpr int kStateThreads = 192;
+constexpr int kStateThreads = 320;  // TMA warp, MMA warp, 8 compute warps
 constexpr int kMaxSeg = 1024;  // segment length bound for the per-token weights
 
 struct StateSmem {
@@ -82,7 +82,7 @@ __global__ void __launch_bounds__(kStateThreads, 2)
         for (int i = 0; i < kStateStages; ++i) {
             mbar_init(&full[i], 1);
             mbar_init(&empty[i], 1);
-            mbar_init(&ready[i], 128);
+            mbar_init(&ready[i], 256);
         }
         mbar_init(done, 1);
         *abort_flag = 0;
@@ -134,18 +134,20 @@ __global__ void __launch_bounds__(kStateThreads, 2)
         }
     } else {
         // ---- compute warps: per-token weights relative to the segment end
-        const int ct = tid - 64;            // 0..127
-        const int head = ct >> 6;           // 0..1
+        const int ct = tid - 64;            // 0..255; the first 128 compute the weights
+        const int head = (ct >> 6) & 1;     // 0..1
         const int j = ct & 63;              // 64 threads per head
         const int per = (si.len + 63) / 64; // consecutive tokens per thread
         const int t_lo = j * per;
+        if (ct < 128) {
         {
-            // delta for the whole segment, loads issued together (2 heads x len tokens)
+            // delta for the whole segment (2 heads x len tokens); unconditional loads
+            // (index clamped into the segment) so that all of them are in flight together
             float v[2 * kMaxSeg / 128];
 #pragma unroll
             for (int k = 0; k < 2 * kMaxSeg / 128; ++k) {
-                const int i = ct + 128 * k, t = i >> 1;
-                v[k] = (t < si.len) ? a.raw[(si.start + t) * a.H + h0 + (i & 1)] : 0.f;
+                const int i = ct + 128 * k, t = min(i >> 1, si.len - 1);
+                v[k] = __ldg(a.raw + (si.start + t) * a.H + h0 + (i & 1));
             }
 #pragma unroll
             for (int k = 0; k < 2 * kMaxSeg / 128; ++k) {
@@ -181,15 +183,16 @@ __global__ void __launch_bounds__(kStateThreads, 2)
             }
         }
         if (MODE == 0 && j == 0) a.lam[(long long)seg * a.H + h0 + head] = -total;
-        named_sync(1, 128);
+        }
+        named_sync(2, 256);  // the weights are visible to all compute warps
         // ---- scale x by the weights in place, chunk by chunk
         for (int c = 0; c < nchunks; ++c) {
             const int s = c % kStateStages;
             if (!wait_or_abort(&full[s], (c / kStateStages) & 1, abort_flag, a.hdr)) break;
             uint4* xs = reinterpret_cast<uint4*>(stages + s * SB);
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const int idx = ct + 128 * i;  // 0..1023 16-byte chunks of the two x tiles
+            for (int i = 0; i < 4; ++i) {
+                const int idx = ct + 256 * i;  // 0..1023 16-byte chunks of the two x tiles
                 const int hh = idx >> 9;
                 const int row = (idx & 511) >> 3;
                 const int t = c * kQ + row;
@@ -204,10 +207,11 @@ __global__ void __launch_bounds__(kStateThreads, 2)
         tc_fence_after();
         const int q = warp & 3;
         const int r = 32 * q + lane;  // accumulator row = (head, p)
+        const int cbase = (ct >> 7) * (N / 2);  // each of the two warpgroups takes half the columns
         float* Arow = (MODE == 0 ? a.A : a.adj) +
                       (((long long)seg * a.H + h0 + (r >> 6)) * kP + (r & 63)) * N;
 #pragma unroll
-        for (int c0 = 0; c0 < N; c0 += 16) {
+        for (int c0 = cbase; c0 < cbase + N / 2; c0 += 16) {
             uint32_t v[16];
             tmem_ld16(tmem + ((uint32_t)(32 * q) << 16) + c0, v);
             tmem_wait_ld();
@@ -226,10 +230,15 @@ __global__ void __launch_bounds__(kStateThreads, 2)
 }
 
 // ================================================================ chunk walk
-// Warps: 0 = TMA producer, 1 = MMA issuer, 2..9 = compute (two warpgroups:
-// WG0 = warps 2..5, WG1 = warps 6..9; each covers the 128 TMEM lanes once).
-constexpr int kWalkThreads = 320;
-constexpr int kCT = 256;  // compute threads
+// Warps: 0 = TMA producer, 1 = MMA issuer, 2.. = compute (kWWG warpgroups of four
+// warps; each warpgroup covers the 128 TMEM lanes once and takes 1/kWWG of the
+// columns of every accumulator).
+constexpr int kCT = 256;  // compute threads of the backward walks (two warpgroups)
+// The forward walk runs four compute warpgroups: the per-chunk epilogues are
+// latency-bound chains, and more warps per scheduler hide their latency.
+constexpr int kWWG = 4;
+constexpr int kWCT = 128 * kWWG;
+constexpr int kWalkThreads = 64 + kWCT;
 
 template <int N>
 struct WalkLayout {
@@ -295,13 +304,13 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
             mbar_init(&full[i], 1);
             mbar_init(&empty[i], 1);
             mbar_init(&d1_full[i], 1);
-            mbar_init(&xg_ready[i], kCT);
-            mbar_init(&l0_ready[i], 64);
+            mbar_init(&xg_ready[i], kWCT);
+            mbar_init(&l0_ready[i], kWCT);
             mbar_init(&s_full[i], 1);
-            mbar_init(&s_free[i], kCT);
+            mbar_init(&s_free[i], kWCT);
             mbar_init(&y_full[i], 1);
-            mbar_init(&y_free[i], kCT);
-            mbar_init(&h_ready[i], kCT);
+            mbar_init(&y_free[i], kWCT);
+            mbar_init(&h_ready[i], kWCT);
         }
         *abort_flag = 0;
         fence_mbar_init();
@@ -396,11 +405,12 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
     } else {
         // ------------------------------------------------ compute warpgroups
         const int ct = tid - 64;        // 0..255
-        const int wg = ct >> 7;         // 0 or 1
+        const int wg = ct >> 7;         // 0 .. kWWG - 1
         const int q = warp & 3;         // TMEM lane quadrant
         const int r = 32 * q + lane;    // accumulator row = (head, p)
         const int rh = r >> 6, rp = r & 63;
-        constexpr int NH = N / 2;       // state columns per warpgroup
+        constexpr int NH = N / kWWG;    // state columns per warpgroup
+        constexpr int YW = kQ / kWWG;   // y columns (tokens) per warpgroup
         const int n0 = wg * NH;
         const uint32_t trow = tmem + ((uint32_t)(32 * q) << 16);
         // The state is kept pre-scaled for its next chunk: Hs_c = exp(m_c) H_c, so that
@@ -421,7 +431,7 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
         // chunk factors for chunk cc into buffer cc & 1 (threads 0..127 compute):
         // f(t) = exp(s_t - m), g(t) = delta_t exp(m - s_t), half = -m = (sum of delta) / 2
         auto factors = [&](int cc, float rawv) {
-            named_sync(1, kCT);
+            named_sync(1, kWCT);
             if (ct < 128) {
                 const int head = ct >> 6, t = ct & 63;
                 const int vc = min(kQ, si.len - cc * kQ);
@@ -442,7 +452,7 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
                     if (send > kMaxChunkDecay) set_status(a.hdr, SSD_ERR_DEVICE);
                 }
             }
-            named_sync(1, kCT);
+            named_sync(1, kWCT);
         };
         // bf16(Hs) -> the G3 operand buffer for chunk cc (K-major, 128-byte swizzle)
         auto write_h = [&](int cc) {
@@ -486,26 +496,27 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
                     const bool ok = wait_or_abort(&y_full[s], ph, abort_flag, a.hdr);
                     tc_fence_after();
                     if (ct == 0) tma_store_wait_read<1>();
-                    named_sync(1, kCT);
+                    named_sync(1, kWCT);
                     unsigned char* yst = sm + Lay::OFF_Y + s * 16384;
-                    const float* fv = fbuf + (s * 2 + rh) * 64 + wg * 32;
-                    uint32_t v[32];
-                    tmem_ld16(trow + col_y(s) + wg * 32, *reinterpret_cast<uint32_t(*)[16]>(&v[0]));
-                    tmem_ld16(trow + col_y(s) + wg * 32 + 16, *reinterpret_cast<uint32_t(*)[16]>(&v[16]));
+                    const float* fv = fbuf + (s * 2 + rh) * 64 + wg * YW;
+                    uint32_t v[YW];
+#pragma unroll
+                    for (int j = 0; j < YW; j += 16)
+                        tmem_ld16(trow + col_y(s) + wg * YW + j, *reinterpret_cast<uint32_t(*)[16]>(&v[j]));
                     tmem_wait_ld();
                     tc_fence_before();
                     mbar_arrive(&y_free[s]);
                     if (ok) {
                         if (vc == kQ) {
-                            unsigned char* yb = yst + wg * 32 * 128;
-    #pragma unroll
-                            for (int u = 0; u < 32; ++u)
+                            unsigned char* yb = yst + wg * YW * 128;
+#pragma unroll
+                            for (int u = 0; u < YW; ++u)
                                 *reinterpret_cast<__nv_bfloat16*>(yb + u * 128 + yoff[u & 7]) =
                                     __float2bfloat16_rn(__uint_as_float(v[u]) * fv[u]);
                         } else {
-    #pragma unroll
-                            for (int u = 0; u < 32; ++u) {
-                                const int t = wg * 32 + u;
+#pragma unroll
+                            for (int u = 0; u < YW; ++u) {
+                                const int t = wg * YW + u;
                                 if (t < vc)
                                     static_cast<__nv_bfloat16*>(a.y)[((tok0 + t) * a.H + h0 + rh) * kP +
                                                                      rp] =
@@ -514,7 +525,7 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
                         }
                     }
                     fence_proxy_async();
-                    named_sync(1, kCT);
+                    named_sync(1, kWCT);
                     if (ct == 0 && vc == kQ && ok) {
                         tma_store_3d(&map_y, sm + Lay::OFF_Y + s * 16384, 0, h0, (int)tok0);
                         tma_store_3d(&map_y, sm + Lay::OFF_Y + s * 16384 + 8192, 0, h0 + 1, (int)tok0);
@@ -536,39 +547,39 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
                 uint4* xs = reinterpret_cast<uint4*>(st);
                 const float* gv = gbuf + s * 128;
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int idx = ct + kCT * i;  // 0..1023: head = idx / 512, row = (idx / 8) % 64
+                for (int i = 0; i < 1024 / kWCT; ++i) {
+                    const int idx = ct + kWCT * i;  // 0..1023: head = idx / 512, row = (idx / 8) % 64
                     xs[idx] = scale_chunk(xs[idx], gv[((idx >> 9) << 6) + ((idx >> 3) & 63)]);
                 }
             }
             fence_proxy_async();
             mbar_arrive(&xg_ready[s]);
-            // B: L0 = CB^T masked to s <= t (warpgroup 0, lanes 0..15 hold rows t)
-            if (wg == 0) {
+            // B: L0 = CB^T masked to s <= t (lanes 0..15 hold rows t; warpgroup wg takes
+            // columns 16 wg .. 16 wg + 15)
+            {
                 const bool ok = wait_or_abort(&d1_full[s], ph, abort_flag, a.hdr);
                 tc_fence_after();
                 const int t = 16 * q + lane;
-                unsigned char* l0 = sm + Lay::OFF_L0 + s * 8192 + t * 128;
-                uint32_t v[64];
-                tmem_ld16(trow + col_d1(s) + 0, *reinterpret_cast<uint32_t(*)[16]>(&v[0]));
-                tmem_ld16(trow + col_d1(s) + 16, *reinterpret_cast<uint32_t(*)[16]>(&v[16]));
-                tmem_ld16(trow + col_d1(s) + 32, *reinterpret_cast<uint32_t(*)[16]>(&v[32]));
-                tmem_ld16(trow + col_d1(s) + 48, *reinterpret_cast<uint32_t(*)[16]>(&v[48]));
+                const int cb = 16 * wg;
+                uint32_t v[16];
+                tmem_ld16(trow + col_d1(s) + cb, v);
                 tmem_wait_ld();
                 if (lane < 16 && ok) {
+                    unsigned char* l0 = sm + Lay::OFF_L0 + s * 8192 + t * 128;
 #pragma unroll
-                    for (int e = 0; e < 64; e += 8) {
+                    for (int e = 0; e < 16; e += 8) {
                         float f[8];
 #pragma unroll
                         for (int u = 0; u < 8; ++u)
-                            f[u] = (e + u <= t) ? __uint_as_float(v[e + u]) : 0.f;
-                        *reinterpret_cast<uint4*>(l0 + ((((e >> 3) ^ t) & 7) << 4)) =
+                            f[u] = (cb + e + u <= t) ? __uint_as_float(v[e + u]) : 0.f;
+                        *reinterpret_cast<uint4*>(l0 + (((((cb + e) >> 3) ^ t) & 7) << 4)) =
                             make_uint4(pack_bf16(f[0], f[1]), pack_bf16(f[2], f[3]),
                                        pack_bf16(f[4], f[5]), pack_bf16(f[6], f[7]));
                     }
                 }
+                tc_fence_before();
                 fence_proxy_async();
-                if (lane < 16) mbar_arrive(&l0_ready[s]);
+                mbar_arrive(&l0_ready[s]);
             }
             // y of the previous chunk (it reads the factor buffer factors(c + 1) rewrites)
             if (c > 0) drain_y(c - 1);
@@ -580,15 +591,13 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
                 const float gam = expf(-(scal[(s * 2 + rh) * 4 + 0] +
                                          scal[((s ^ 1) * 2 + rh) * 4 + 0]));
 #pragma unroll
-                for (int c0 = 0; c0 < NH; c0 += 32) {
-                    uint32_t v[32];
-                    tmem_ld16(trow + col_s<N>(s) + n0 + c0, *reinterpret_cast<uint32_t(*)[16]>(&v[0]));
-                    tmem_ld16(trow + col_s<N>(s) + n0 + c0 + 16,
-                              *reinterpret_cast<uint32_t(*)[16]>(&v[16]));
+                for (int c0 = 0; c0 < NH; c0 += 16) {
+                    uint32_t v[16];
+                    tmem_ld16(trow + col_s<N>(s) + n0 + c0, v);
                     tmem_wait_ld();
                     if (ok) {
 #pragma unroll
-                        for (int u = 0; u < 32; ++u)
+                        for (int u = 0; u < 16; ++u)
                             Hs[c0 + u] = gam * (Hs[c0 + u] + __uint_as_float(v[u]));
                     }
                 }
