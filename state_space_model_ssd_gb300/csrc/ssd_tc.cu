@@ -753,23 +753,24 @@ __device__ __forceinline__ void bwd_scale_stage(unsigned char* st, const float* 
 
 // Masked copy of a 64 x 64 M=64 accumulator (rows t in lanes 0..15 of each
 // quadrant) into a K-major bf16 tile; keep (t, u) when (lower ? u <= t : u >= t).
+// Every lane of the warp takes part: lane half hf holds columns 32 hf .. 32 hf + 31
+// of row t.
 __device__ __forceinline__ void masked_tile(uint32_t taddr_row, unsigned char* tile, int t,
-                                            bool active, bool lower) {
-    uint32_t v[64];
-    tmem_ld16(taddr_row + 0, *reinterpret_cast<uint32_t(*)[16]>(&v[0]));
-    tmem_ld16(taddr_row + 16, *reinterpret_cast<uint32_t(*)[16]>(&v[16]));
-    tmem_ld16(taddr_row + 32, *reinterpret_cast<uint32_t(*)[16]>(&v[32]));
-    tmem_ld16(taddr_row + 48, *reinterpret_cast<uint32_t(*)[16]>(&v[48]));
+                                            int hf, bool active, bool lower) {
+    uint32_t v[32];
+    tmem_ld16x2<32>(taddr_row + 0, &v[0]);
+    tmem_ld16x2<32>(taddr_row + 16, &v[16]);
     tmem_wait_ld();
     if (!active) return;
     unsigned char* row = tile + t * 128;
 #pragma unroll
-    for (int e = 0; e < 64; e += 8) {
+    for (int e0 = 0; e0 < 32; e0 += 8) {
+        const int e = 32 * hf + e0;
         float f[8];
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
             const bool keep = lower ? (e + u <= t) : (e + u >= t);
-            f[u] = keep ? __uint_as_float(v[e + u]) : 0.f;
+            f[u] = keep ? __uint_as_float(v[e0 + u]) : 0.f;
         }
         *reinterpret_cast<uint4*>(row + ((((e >> 3) ^ t) & 7) << 4)) =
             make_uint4(pack_bf16(f[0], f[1]), pack_bf16(f[2], f[3]), pack_bf16(f[4], f[5]),
@@ -945,8 +946,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const int q = warp & 3;
         const int r = 32 * q + lane;        // M=128 row (h, p)
         const int rh = r >> 6, rp = r & 63;
-        const int t = 16 * q + lane;        // M=64 row (token), valid for lane < 16
-        const bool trow = lane < 16;
+        const int t = 16 * q + (lane & 15);  // M=64 row (token)
+        const int hf = lane >> 4;            // M=64 column half of this lane
         constexpr int NH = N / 2;
         const int n0 = wg * NH;
         const uint32_t tq = tmem + ((uint32_t)(32 * q) << 16);
@@ -986,7 +987,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             {
                 const bool ok = wait_or_abort(p1_full, pc, abort_flag, a.hdr);
                 tc_fence_after();
-                masked_tile(tq + T_P1 + wg * 64, sm + Lay::OFF_T0 + wg * 8192, t, ok && trow, true);
+                masked_tile(tq + T_P1 + wg * 64, sm + Lay::OFF_T0 + wg * 8192, t, hf, ok, true);
                 fence_proxy_async();
                 mbar_arrive(w_ready);
             }
@@ -1017,9 +1018,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             } else {
                 mbar_arrive(s_free);
             }
-            // D: dC rows (both heads, this warpgroup's column half), r partials
+            // D: dC rows (both heads, this warpgroup's column half split over the two lane
+            // halves), r partials
             {
-                const bool ok = wait_or_abort(dc_full, pc, abort_flag, a.hdr) && trow;
+                const bool ok = wait_or_abort(dc_full, pc, abort_flag, a.hdr);
                 tc_fence_after();
                 const unsigned char* cst = st + 32768 + N * 128;
                 float rp0 = 0.f, rp1 = 0.f;
@@ -1032,11 +1034,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     pending_empty = -1;
                 }
 #pragma unroll
-                for (int c0 = 0; c0 < NH; c0 += 16) {
-                    const int n = n0 + c0;
+                for (int c0 = 0; c0 < NH / 2; c0 += 16) {
+                    const int n = n0 + (NH / 2) * hf + c0;
                     uint32_t v0[16], v1[16];
-                    tmem_ld16(tq + T_DC + n, v0);
-                    tmem_ld16(tq + T_DC + N + n, v1);
+                    tmem_ld16x2<NH / 2>(tq + T_DC + n0 + c0, v0);
+                    tmem_ld16x2<NH / 2>(tq + T_DC + N + n0 + c0, v1);
                     tmem_wait_ld();
                     if (ok) {
                         const unsigned char* crow = cst + (n >> 6) * 8192 + t * 128;
@@ -1061,7 +1063,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                             rp1 = fmaf(cv[u], d1, rp1);
                         }
                     }
-                    if (trow) {  // partial dC (both heads); rows past the chunk's tokens add zero
+                    {  // partial dC (both heads); rows past the chunk's tokens add zero
                         float sum[16];
 #pragma unroll
                         for (int u = 0; u < 16; ++u)
@@ -1070,6 +1072,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                         stage_row16(rtiles, t, n, sum);
                     }
                 }
+                rp0 += __shfl_xor_sync(0xffffffffu, rp0, 16);
+                rp1 += __shfl_xor_sync(0xffffffffu, rp1, 16);
                 tc_fence_before();
                 mbar_arrive(dc_free);
                 fence_proxy_async();
@@ -1080,12 +1084,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     tma_store_commit();
                     pending_empty = s;  // released once the reduce-add has read the tiles
                 }
-                if (trow) {
+                if (hf == 0) {
                     rpart[(wg * 2 + 0) * 64 + t] = rp0;
                     rpart[(wg * 2 + 1) * 64 + t] = rp1;
                 }
                 named_sync(1, kCT);
-                if (wg == 0 && trow && t < vc && ok) {
+                if (wg == 0 && hf == 0 && t < vc && ok) {
                     a.rtok[(tok0 + t) * a.H + h0] = rpart[0 * 64 + t] + rpart[2 * 64 + t];
                     a.rtok[(tok0 + t) * a.H + h0 + 1] = rpart[1 * 64 + t] + rpart[3 * 64 + t];
                 }
@@ -1267,8 +1271,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const int q = warp & 3;
         const int r = 32 * q + lane;
         const int rh = r >> 6, rp = r & 63;
-        const int t = 16 * q + lane;
-        const bool trow = lane < 16;
+        const int t = 16 * q + (lane & 15);  // M=64 row (token)
+        const int hf = lane >> 4;            // M=64 column half of this lane
         constexpr int NH = N / 2;
         const int n0 = wg * NH;
         const uint32_t tq = tmem + ((uint32_t)(32 * q) << 16);
@@ -1337,13 +1341,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 pending_empty = -1;
             }
             const float raw_next = bwd_load_raw(a, si, h0, c - 1, nchunks, ct);
-            const float rv = (trow && t < vc) ? a.rtok[(tok0 + t) * a.H + h0 + wg] : 0.f;
+            const float rv = (t < vc) ? a.rtok[(tok0 + t) * a.H + h0 + wg] : 0.f;
             // B: L0T and the factors of the next chunk (warpgroup 0), the masked P2 tiles
             // (warpgroup 1, both heads)
             if (wg == 0) {
                 const bool ok = wait_or_abort(d1_full, pi, abort_flag, a.hdr);
                 tc_fence_after();
-                masked_tile(tq + T_D1, sm + Lay::OFF_T1, t, ok && trow, false);
+                masked_tile(tq + T_D1, sm + Lay::OFF_T1, t, hf, ok, false);
                 tc_fence_before();
                 fence_proxy_async();
                 mbar_arrive(e_ready);
@@ -1351,8 +1355,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             } else {
                 const bool ok = wait_or_abort(p2_full, pi, abort_flag, a.hdr);
                 tc_fence_after();
-                masked_tile(tq + T_P2, sm + Lay::OFF_T0, t, ok && trow, false);
-                masked_tile(tq + T_P2 + 64, sm + Lay::OFF_T0 + 8192, t, ok && trow, false);
+                masked_tile(tq + T_P2, sm + Lay::OFF_T0, t, hf, ok, false);
+                masked_tile(tq + T_P2 + 64, sm + Lay::OFF_T0 + 8192, t, hf, ok, false);
                 tc_fence_before();
                 fence_proxy_async();
                 mbar_arrive(e_ready);
@@ -1386,9 +1390,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             }
             // A for the next chunk: its tiles are scaled while this chunk's DX/dB MMAs run
             if (it + 1 < nchunks) scale_chunk_tiles(it + 1);
-            // D: dx (head wg), q, dB (columns of this warpgroup), partial d_raw
+            // D: dx (head wg), q, dB (columns of this warpgroup), partial d_raw; lane half
+            // hf takes half of the dx columns and half of the dB columns
             {
-                const bool ok = wait_or_abort(o_full, pi, abort_flag, a.hdr) && trow;
+                const bool ok = wait_or_abort(o_full, pi, abort_flag, a.hdr);
                 tc_fence_after();
                 const float gt = F.gbuf[(fb * 2 + wg) * 64 + (t & 63)];
                 const float dt = F.dbuf[(fb * 2 + wg) * 64 + (t & 63)];
@@ -1396,11 +1401,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 __nv_bfloat16* dxrow =
                     static_cast<__nv_bfloat16*>(a.dx) + ((tok0 + t) * a.H + h0 + wg) * kP;
                 float qv = 0.f;
-#pragma unroll
-                for (int c0 = 0; c0 < 64; c0 += 32) {
+                {
+                    const int c0 = 32 * hf;
                     uint32_t v[32];
-                    tmem_ld16(tq + T_DX + wg * 64 + c0, *reinterpret_cast<uint32_t(*)[16]>(&v[0]));
-                    tmem_ld16(tq + T_DX + wg * 64 + c0 + 16, *reinterpret_cast<uint32_t(*)[16]>(&v[16]));
+                    tmem_ld16x2<32>(tq + T_DX + wg * 64, &v[0]);
+                    tmem_ld16x2<32>(tq + T_DX + wg * 64 + 16, &v[16]);
                     tmem_wait_ld();
                     if (ok) {
 #pragma unroll
@@ -1427,22 +1432,26 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                         }
                     }
                 }
+                qv += __shfl_xor_sync(0xffffffffu, qv, 16);
                 // the partial dB tiles go into this stage's x / dy tiles once every thread
                 // has read its x row for q above and every MMA of the chunk is done
                 unsigned char* rtiles = st;
                 named_sync(1, kCT);
+                constexpr int HW = NH / 2;               // dB columns per lane half
+                constexpr int STEP = HW >= 32 ? 32 : 16;  // two loads in flight when possible
 #pragma unroll
-                for (int c0 = 0; c0 < NH; c0 += 32) {
-                    uint32_t v[32];
-                    tmem_ld16(tq + T_DB + n0 + c0, *reinterpret_cast<uint32_t(*)[16]>(&v[0]));
-                    tmem_ld16(tq + T_DB + n0 + c0 + 16, *reinterpret_cast<uint32_t(*)[16]>(&v[16]));
+                for (int c0 = 0; c0 < HW; c0 += STEP) {
+                    uint32_t v[STEP];
+                    tmem_ld16x2<HW>(tq + T_DB + n0 + c0, &v[0]);
+                    if constexpr (STEP == 32) tmem_ld16x2<HW>(tq + T_DB + n0 + c0 + 16, &v[16]);
                     tmem_wait_ld();
-                    if (trow) {  // partial dB; rows past the chunk's tokens add zero
-                        float val[32];
+                    {  // partial dB; rows past the chunk's tokens add zero
+                        const int n = n0 + HW * hf + c0;
+                        float val[STEP];
 #pragma unroll
-                        for (int u = 0; u < 32; ++u) val[u] = (ok && t < vc) ? __uint_as_float(v[u]) : 0.f;
-                        stage_row16(rtiles, t, n0 + c0, val);
-                        stage_row16(rtiles, t, n0 + c0 + 16, val + 16);
+                        for (int u = 0; u < STEP; ++u) val[u] = (ok && t < vc) ? __uint_as_float(v[u]) : 0.f;
+                        stage_row16(rtiles, t, n, val);
+                        if constexpr (STEP == 32) stage_row16(rtiles, t, n + 16, val + 16);
                     }
                 }
                 tc_fence_before();
@@ -1459,7 +1468,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 const float xgb = (dt > 1e-30f) ? qv / dt : 0.f;
                 // suffix sums of (r - q) over the chunk's rows u >= t: a reverse scan over
                 // the 16 rows of this quadrant, plus the totals of the later quadrants
-                float suf = (trow && t < vc) ? (rv - qv) : 0.f;
+                float suf = (t < vc) ? (rv - qv) : 0.f;
 #pragma unroll
                 for (int o = 1; o < 16; o <<= 1) {
                     const float nb = __shfl_down_sync(0xffffffffu, suf, o, 16);
@@ -1476,7 +1485,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 }
                 suf += later;
                 // d raw = sigmoid(raw + delta_init) d delta, sigmoid = 1 - exp(-delta)
-                if (ok && t < vc)
+                if (ok && hf == 0 && t < vc)
                     a.draw[(tok0 + t) * a.H + h0 + wg] = -expm1f(-dt) * (xgb - (carry + suf + kseg));
                 carry += tot;
                 if (ct != 0) mbar_arrive(&empty[s]);
