@@ -9,9 +9,9 @@
 //   reference point m = s_end / 2, f(t) = exp(s_t - m), g(s) = delta_s exp(m - s_s)):
 //     G1  CB[t, s]       = C_t . B_s                                  (M=64,  N=64,  K=N)
 //     L0[t, s]           = CB[t, s] * [s <= t]                      (epilogue, bf16)
-//     G2  Y[(h,p), t]    = sum_s g(s) x_s[(h,p)] L0[t, s]            (M=128, N=64,  K=64)
-//     G3  Y[(h,p), t]   += sum_n exp(m) H[(h,p), n] C_t[n]           (M=128, N=64,  K=N)
-//         y_t            = f(t) Y[., t]            = diagonal block + exp(s_t) H C_t
+//     G2  Y[t, (h,p)]    = sum_s L0[t, s] g(s) x_s[(h,p)]            (M=64,  N=128, K=64)
+//     G3  Y[t, (h,p)]   += sum_n C_t[n] exp(m) H[(h,p), n]           (M=64,  N=128, K=N)
+//         y_t            = f(t) Y[t, .]            = diagonal block + exp(s_t) H C_t
 //     G4  S[(h,p), n]    = sum_s g(s) x_s[(h,p)] B_s[n]              (M=128, N=N,   K=64)
 //         H             <- exp(s_end) H + exp(s_end - m) S          (fp32, registers)
 //
@@ -247,8 +247,7 @@ struct WalkLayout {
     static constexpr int OFF_L0 = 2 * STAGE;                 // 2 x 8K
     static constexpr int OFF_H = OFF_L0 + 2 * 8192;         // 2 x (N/64) x 16K
     static constexpr int HBUF = (N / 64) * 16384;
-    static constexpr int OFF_Y = OFF_H + 2 * HBUF;          // 2 x 16K
-    static constexpr int OFF_F = OFF_Y + 2 * 16384;         // f,g: [2 buf][2 head][64] x 2
+    static constexpr int OFF_F = OFF_H + 2 * HBUF;          // f,g: [2 buf][2 head][64] x 2
     static constexpr int OFF_SC = OFF_F + 2 * 2 * 2 * 64 * 4;  // scalars [2 buf][2 head][4]
     static constexpr int OFF_RED = OFF_SC + 2 * 2 * 4 * 4;     // [8]
     static constexpr int OFF_BAR = OFF_RED + 64;
@@ -257,18 +256,18 @@ struct WalkLayout {
     static constexpr int TOTAL = OFF_MISC + 16 + 1024;  // + alignment slack
 };
 
-// TMEM columns: D1 (CB^T) 2 x 64 | Y 2 x 64 | S 2 x N
+// TMEM columns: D1 (CB^T, M=64) 2 x 64 | Y (M=64) 2 x 128 | S (M=128) N.  S has one
+// buffer: the state update of chunk c always precedes the scaling of chunk c + 1,
+// which G4 of chunk c + 1 waits for.
 __device__ __forceinline__ uint32_t col_d1(int b) { return b * 64; }
-__device__ __forceinline__ uint32_t col_y(int b) { return 128 + b * 64; }
-template <int N>
-__device__ __forceinline__ uint32_t col_s(int b) { return 256 + b * N; }
+__device__ __forceinline__ uint32_t col_y(int b) { return 128 + b * 128; }
+constexpr uint32_t kColS = 384;
 
 template <int N>
 __global__ void __launch_bounds__(kWalkThreads, 1)
     tc_fwd_walk_kernel(const __grid_constant__ CUtensorMap map_x,
                        const __grid_constant__ CUtensorMap map_b,
-                       const __grid_constant__ CUtensorMap map_c,
-                       const __grid_constant__ CUtensorMap map_y, Args a) {
+                       const __grid_constant__ CUtensorMap map_c, Args a) {
     using Lay = WalkLayout<N>;
     const int seg = blockIdx.x;
     const int h0 = blockIdx.y * 2;
@@ -347,8 +346,8 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
         // ------------------------------------------------ MMA issuer
         if (lane == 0) {
             const uint32_t id_cb = idesc_bf16(64, 64, 0, 0);
-            const uint32_t id_y = idesc_bf16(128, 64, 1, 0);
-            const uint32_t id_h = idesc_bf16(128, 64, 0, 0);
+            const uint32_t id_y = idesc_bf16(64, 128, 0, 1);
+            const uint32_t id_h = idesc_bf16(64, 128, 0, 0);
             const uint32_t id_s = idesc_bf16(128, N, 1, 1);
             for (int c = 0; c < nchunks; ++c) {
                 const int s = c & 1, ph = (c >> 1) & 1;
@@ -370,13 +369,13 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
                 tc_fence_after();
                 // G4: chunk state contribution (not needed after the last chunk)
                 if (!last) {
-                    if (c >= 2 && !wait_or_abort(&s_free[s], ph ^ 1, abort_flag, a.hdr)) break;
+                    if (c >= 1 && !wait_or_abort(&s_free[0], (c - 1) & 1, abort_flag, a.hdr)) break;
                     tc_fence_after();
 #pragma unroll
                     for (int k = 0; k < kQ / 16; ++k)
-                        mma_bf16(tmem + col_s<N>(s), sw128_desc(xs + k * 2048, 8192, 1024),
+                        mma_bf16(tmem + kColS, sw128_desc(xs + k * 2048, 8192, 1024),
                                  sw128_desc(bs + k * 2048, 8192, 1024), id_s, k > 0 ? 1u : 0u);
-                    mma_commit(&s_full[s]);
+                    mma_commit(&s_full[0]);
                 }
                 // G2: diagonal block
                 if (!wait_or_abort(&l0_ready[s], ph, abort_flag, a.hdr)) break;
@@ -385,18 +384,18 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
                 const uint32_t l0 = smem_u32(sm + Lay::OFF_L0 + s * 8192);
 #pragma unroll
                 for (int k = 0; k < kQ / 16; ++k)
-                    mma_bf16(tmem + col_y(s), sw128_desc(xs + k * 2048, 8192, 1024),
-                             sw128_desc(l0 + k * 32, 16, 1024), id_y, k > 0 ? 1u : 0u);
+                    mma_bf16(tmem + col_y(s), sw128_desc(l0 + k * 32, 16, 1024),
+                             sw128_desc(xs + k * 2048, 8192, 1024), id_y, k > 0 ? 1u : 0u);
                 // G3: state entering the chunk
                 if (!wait_or_abort(&h_ready[s], ph, abort_flag, a.hdr)) break;
                 tc_fence_after();
                 const uint32_t hs = smem_u32(sm + Lay::OFF_H + s * Lay::HBUF);
 #pragma unroll
                 for (int k = 0; k < N / 16; ++k) {
-                    const uint32_t ka = (k >> 2) * 16384 + (k & 3) * 32;
-                    const uint32_t kb = (k >> 2) * 8192 + (k & 3) * 32;
-                    mma_bf16(tmem + col_y(s), sw128_desc(hs + ka, 16, 1024),
-                             sw128_desc(cs + kb, 16, 1024), id_h, 1u);
+                    const uint32_t kc = (k >> 2) * 8192 + (k & 3) * 32;
+                    const uint32_t kh = (k >> 2) * 16384 + (k & 3) * 32;
+                    mma_bf16(tmem + col_y(s), sw128_desc(cs + kc, 16, 1024),
+                             sw128_desc(hs + kh, 16, 1024), id_h, 1u);
                 }
                 mma_commit(&y_full[s]);
                 mma_commit(&empty[s]);
@@ -410,18 +409,14 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
         const int r = 32 * q + lane;    // accumulator row = (head, p)
         const int rh = r >> 6, rp = r & 63;
         constexpr int NH = N / kWWG;    // state columns per warpgroup
-        constexpr int YW = kQ / kWWG;   // y columns (tokens) per warpgroup
         const int n0 = wg * NH;
+        const int tt = 16 * q + (lane & 15);  // M=64 accumulator row (token)
+        const int hf = lane >> 4;             // M=64 column half of this lane
         const uint32_t trow = tmem + ((uint32_t)(32 * q) << 16);
         // The state is kept pre-scaled for its next chunk: Hs_c = exp(m_c) H_c, so that
         //   Hs_{c+1} = exp(m_{c+1} + s_end_c / 2) (Hs_c + S_c)      (m_c = s_end_c / 2)
         // and Hs_c is directly the bf16 operand of G3.
         float Hs[NH];
-        // byte offsets of this thread's y elements inside a staging tile, by t % 8
-        uint32_t yoff[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k)
-            yoff[k] = rh * 8192 + ((((rp >> 3) ^ k) & 7) << 4) + (rp & 7) * 2;
 
         auto load_raw = [&](int cc) -> float {
             const int head = ct >> 6, t = ct & 63;
@@ -485,53 +480,35 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
                 Hs[i + 3] = v.w * sc0;
             }
         }
-        // y epilogue of chunk cc: y = f(t) Y -> staging tile -> TMA store (or direct stores
-        // on a partial chunk).  Runs one chunk behind, so the state MMA of the current
+        // y epilogue of chunk cc: y = f(t) Y, written straight from registers (warpgroup
+        // wg holds head wg / 2, p in [32 (wg % 2), 32 (wg % 2) + 32); each lane 16 of
+        // them for token tt).  Runs one chunk behind, so the state MMA of the current
         // chunk overlaps it.
         auto drain_y = [&](int cc) {
             const int s = cc & 1, ph = (cc >> 1) & 1;
             const int vc = min(kQ, si.len - cc * kQ);
             const long long tok0 = si.start + (long long)cc * kQ;
-                {
-                    const bool ok = wait_or_abort(&y_full[s], ph, abort_flag, a.hdr);
-                    tc_fence_after();
-                    if (ct == 0) tma_store_wait_read<1>();
-                    named_sync(1, kWCT);
-                    unsigned char* yst = sm + Lay::OFF_Y + s * 16384;
-                    const float* fv = fbuf + (s * 2 + rh) * 64 + wg * YW;
-                    uint32_t v[YW];
+            const bool ok = wait_or_abort(&y_full[s], ph, abort_flag, a.hdr);
+            tc_fence_after();
+            uint32_t v[16];
+            tmem_ld16x2<16>(trow + col_y(s) + 32 * wg, v);
+            tmem_wait_ld();
+            tc_fence_before();
+            mbar_arrive(&y_free[s]);
+            const int yh = wg >> 1;
+            const int yp = 32 * (wg & 1) + 16 * hf;
+            if (ok && tt < vc) {
+                const float fv = fbuf[(s * 2 + yh) * 64 + tt];
+                uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.y) +
+                                                      ((tok0 + tt) * a.H + h0 + yh) * kP + yp);
 #pragma unroll
-                    for (int j = 0; j < YW; j += 16)
-                        tmem_ld16(trow + col_y(s) + wg * YW + j, *reinterpret_cast<uint32_t(*)[16]>(&v[j]));
-                    tmem_wait_ld();
-                    tc_fence_before();
-                    mbar_arrive(&y_free[s]);
-                    if (ok) {
-                        if (vc == kQ) {
-                            unsigned char* yb = yst + wg * YW * 128;
-#pragma unroll
-                            for (int u = 0; u < YW; ++u)
-                                *reinterpret_cast<__nv_bfloat16*>(yb + u * 128 + yoff[u & 7]) =
-                                    __float2bfloat16_rn(__uint_as_float(v[u]) * fv[u]);
-                        } else {
-#pragma unroll
-                            for (int u = 0; u < YW; ++u) {
-                                const int t = wg * YW + u;
-                                if (t < vc)
-                                    static_cast<__nv_bfloat16*>(a.y)[((tok0 + t) * a.H + h0 + rh) * kP +
-                                                                     rp] =
-                                        __float2bfloat16_rn(__uint_as_float(v[u]) * fv[u]);
-                            }
-                        }
-                    }
-                    fence_proxy_async();
-                    named_sync(1, kWCT);
-                    if (ct == 0 && vc == kQ && ok) {
-                        tma_store_3d(&map_y, sm + Lay::OFF_Y + s * 16384, 0, h0, (int)tok0);
-                        tma_store_3d(&map_y, sm + Lay::OFF_Y + s * 16384 + 8192, 0, h0 + 1, (int)tok0);
-                        tma_store_commit();
-                    }
-                }
+                for (int e = 0; e < 16; e += 8)
+                    dst[e >> 3] = make_uint4(
+                        pack_bf16(fv * __uint_as_float(v[e]), fv * __uint_as_float(v[e + 1])),
+                        pack_bf16(fv * __uint_as_float(v[e + 2]), fv * __uint_as_float(v[e + 3])),
+                        pack_bf16(fv * __uint_as_float(v[e + 4]), fv * __uint_as_float(v[e + 5])),
+                        pack_bf16(fv * __uint_as_float(v[e + 6]), fv * __uint_as_float(v[e + 7])));
+            }
         };
 
         write_h(0);
@@ -554,46 +531,45 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
             }
             fence_proxy_async();
             mbar_arrive(&xg_ready[s]);
-            // B: L0 = CB^T masked to s <= t (lanes 0..15 hold rows t; warpgroup wg takes
-            // columns 16 wg .. 16 wg + 15)
-            {
+            // B: L0 = CB^T masked to s <= t (warpgroups 0 and 1: columns 32 wg + 16 hf ..
+            // + 15 of row tt); warpgroups 2 and 3 go on to the y epilogue
+            if (wg < 2) {
                 const bool ok = wait_or_abort(&d1_full[s], ph, abort_flag, a.hdr);
                 tc_fence_after();
-                const int t = 16 * q + lane;
-                const int cb = 16 * wg;
+                const int cb = 32 * wg + 16 * hf;
                 uint32_t v[16];
-                tmem_ld16(trow + col_d1(s) + cb, v);
+                tmem_ld16x2<16>(trow + col_d1(s) + 32 * wg, v);
                 tmem_wait_ld();
-                if (lane < 16 && ok) {
-                    unsigned char* l0 = sm + Lay::OFF_L0 + s * 8192 + t * 128;
+                if (ok) {
+                    unsigned char* l0 = sm + Lay::OFF_L0 + s * 8192 + tt * 128;
 #pragma unroll
                     for (int e = 0; e < 16; e += 8) {
                         float f[8];
 #pragma unroll
                         for (int u = 0; u < 8; ++u)
-                            f[u] = (cb + e + u <= t) ? __uint_as_float(v[e + u]) : 0.f;
-                        *reinterpret_cast<uint4*>(l0 + (((((cb + e) >> 3) ^ t) & 7) << 4)) =
+                            f[u] = (cb + e + u <= tt) ? __uint_as_float(v[e + u]) : 0.f;
+                        *reinterpret_cast<uint4*>(l0 + (((((cb + e) >> 3) ^ tt) & 7) << 4)) =
                             make_uint4(pack_bf16(f[0], f[1]), pack_bf16(f[2], f[3]),
                                        pack_bf16(f[4], f[5]), pack_bf16(f[6], f[7]));
                     }
                 }
                 tc_fence_before();
                 fence_proxy_async();
-                mbar_arrive(&l0_ready[s]);
             }
+            mbar_arrive(&l0_ready[s]);
             // y of the previous chunk (it reads the factor buffer factors(c + 1) rewrites)
             if (c > 0) drain_y(c - 1);
             // C: factors of the next chunk, state update, H operand of the next chunk
             if (!last) {
                 factors(c + 1, raw_next);
-                const bool ok = wait_or_abort(&s_full[s], ph, abort_flag, a.hdr);
+                const bool ok = wait_or_abort(&s_full[0], c & 1, abort_flag, a.hdr);
                 tc_fence_after();
                 const float gam = expf(-(scal[(s * 2 + rh) * 4 + 0] +
                                          scal[((s ^ 1) * 2 + rh) * 4 + 0]));
 #pragma unroll
                 for (int c0 = 0; c0 < NH; c0 += 16) {
                     uint32_t v[16];
-                    tmem_ld16(trow + col_s<N>(s) + n0 + c0, v);
+                    tmem_ld16(trow + kColS + n0 + c0, v);
                     tmem_wait_ld();
                     if (ok) {
 #pragma unroll
@@ -602,12 +578,11 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
                     }
                 }
                 tc_fence_before();
-                mbar_arrive(&s_free[s]);
+                mbar_arrive(&s_free[0]);
                 write_h(c + 1);
             }
         }
         drain_y(nchunks - 1);
-        if (ct == 0) tma_store_wait_all<0>();
     }
     tc_fence_before();
     __syncthreads();
@@ -1511,9 +1486,9 @@ cudaError_t set_smem(K kernel, int bytes) {
 
 template <int N>
 cudaError_t forward_n(const Prob& pb, const Args& a, Launch& L) {
-    CUtensorMap mx, mb, mc, my;
+    CUtensorMap mx, mb, mc;
     if (!make_map(&mx, a.x, pb.T, pb.H, kP) || !make_map(&mb, a.B, pb.T, pb.G, N) ||
-        !make_map(&mc, a.C, pb.T, pb.G, N) || !make_map(&my, a.y, pb.T, pb.H, kP))
+        !make_map(&mc, a.C, pb.T, pb.G, N))
         return cudaErrorInvalidValue;
     cudaError_t e = launch_seg_table(pb, a, L);
     if (e != cudaSuccess) return e;
@@ -1529,8 +1504,7 @@ cudaError_t forward_n(const Prob& pb, const Args& a, Launch& L) {
     e = set_smem(tc_fwd_walk_kernel<N>, WalkLayout<N>::TOTAL);
     if (e != cudaSuccess) return e;
     L.begin("tc_fwd_walk");
-    tc_fwd_walk_kernel<N><<<grid, kWalkThreads, WalkLayout<N>::TOTAL, L.stream>>>(mx, mb, mc, my,
-                                                                                  a);
+    tc_fwd_walk_kernel<N><<<grid, kWalkThreads, WalkLayout<N>::TOTAL, L.stream>>>(mx, mb, mc, a);
     return L.end();
 }
 
