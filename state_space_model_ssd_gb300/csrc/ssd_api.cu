@@ -151,6 +151,11 @@ Layout make_layout(const Prob& b, bool bwd) {
         l.rtok = off;
         off = align_up(off + sizeof(float) * (size_t)b.T * b.H);
     }
+    l.l0 = 0;
+    if (b.tc) {  // one 64 x 64 bf16 tile per chunk slot of every segment and group
+        l.l0 = off;
+        off = align_up(off + (size_t)8192 * b.nseg_max * (b.Ls / b.Q) * b.G);
+    }
     l.total = off;
     return l;
 }
@@ -173,6 +178,7 @@ Args make_args(const Prob& b, const Layout& l, void* ws) {
         a.dcacc = reinterpret_cast<float*>(base + l.dcacc);
         a.rtok = reinterpret_cast<float*>(base + l.rtok);
     }
+    if (l.l0) a.l0 = reinterpret_cast<unsigned char*>(base + l.l0);
     a.T = b.T;
     a.rowlen = b.rowlen;
     a.nseg_max = b.nseg_max;

@@ -46,7 +46,7 @@ struct Prob {
 
 // Byte offsets of the workspace regions.
 struct Layout {
-    size_t header, segtab, A, lam, adj, rq, rqsuf, dbacc, dcacc, rtok, total;
+    size_t header, segtab, A, lam, adj, rq, rqsuf, dbacc, dcacc, rtok, l0, total;
 };
 
 // Everything a kernel needs; passed by value.
@@ -73,6 +73,7 @@ struct Args {
     float* dbacc;   // [T][G][N] fp32
     float* dcacc;   // [T][G][N] fp32
     float* rtok;    // [T][H] fp32: dy_t . y_t per token and head (tensor-core backward)
+    unsigned char* l0;  // tensor-core path: [nseg_max][Ls / Q][G] 8 KB tiles, masked C B^T per chunk
     long long T, rowlen;
     long long nseg_max;
     int nseq, H, P, N, G, Q, Ls;

@@ -214,7 +214,7 @@ __global__ void __launch_bounds__(kStateThreads, 2)
         for (int c0 = cbase; c0 < cbase + N / 2; c0 += 16) {
             uint32_t v[16];
             tmem_ld16(tmem + ((uint32_t)(32 * q) << 16) + c0, v);
-            tmem_wait_ld();
+            tmem_wait_ld_regs<16>(v);
             if (ok) {
 #pragma unroll
                 for (int i = 0; i < 16; i += 4)
@@ -229,39 +229,171 @@ __global__ void __launch_bounds__(kStateThreads, 2)
     if (warp == 1) tmem_dealloc(tmem, N);
 }
 
+// ================================================================ masked CB^T tiles
+// L0[t, s] = (C_t . B_s) [s <= t] for every chunk of every segment and B/C group, as a
+// bf16 image of the 128-byte-swizzled K-major operand layout (8 KB: row t at t * 128,
+// 16-byte chunk j of it at ((j ^ t) & 7) * 16).  The tile does not depend on the head,
+// so it is made once here and copied into each walk's shared memory as it is: the
+// forward walk reads it as the A operand of the diagonal block (rows t, K = s), the
+// dx/dB walk reads the same bytes as the MN-major A operand of L0^T (rows u, K = t).
+// Warps: 0 = TMA producer, 1 = MMA issuer, 2..5 = masking epilogue.  Each CTA takes
+// kL0Chunks consecutive chunks of one segment.
+constexpr int kL0Threads = 192;
+constexpr int kL0Chunks = 4;
+
+template <int N>
+__global__ void __launch_bounds__(kL0Threads)
+    tc_l0_kernel(const __grid_constant__ CUtensorMap map_b,
+                 const __grid_constant__ CUtensorMap map_c, Args a) {
+    const int cps = a.Ls / kQ;                       // chunk slots per segment
+    const int parts = (cps + kL0Chunks - 1) / kL0Chunks;
+    const int seg = blockIdx.x / parts;
+    const int g = blockIdx.y;
+    if (seg >= a.hdr->nseg) return;
+    const SegInfo si = a.segtab[seg];
+    const int c0 = (blockIdx.x % parts) * kL0Chunks;
+    const int nloc = min(kL0Chunks, (si.len + kQ - 1) / kQ - c0);
+    if (nloc <= 0) return;
+    constexpr int STAGE = 2 * N * 128;  // C | B
+
+    extern __shared__ __align__(1024) unsigned char smraw[];
+    unsigned char* sm = reinterpret_cast<unsigned char*>(
+        (reinterpret_cast<uintptr_t>(smraw) + 1023) & ~(uintptr_t)1023);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + 2 * STAGE);
+    uint64_t* full = bars + 0;    // [2]
+    uint64_t* empty = bars + 2;   // [2]
+    uint64_t* tfull = bars + 4;   // [2]
+    uint64_t* tfree = bars + 6;   // [2]
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 8);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tslot + 1);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    if (tid == 0) {
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], 1);
+            mbar_init(&tfull[i], 1);
+            mbar_init(&tfree[i], 128);
+        }
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(tslot, 128);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tslot;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            for (int j = 0; j < nloc; ++j) {
+                const int s = j & 1;
+                if (j >= 2 && !wait_or_abort(&empty[s], ((j >> 1) - 1) & 1, abort_flag, a.hdr))
+                    break;
+                unsigned char* st = sm + s * STAGE;
+                const int tok = (int)(si.start + (long long)(c0 + j) * kQ);
+                mbar_expect_tx(&full[s], STAGE);
+                for (int nb = 0; nb < N / 64; ++nb) {
+                    tma_load_3d(st + nb * 8192, &map_c, &full[s], nb * 64, g, tok);
+                    tma_load_3d(st + N * 128 + nb * 8192, &map_b, &full[s], nb * 64, g, tok);
+                }
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            const uint32_t id = idesc_bf16(64, 64, 0, 0);
+            for (int j = 0; j < nloc; ++j) {
+                const int s = j & 1, ph = (j >> 1) & 1;
+                if (!wait_or_abort(&full[s], ph, abort_flag, a.hdr)) break;
+                if (j >= 2 && !wait_or_abort(&tfree[s], ph ^ 1, abort_flag, a.hdr)) break;
+                tc_fence_after();
+                const uint32_t cs = smem_u32(sm + s * STAGE), bs = cs + N * 128;
+#pragma unroll
+                for (int k = 0; k < N / 16; ++k) {
+                    const uint32_t koff = (k >> 2) * 8192 + (k & 3) * 32;
+                    mma_bf16(tmem + s * 64, sw128_desc(cs + koff, 16, 1024),
+                             sw128_desc(bs + koff, 16, 1024), id, k > 0 ? 1u : 0u);
+                }
+                mma_commit(&tfull[s]);
+                mma_commit(&empty[s]);
+            }
+        }
+    } else {
+        // row tt of the tile; lane half hf holds columns 32 hf .. 32 hf + 31
+        const int q = warp & 3;
+        const int tt = 16 * q + (lane & 15), hf = lane >> 4;
+        const uint32_t trow = tmem + ((uint32_t)(32 * q) << 16);
+        for (int j = 0; j < nloc; ++j) {
+            const int s = j & 1, ph = (j >> 1) & 1;
+            const bool ok = wait_or_abort(&tfull[s], ph, abort_flag, a.hdr);
+            tc_fence_after();
+            uint32_t v[32];
+            tmem_ld16x2<32>(trow + s * 64, &v[0]);
+            tmem_ld16x2<32>(trow + s * 64 + 16, &v[16]);
+            tmem_wait_ld_regs<32>(v);
+            tc_fence_before();
+            mbar_arrive(&tfree[s]);
+            if (!ok) continue;
+            unsigned char* tile =
+                a.l0 + (((long long)seg * cps + c0 + j) * a.G + g) * 8192 + tt * 128;
+#pragma unroll
+            for (int e0 = 0; e0 < 32; e0 += 8) {
+                const int e = 32 * hf + e0;
+                float f[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) f[u] = (e + u <= tt) ? __uint_as_float(v[e0 + u]) : 0.f;
+                *reinterpret_cast<uint4*>(tile + ((((e >> 3) ^ tt) & 7) << 4)) =
+                    make_uint4(pack_bf16(f[0], f[1]), pack_bf16(f[2], f[3]), pack_bf16(f[4], f[5]),
+                               pack_bf16(f[6], f[7]));
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) tmem_dealloc(tmem, 128);
+}
+
+template <int N>
+constexpr int l0_smem_bytes() {
+    return 2 * (2 * N * 128) + 8 * 8 + 16 + 1024;
+}
+
 // ================================================================ chunk walk
-// Warps: 0 = TMA producer, 1 = MMA issuer, 2.. = compute (kWWG warpgroups of four
-// warps; each warpgroup covers the 128 TMEM lanes once and takes 1/kWWG of the
-// columns of every accumulator).
+// Warps: 0 = TMA producer (x, B, C and the chunk's L0 tile), 1 = MMA issuer, 2..17 =
+// four compute warpgroups, each with its own task so that the tasks of neighbouring
+// chunks overlap:
+//   warpgroup 0     factors of the next chunk, x -> g x of the current one;
+//   warpgroup 1     the y epilogue;
+//   warpgroups 2-3  the state update Hs <- gamma (Hs + S) and the G3 operand.
+// The groups hand work to each other and to the MMA warp through mbarriers only.
 constexpr int kCT = 256;  // compute threads of the backward walks (two warpgroups)
-// The forward walk runs four compute warpgroups: the per-chunk epilogues are
-// latency-bound chains, and more warps per scheduler hide their latency.
-constexpr int kWWG = 4;
-constexpr int kWCT = 128 * kWWG;
-constexpr int kWalkThreads = 64 + kWCT;
+constexpr int kWalkThreads = 64 + 4 * 128;
+constexpr int kFS = 4;    // factor slots (chunk c uses slot c % kFS)
 
 template <int N>
 struct WalkLayout {
-    static constexpr int STAGE = 16384 + 2 * N * 128;  // X h0 | X h1 | B | C
+    static constexpr int STAGE = 16384 + 2 * N * 128 + 8192;  // X h0 | X h1 | B | C | L0
+    static constexpr int L0_IN_STAGE = 16384 + 2 * N * 128;
     static constexpr int OFF_STAGE = 0;
-    static constexpr int OFF_L0 = 2 * STAGE;                 // 2 x 8K
-    static constexpr int OFF_H = OFF_L0 + 2 * 8192;         // 2 x (N/64) x 16K
+    static constexpr int OFF_H = 2 * STAGE;                 // 2 x (N/64) x 16K
     static constexpr int HBUF = (N / 64) * 16384;
-    static constexpr int OFF_F = OFF_H + 2 * HBUF;          // f,g: [2 buf][2 head][64] x 2
-    static constexpr int OFF_SC = OFF_F + 2 * 2 * 2 * 64 * 4;  // scalars [2 buf][2 head][4]
-    static constexpr int OFF_RED = OFF_SC + 2 * 2 * 4 * 4;     // [8]
+    static constexpr int OFF_F = OFF_H + 2 * HBUF;          // f, g: [slot][head][64] each
+    static constexpr int OFF_SC = OFF_F + 2 * kFS * 2 * 64 * 4;  // half: [slot][head][4]
+    static constexpr int OFF_RED = OFF_SC + kFS * 2 * 4 * 4;     // [4]
     static constexpr int OFF_BAR = OFF_RED + 64;
-    static constexpr int NBAR = 2 * 11;
+    static constexpr int NBAR = 32;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr int TOTAL = OFF_MISC + 16 + 1024;  // + alignment slack
 };
 
-// TMEM columns: D1 (CB^T, M=64) 2 x 64 | Y (M=64) 2 x 128 | S (M=128) N.  S has one
-// buffer: the state update of chunk c always precedes the scaling of chunk c + 1,
-// which G4 of chunk c + 1 waits for.
-__device__ __forceinline__ uint32_t col_d1(int b) { return b * 64; }
-__device__ __forceinline__ uint32_t col_y(int b) { return 128 + b * 128; }
-constexpr uint32_t kColS = 384;
+// TMEM columns: Y (M=64) 2 x 128 | state (M=128) N.  The state lives in TMEM: G4 of
+// chunk c adds S_c onto Hs_c there, the state warps turn the sum into Hs_{c+1} in
+// place, and G4 of chunk c + 1 waits for that.
+__device__ __forceinline__ uint32_t col_y(int b) { return b * 128; }
+constexpr uint32_t kColS = 256;
 
 template <int N>
 __global__ void __launch_bounds__(kWalkThreads, 1)
@@ -279,21 +411,22 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
     extern __shared__ __align__(1024) unsigned char smraw[];
     unsigned char* sm = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smraw) + 1023) & ~(uintptr_t)1023);
-    float* fbuf = reinterpret_cast<float*>(sm + Lay::OFF_F);   // [buf][head][64]
-    float* gbuf = fbuf + 2 * 2 * 64;                           // [buf][head][64]
-    float* scal = reinterpret_cast<float*>(sm + Lay::OFF_SC);  // [buf][head][4]: e_end, k, hs, -
+    float* fbuf = reinterpret_cast<float*>(sm + Lay::OFF_F);   // [slot][head][64]
+    float* gbuf = fbuf + kFS * 2 * 64;                         // [slot][head][64]
+    float* scal = reinterpret_cast<float*>(sm + Lay::OFF_SC);  // [slot][head][4]: half
     float* red = reinterpret_cast<float*>(sm + Lay::OFF_RED);
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + Lay::OFF_BAR);
-    uint64_t* full = bars + 0;       // [2] TMA stage landed
-    uint64_t* empty = bars + 2;      // [2] stage consumed by the MMAs
-    uint64_t* d1_full = bars + 4;    // [2]
-    uint64_t* xg_ready = bars + 6;   // [2]
-    uint64_t* l0_ready = bars + 8;   // [2]
-    uint64_t* s_full = bars + 10;    // [2]
-    uint64_t* s_free = bars + 12;    // [2]
-    uint64_t* y_full = bars + 14;    // [2]
-    uint64_t* y_free = bars + 16;    // [2]
-    uint64_t* h_ready = bars + 18;   // [2]
+    uint64_t* full = bars + 0;        // [2] TMA stage landed
+    uint64_t* empty = bars + 2;       // [2] stage consumed by the MMAs
+    uint64_t* xg_ready = bars + 6;    // [2] x scaled in place (warpgroup 0)
+    uint64_t* s_full = bars + 10;     // S accumulated
+    uint64_t* s_free = bars + 11;     // S read by the state warps
+    uint64_t* y_full = bars + 12;     // [2] Y accumulated
+    uint64_t* y_free = bars + 14;     // [2] Y read by warpgroup 1
+    uint64_t* h_ready = bars + 16;    // [2] G3 operand written (state warps)
+    uint64_t* h_free = bars + 18;     // [2] G3 operand read by the MMAs
+    uint64_t* fac_full = bars + 20;   // [kFS] factors of a chunk written (warpgroup 0)
+    uint64_t* fac_empty = bars + 24;  // [kFS] factors of a chunk no longer needed
     uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + Lay::OFF_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tslot + 1);
 
@@ -302,14 +435,17 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
         for (int i = 0; i < 2; ++i) {
             mbar_init(&full[i], 1);
             mbar_init(&empty[i], 1);
-            mbar_init(&d1_full[i], 1);
-            mbar_init(&xg_ready[i], kWCT);
-            mbar_init(&l0_ready[i], kWCT);
-            mbar_init(&s_full[i], 1);
-            mbar_init(&s_free[i], kWCT);
+            mbar_init(&xg_ready[i], 128);
             mbar_init(&y_full[i], 1);
-            mbar_init(&y_free[i], kWCT);
-            mbar_init(&h_ready[i], kWCT);
+            mbar_init(&y_free[i], 128);
+            mbar_init(&h_ready[i], 256);
+            mbar_init(&h_free[i], 1);
+        }
+        mbar_init(s_full, 1);
+        mbar_init(s_free, 256);
+        for (int i = 0; i < kFS; ++i) {
+            mbar_init(&fac_full[i], 128);
+            mbar_init(&fac_empty[i], 128 + 256);
         }
         *abort_flag = 0;
         fence_mbar_init();
@@ -326,6 +462,7 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
     if (warp == 0) {
         // ------------------------------------------------ TMA producer
         if (lane == 0) {
+            const int cps = a.Ls / kQ;
             for (int c = 0; c < nchunks; ++c) {
                 const int s = c & 1;
                 if (c >= 2 && !wait_or_abort(&empty[s], ((c >> 1) - 1) & 1, abort_flag, a.hdr))
@@ -340,12 +477,13 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
                     tma_load_3d(st + 16384 + N * 128 + nb * 8192, &map_c, &full[s], nb * 64, g,
                                 tok);
                 }
+                bulk_load(st + Lay::L0_IN_STAGE,
+                          a.l0 + (((long long)seg * cps + c) * a.G + g) * 8192, 8192, &full[s]);
             }
         }
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer
         if (lane == 0) {
-            const uint32_t id_cb = idesc_bf16(64, 64, 0, 0);
             const uint32_t id_y = idesc_bf16(64, 128, 0, 1);
             const uint32_t id_h = idesc_bf16(64, 128, 0, 0);
             const uint32_t id_s = idesc_bf16(128, N, 1, 1);
@@ -357,31 +495,22 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
                 const uint32_t xs = smem_u32(sm + Lay::OFF_STAGE + s * Lay::STAGE);
                 const uint32_t bs = xs + 16384;
                 const uint32_t cs = bs + N * 128;
-                // G1: CB^T (M = 64 rows t, N = 64 columns s, K = N)
-#pragma unroll
-                for (int k = 0; k < N / 16; ++k) {
-                    const uint32_t koff = (k >> 2) * 8192 + (k & 3) * 32;
-                    mma_bf16(tmem + col_d1(s), sw128_desc(cs + koff, 16, 1024),
-                             sw128_desc(bs + koff, 16, 1024), id_cb, k > 0 ? 1u : 0u);
-                }
-                mma_commit(&d1_full[s]);
+                const uint32_t l0 = xs + Lay::L0_IN_STAGE;
                 if (!wait_or_abort(&xg_ready[s], ph, abort_flag, a.hdr)) break;
                 tc_fence_after();
-                // G4: chunk state contribution (not needed after the last chunk)
+                // G4: Hs_c + S_c in the state columns (not needed after the last chunk)
                 if (!last) {
-                    if (c >= 1 && !wait_or_abort(&s_free[0], (c - 1) & 1, abort_flag, a.hdr)) break;
+                    if (!wait_or_abort(s_free, c & 1, abort_flag, a.hdr)) break;
                     tc_fence_after();
 #pragma unroll
                     for (int k = 0; k < kQ / 16; ++k)
                         mma_bf16(tmem + kColS, sw128_desc(xs + k * 2048, 8192, 1024),
-                                 sw128_desc(bs + k * 2048, 8192, 1024), id_s, k > 0 ? 1u : 0u);
-                    mma_commit(&s_full[0]);
+                                 sw128_desc(bs + k * 2048, 8192, 1024), id_s, 1u);
+                    mma_commit(s_full);
                 }
                 // G2: diagonal block
-                if (!wait_or_abort(&l0_ready[s], ph, abort_flag, a.hdr)) break;
                 if (c >= 2 && !wait_or_abort(&y_free[s], ph ^ 1, abort_flag, a.hdr)) break;
                 tc_fence_after();
-                const uint32_t l0 = smem_u32(sm + Lay::OFF_L0 + s * 8192);
 #pragma unroll
                 for (int k = 0; k < kQ / 16; ++k)
                     mma_bf16(tmem + col_y(s), sw128_desc(l0 + k * 32, 16, 1024),
@@ -398,191 +527,190 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
                              sw128_desc(hs + kh, 16, 1024), id_h, 1u);
                 }
                 mma_commit(&y_full[s]);
+                mma_commit(&h_free[s]);
                 mma_commit(&empty[s]);
             }
         }
     } else {
-        // ------------------------------------------------ compute warpgroups
-        const int ct = tid - 64;        // 0..255
-        const int wg = ct >> 7;         // 0 .. kWWG - 1
+        const int ct = tid - 64;        // 0..511
+        const int wg = ct >> 7;         // compute warpgroup: task
         const int q = warp & 3;         // TMEM lane quadrant
-        const int r = 32 * q + lane;    // accumulator row = (head, p)
-        const int rh = r >> 6, rp = r & 63;
-        constexpr int NH = N / kWWG;    // state columns per warpgroup
-        const int n0 = wg * NH;
-        const int tt = 16 * q + (lane & 15);  // M=64 accumulator row (token)
-        const int hf = lane >> 4;             // M=64 column half of this lane
         const uint32_t trow = tmem + ((uint32_t)(32 * q) << 16);
-        // The state is kept pre-scaled for its next chunk: Hs_c = exp(m_c) H_c, so that
-        //   Hs_{c+1} = exp(m_{c+1} + s_end_c / 2) (Hs_c + S_c)      (m_c = s_end_c / 2)
-        // and Hs_c is directly the bf16 operand of G3.
-        float Hs[NH];
-
-        auto load_raw = [&](int cc) -> float {
-            const int head = ct >> 6, t = ct & 63;
-            if (ct >= 128 || cc >= nchunks || t >= si.len - cc * kQ) return 0.f;
-            return a.raw[(si.start + (long long)cc * kQ + t) * a.H + h0 + head];
-        };
-        // chunk factors for chunk cc into buffer cc & 1 (threads 0..127 compute):
-        // f(t) = exp(s_t - m), g(t) = delta_t exp(m - s_t), half = -m = (sum of delta) / 2
-        auto factors = [&](int cc, float rawv) {
-            named_sync(1, kWCT);
-            if (ct < 128) {
-                const int head = ct >> 6, t = ct & 63;
+        if (wg == 0) {
+            // ------------------------------------------------ factors, x -> g x
+            // thread (head, t): f(t) = exp(s_t - m), g(t) = delta_t exp(m - s_t),
+            // half = -m = (sum of delta) / 2, for chunk cc into slot cc % kFS
+            const int head = ct >> 6, t = ct & 63, hw = (ct >> 5) & 1;
+            auto load_raw = [&](int cc) -> float {
+                if (cc >= nchunks || t >= si.len - cc * kQ) return 0.f;
+                return a.raw[(si.start + (long long)cc * kQ + t) * a.H + h0 + head];
+            };
+            auto factors = [&](int cc, float rawv) {
                 const int vc = min(kQ, si.len - cc * kQ);
                 float d = 0.f;
                 if (t < vc) d = softplus_f(rawv + a.delta_init);
                 float inc = warp_scan(d, lane);
-                const int hw = (ct >> 5) & 1;
                 if (lane == 31) red[head * 2 + hw] = inc;
                 named_sync(2 + head, 64);
                 if (hw) inc += red[head * 2];
                 const float send = red[head * 2] + red[head * 2 + 1];  // sum of delta
                 const float half = 0.5f * send;
-                const int b = cc & 1;
-                fbuf[(b * 2 + head) * 64 + t] = expf(half - inc);
-                gbuf[(b * 2 + head) * 64 + t] = d * expf(inc - half);
+                const int sl = cc % kFS;
+                fbuf[(sl * 2 + head) * 64 + t] = expf(half - inc);
+                gbuf[(sl * 2 + head) * 64 + t] = d * expf(inc - half);
                 if (t == 0) {
-                    scal[(b * 2 + head) * 4 + 0] = half;
+                    scal[(sl * 2 + head) * 4 + 0] = half;
                     if (send > kMaxChunkDecay) set_status(a.hdr, SSD_ERR_DEVICE);
                 }
-            }
-            named_sync(1, kWCT);
-        };
-        // bf16(Hs) -> the G3 operand buffer for chunk cc (K-major, 128-byte swizzle)
-        auto write_h = [&](int cc) {
-            unsigned char* hb = sm + Lay::OFF_H + (cc & 1) * Lay::HBUF + r * 128;
+                // every g of the chunk is written before this warpgroup scales x with it
+                // (each thread reads rows other threads wrote), and red is read before the
+                // next call rewrites it
+                named_sync(4, 128);
+                mbar_arrive(&fac_full[sl]);
+            };
+            factors(0, load_raw(0));
+            for (int c = 0; c < nchunks; ++c) {
+                const int s = c & 1, ph = (c >> 1) & 1;
+                const float raw_next = load_raw(c + 1);
+                if (wait_or_abort(&full[s], ph, abort_flag, a.hdr)) {
+                    uint4* xs = reinterpret_cast<uint4*>(sm + Lay::OFF_STAGE + s * Lay::STAGE);
+                    const float* gv = gbuf + (c % kFS) * 128;
 #pragma unroll
-            for (int c8 = 0; c8 < NH; c8 += 8) {
-                const int n = n0 + c8;
-                const uint4 v = make_uint4(pack_bf16(Hs[c8], Hs[c8 + 1]),
-                                           pack_bf16(Hs[c8 + 2], Hs[c8 + 3]),
-                                           pack_bf16(Hs[c8 + 4], Hs[c8 + 5]),
-                                           pack_bf16(Hs[c8 + 6], Hs[c8 + 7]));
-                *reinterpret_cast<uint4*>(hb + (n >> 6) * 16384 +
-                                          (((((n & 63) >> 3) ^ r) & 7) << 4)) = v;
-            }
-            fence_proxy_async();
-            mbar_arrive(&h_ready[cc & 1]);
-        };
-
-        // prologue: state entering the segment, factors of chunk 0
-        factors(0, load_raw(0));
-        {
-            const float sc0 = expf(-scal[(0 * 2 + rh) * 4 + 0]);  // exp(m_0)
-            const float* Hin = a.A + (((long long)seg * a.H + h0 + rh) * kP + rp) * N + n0;
-#pragma unroll
-            for (int i = 0; i < NH; i += 4) {
-                const float4 v = *reinterpret_cast<const float4*>(Hin + i);
-                Hs[i] = v.x * sc0;
-                Hs[i + 1] = v.y * sc0;
-                Hs[i + 2] = v.z * sc0;
-                Hs[i + 3] = v.w * sc0;
-            }
-        }
-        // y epilogue of chunk cc: y = f(t) Y, written straight from registers (warpgroup
-        // wg holds head wg / 2, p in [32 (wg % 2), 32 (wg % 2) + 32); each lane 16 of
-        // them for token tt).  Runs one chunk behind, so the state MMA of the current
-        // chunk overlaps it.
-        auto drain_y = [&](int cc) {
-            const int s = cc & 1, ph = (cc >> 1) & 1;
-            const int vc = min(kQ, si.len - cc * kQ);
-            const long long tok0 = si.start + (long long)cc * kQ;
-            const bool ok = wait_or_abort(&y_full[s], ph, abort_flag, a.hdr);
-            tc_fence_after();
-            uint32_t v[16];
-            tmem_ld16x2<16>(trow + col_y(s) + 32 * wg, v);
-            tmem_wait_ld();
-            tc_fence_before();
-            mbar_arrive(&y_free[s]);
-            const int yh = wg >> 1;
-            const int yp = 32 * (wg & 1) + 16 * hf;
-            if (ok && tt < vc) {
-                const float fv = fbuf[(s * 2 + yh) * 64 + tt];
-                uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.y) +
-                                                      ((tok0 + tt) * a.H + h0 + yh) * kP + yp);
-#pragma unroll
-                for (int e = 0; e < 16; e += 8)
-                    dst[e >> 3] = make_uint4(
-                        pack_bf16(fv * __uint_as_float(v[e]), fv * __uint_as_float(v[e + 1])),
-                        pack_bf16(fv * __uint_as_float(v[e + 2]), fv * __uint_as_float(v[e + 3])),
-                        pack_bf16(fv * __uint_as_float(v[e + 4]), fv * __uint_as_float(v[e + 5])),
-                        pack_bf16(fv * __uint_as_float(v[e + 6]), fv * __uint_as_float(v[e + 7])));
-            }
-        };
-
-        write_h(0);
-
-        for (int c = 0; c < nchunks; ++c) {
-            const int s = c & 1, ph = (c >> 1) & 1;
-            const bool last = (c == nchunks - 1);
-            unsigned char* st = sm + Lay::OFF_STAGE + s * Lay::STAGE;
-            const float raw_next = load_raw(c + 1);  // consumed by factors(c + 1) below
-            // A: x -> g(s) x in place (the operand of G2 and G4)
-            const bool have = wait_or_abort(&full[s], ph, abort_flag, a.hdr);
-            if (have) {
-                uint4* xs = reinterpret_cast<uint4*>(st);
-                const float* gv = gbuf + s * 128;
-#pragma unroll
-                for (int i = 0; i < 1024 / kWCT; ++i) {
-                    const int idx = ct + kWCT * i;  // 0..1023: head = idx / 512, row = (idx / 8) % 64
-                    xs[idx] = scale_chunk(xs[idx], gv[((idx >> 9) << 6) + ((idx >> 3) & 63)]);
-                }
-            }
-            fence_proxy_async();
-            mbar_arrive(&xg_ready[s]);
-            // B: L0 = CB^T masked to s <= t (warpgroups 0 and 1: columns 32 wg + 16 hf ..
-            // + 15 of row tt); warpgroups 2 and 3 go on to the y epilogue
-            if (wg < 2) {
-                const bool ok = wait_or_abort(&d1_full[s], ph, abort_flag, a.hdr);
-                tc_fence_after();
-                const int cb = 32 * wg + 16 * hf;
-                uint32_t v[16];
-                tmem_ld16x2<16>(trow + col_d1(s) + 32 * wg, v);
-                tmem_wait_ld();
-                if (ok) {
-                    unsigned char* l0 = sm + Lay::OFF_L0 + s * 8192 + tt * 128;
-#pragma unroll
-                    for (int e = 0; e < 16; e += 8) {
-                        float f[8];
-#pragma unroll
-                        for (int u = 0; u < 8; ++u)
-                            f[u] = (cb + e + u <= tt) ? __uint_as_float(v[e + u]) : 0.f;
-                        *reinterpret_cast<uint4*>(l0 + (((((cb + e) >> 3) ^ tt) & 7) << 4)) =
-                            make_uint4(pack_bf16(f[0], f[1]), pack_bf16(f[2], f[3]),
-                                       pack_bf16(f[4], f[5]), pack_bf16(f[6], f[7]));
+                    for (int i = 0; i < 8; ++i) {
+                        const int idx = ct + 128 * i;  // head = idx / 512, row = (idx / 8) % 64
+                        xs[idx] = scale_chunk(xs[idx], gv[((idx >> 9) << 6) + ((idx >> 3) & 63)]);
                     }
                 }
-                tc_fence_before();
                 fence_proxy_async();
+                mbar_arrive(&xg_ready[s]);
+                if (c + 1 < nchunks) {
+                    const int cn = c + 1;
+                    if (cn >= kFS)
+                        wait_or_abort(&fac_empty[cn % kFS], ((cn / kFS) - 1) & 1, abort_flag,
+                                      a.hdr);
+                    factors(cn, raw_next);
+                }
             }
-            mbar_arrive(&l0_ready[s]);
-            // y of the previous chunk (it reads the factor buffer factors(c + 1) rewrites)
-            if (c > 0) drain_y(c - 1);
-            // C: factors of the next chunk, state update, H operand of the next chunk
-            if (!last) {
-                factors(c + 1, raw_next);
-                const bool ok = wait_or_abort(&s_full[0], c & 1, abort_flag, a.hdr);
+        } else if (wg == 1) {
+            // ------------------------------------------------ the y epilogue
+            const int tt = 16 * q + (lane & 15);  // M=64 accumulator row (token)
+            const int hf = lane >> 4;             // M=64 column half of this lane
+            // y of chunk cc: lane half hf holds head hf, p = 0..63 of token tt
+            auto drain_y = [&](int cc) {
+                const int s = cc & 1, ph = (cc >> 1) & 1, sl = cc % kFS;
+                const int vc = min(kQ, si.len - cc * kQ);
+                const long long tok0 = si.start + (long long)cc * kQ;
+                bool ok = wait_or_abort(&fac_full[sl], (cc / kFS) & 1, abort_flag, a.hdr);
+                ok = wait_or_abort(&y_full[s], ph, abort_flag, a.hdr) && ok;
                 tc_fence_after();
-                const float gam = expf(-(scal[(s * 2 + rh) * 4 + 0] +
-                                         scal[((s ^ 1) * 2 + rh) * 4 + 0]));
+                const float fv = fbuf[(sl * 2 + hf) * 64 + tt];
+                mbar_arrive(&fac_empty[sl]);
+                uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.y) +
+                                                      ((tok0 + tt) * a.H + h0 + hf) * kP);
 #pragma unroll
-                for (int c0 = 0; c0 < NH; c0 += 16) {
-                    uint32_t v[16];
-                    tmem_ld16(trow + kColS + n0 + c0, v);
-                    tmem_wait_ld();
-                    if (ok) {
+                for (int j = 0; j < 64; j += 32) {
+                    uint32_t v[32];
+                    tmem_ld16x2<64>(trow + col_y(s) + j, &v[0]);
+                    tmem_ld16x2<64>(trow + col_y(s) + j + 16, &v[16]);
+                    tmem_wait_ld_regs<32>(v);
+                    if (j == 32) {
+                        tc_fence_before();
+                        mbar_arrive(&y_free[s]);
+                    }
+                    if (ok && tt < vc) {
 #pragma unroll
-                        for (int u = 0; u < 16; ++u)
-                            Hs[c0 + u] = gam * (Hs[c0 + u] + __uint_as_float(v[u]));
+                        for (int e = 0; e < 32; e += 8)
+                            dst[(j + e) >> 3] = make_uint4(
+                                pack_bf16(fv * __uint_as_float(v[e]), fv * __uint_as_float(v[e + 1])),
+                                pack_bf16(fv * __uint_as_float(v[e + 2]), fv * __uint_as_float(v[e + 3])),
+                                pack_bf16(fv * __uint_as_float(v[e + 4]), fv * __uint_as_float(v[e + 5])),
+                                pack_bf16(fv * __uint_as_float(v[e + 6]), fv * __uint_as_float(v[e + 7])));
                     }
                 }
+            };
+            for (int c = 0; c < nchunks; ++c) drain_y(c);
+        } else {
+            // ------------------------------------------------ state chain
+            // The state is kept pre-scaled for its next chunk, Hs_c = exp(m_c) H_c, in the
+            // TMEM state columns (row r = (head, p), columns [n0, n0 + N / 2) per
+            // warpgroup).  G4 leaves Hs_c + S_c there; this group rewrites it as
+            //   Hs_{c+1} = exp(m_{c+1} + s_end_c / 2) (Hs_c + S_c)      (m_c = s_end_c / 2)
+            // and stores bf16(Hs_{c+1}), the G3 operand of the next chunk.
+            constexpr int NH = N / 2;
+            const int r = 32 * q + lane;
+            const int rh = r >> 6, rp = r & 63;
+            const int n0 = (wg - 2) * NH;
+            const uint32_t tcol = trow + kColS + n0;
+            // bf16 of 32 state values (columns n0 + c0 ..) into the G3 operand of chunk cc
+            auto write_h32 = [&](int cc, int c0, const float* h) {
+                unsigned char* hb = sm + Lay::OFF_H + (cc & 1) * Lay::HBUF + r * 128;
+#pragma unroll
+                for (int c8 = 0; c8 < 32; c8 += 8) {
+                    const int n = n0 + c0 + c8;
+                    const uint4 v = make_uint4(pack_bf16(h[c8], h[c8 + 1]),
+                                               pack_bf16(h[c8 + 2], h[c8 + 3]),
+                                               pack_bf16(h[c8 + 4], h[c8 + 5]),
+                                               pack_bf16(h[c8 + 6], h[c8 + 7]));
+                    *reinterpret_cast<uint4*>(hb + (n >> 6) * 16384 +
+                                              (((((n & 63) >> 3) ^ r) & 7) << 4)) = v;
+                }
+            };
+            {
+                wait_or_abort(&fac_full[0], 0, abort_flag, a.hdr);
+                const float sc0 = expf(-scal[(0 * 2 + rh) * 4 + 0]);  // exp(m_0)
+                const float* Hin = a.A + (((long long)seg * a.H + h0 + rh) * kP + rp) * N + n0;
+#pragma unroll
+                for (int c0 = 0; c0 < NH; c0 += 32) {
+                    float h[32];
+#pragma unroll
+                    for (int i = 0; i < 32; i += 4) {
+                        const float4 v = *reinterpret_cast<const float4*>(Hin + c0 + i);
+                        h[i] = v.x * sc0;
+                        h[i + 1] = v.y * sc0;
+                        h[i + 2] = v.z * sc0;
+                        h[i + 3] = v.w * sc0;
+                    }
+                    tmem_st16(tcol + c0, reinterpret_cast<const uint32_t*>(&h[0]));
+                    tmem_st16(tcol + c0 + 16, reinterpret_cast<const uint32_t*>(&h[16]));
+                    write_h32(0, c0, h);
+                }
+                tmem_wait_st();
                 tc_fence_before();
-                mbar_arrive(&s_free[0]);
-                write_h(c + 1);
+                mbar_arrive(s_free);
+                fence_proxy_async();
+                mbar_arrive(&h_ready[0]);
             }
+            for (int c = 0; c + 1 < nchunks; ++c) {
+                const int sl = c % kFS, sn = (c + 1) % kFS;
+                bool ok = wait_or_abort(&fac_full[sn], ((c + 1) / kFS) & 1, abort_flag, a.hdr);
+                const float gam = expf(-(scal[(sl * 2 + rh) * 4] + scal[(sn * 2 + rh) * 4]));
+                // the G3 operand buffer of chunk c + 1 was last read by G3 of chunk c - 1
+                if (c >= 1)
+                    wait_or_abort(&h_free[(c + 1) & 1], ((c - 1) >> 1) & 1, abort_flag, a.hdr);
+                ok = wait_or_abort(s_full, c & 1, abort_flag, a.hdr) && ok;
+                tc_fence_after();
+#pragma unroll
+                for (int c0 = 0; c0 < NH; c0 += 32) {
+                    uint32_t v[32];
+                    tmem_ld16(tcol + c0, *reinterpret_cast<uint32_t(*)[16]>(&v[0]));
+                    tmem_ld16(tcol + c0 + 16, *reinterpret_cast<uint32_t(*)[16]>(&v[16]));
+                    tmem_wait_ld_regs<32>(v);
+                    float h[32];
+#pragma unroll
+                    for (int u = 0; u < 32; ++u) h[u] = ok ? gam * __uint_as_float(v[u]) : 0.f;
+                    tmem_st16(tcol + c0, reinterpret_cast<const uint32_t*>(&h[0]));
+                    tmem_st16(tcol + c0 + 16, reinterpret_cast<const uint32_t*>(&h[16]));
+                    write_h32(c + 1, c0, h);
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(s_free);
+                mbar_arrive(&fac_empty[sl]);
+                fence_proxy_async();
+                mbar_arrive(&h_ready[(c + 1) & 1]);
+            }
+            mbar_arrive(&fac_empty[(nchunks - 1) % kFS]);
         }
-        drain_y(nchunks - 1);
     }
     tc_fence_before();
     __syncthreads();
@@ -623,7 +751,7 @@ struct BwdLayout {
     static constexpr int OFF_F = OFF_S + 2 * SBUF;         // f, g, delta: [2 buf][2 head][64] each
     static constexpr int OFF_SC = OFF_F + 3 * 2 * 2 * 64 * 4;  // half: [2 buf][2 head][4]
     static constexpr int OFF_RQ = OFF_SC + 2 * 2 * 4 * 4;      // [2 wg][2 head][64]
-    static constexpr int OFF_RED = OFF_RQ + 2 * 2 * 64 * 4;    // [8]
+    static constexpr int OFF_RED = OFF_RQ + 2 * 2 * 64 * 4;    // [16]
     static constexpr int OFF_BAR = OFF_RED + 64;
     static constexpr int NBAR = 16;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
@@ -735,7 +863,7 @@ __device__ __forceinline__ void masked_tile(uint32_t taddr_row, unsigned char* t
     uint32_t v[32];
     tmem_ld16x2<32>(taddr_row + 0, &v[0]);
     tmem_ld16x2<32>(taddr_row + 16, &v[16]);
-    tmem_wait_ld();
+    tmem_wait_ld_regs<32>(v);
     if (!active) return;
     unsigned char* row = tile + t * 128;
 #pragma unroll
@@ -977,7 +1105,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     uint32_t v[32];
                     tmem_ld16(tq + T_S + n0 + c0, *reinterpret_cast<uint32_t(*)[16]>(&v[0]));
                     tmem_ld16(tq + T_S + n0 + c0 + 16, *reinterpret_cast<uint32_t(*)[16]>(&v[16]));
-                    tmem_wait_ld();
+                    tmem_wait_ld_regs<32>(v);
                     if (ok) {
 #pragma unroll
                         for (int u = 0; u < 32; ++u) Hs[c0 + u] = gam * (Hs[c0 + u] + __uint_as_float(v[u]));
@@ -1014,7 +1142,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     uint32_t v0[16], v1[16];
                     tmem_ld16x2<NH / 2>(tq + T_DC + n0 + c0, v0);
                     tmem_ld16x2<NH / 2>(tq + T_DC + N + n0 + c0, v1);
-                    tmem_wait_ld();
+                    tmem_wait_ld_regs<16>(v0);
+                    reg_dep16(v1);
                     if (ok) {
                         const unsigned char* crow = cst + (n >> 6) * 8192 + t * 128;
                         float cv[16];
@@ -1259,10 +1388,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         // before this segment and u after it, which equals the sum over later tokens of
         // r_u - q_u (both states come from the fp32 scans)
         const int clast = nchunks - 1;
-        if (ct == 0) {
-            F.red[4] = 0.f;
-            F.red[5] = 0.f;
-        }
         bwd_factors(F, si, a, h0, clast, bwd_load_raw(a, si, h0, clast, nchunks, ct), ct, lane);
         {
             const float sc = expf(-F.scal[((clast & 1) * 2 + rh) * 4 + 0]);
@@ -1283,10 +1408,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 Gs[i + 3] = v.w * sc;
             }
             kp = warp_sum(kp);
-            if (lane == 0) atomicAdd(&F.red[4 + rh], kp);
+            if (lane == 0) F.red[8 + wg * 4 + q] = kp;  // partial of head q / 2
         }
         named_sync(1, kCT);
-        const float kseg = F.red[4 + wg];  // for head wg (the head this warpgroup's dx rows belong to)
+        // for head wg (the head this warpgroup's dx rows belong to), summed in a fixed order
+        const float kseg = (F.red[8 + 2 * wg] + F.red[9 + 2 * wg]) +
+                           (F.red[12 + 2 * wg] + F.red[13 + 2 * wg]);
         write_state<NH>(sm + Lay::OFF_S + (clast & 1) * Lay::SBUF, Gs, r, n0);
         fence_proxy_async();
         mbar_arrive(&g_ready[clast & 1]);
@@ -1347,7 +1474,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     uint32_t v[32];
                     tmem_ld16(tq + T_SP + n0 + c0, *reinterpret_cast<uint32_t(*)[16]>(&v[0]));
                     tmem_ld16(tq + T_SP + n0 + c0 + 16, *reinterpret_cast<uint32_t(*)[16]>(&v[16]));
-                    tmem_wait_ld();
+                    tmem_wait_ld_regs<32>(v);
                     if (ok) {
 #pragma unroll
                         for (int u = 0; u < 32; ++u) Gs[c0 + u] = gam * (Gs[c0 + u] + __uint_as_float(v[u]));
@@ -1381,7 +1508,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     uint32_t v[32];
                     tmem_ld16x2<32>(tq + T_DX + wg * 64, &v[0]);
                     tmem_ld16x2<32>(tq + T_DX + wg * 64 + 16, &v[16]);
-                    tmem_wait_ld();
+                    tmem_wait_ld_regs<32>(v);
                     if (ok) {
 #pragma unroll
                         for (int e = 0; e < 32; e += 8) {
@@ -1419,7 +1546,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     uint32_t v[STEP];
                     tmem_ld16x2<HW>(tq + T_DB + n0 + c0, &v[0]);
                     if constexpr (STEP == 32) tmem_ld16x2<HW>(tq + T_DB + n0 + c0 + 16, &v[16]);
-                    tmem_wait_ld();
+                    tmem_wait_ld_regs<STEP>(v);
                     {  // partial dB; rows past the chunk's tokens add zero
                         const int n = n0 + HW * hf + c0;
                         float val[STEP];
@@ -1485,6 +1612,18 @@ cudaError_t set_smem(K kernel, int bytes) {
 }
 
 template <int N>
+cudaError_t launch_l0(const Prob& pb, const Args& a, Launch& L, const CUtensorMap& mb,
+                      const CUtensorMap& mc) {
+    const int cps = pb.Ls / kQ;
+    const dim3 grid((unsigned)(pb.nseg_max * ((cps + kL0Chunks - 1) / kL0Chunks)), pb.G);
+    cudaError_t e = set_smem(tc_l0_kernel<N>, l0_smem_bytes<N>());
+    if (e != cudaSuccess) return e;
+    L.begin("tc_l0");
+    tc_l0_kernel<N><<<grid, kL0Threads, l0_smem_bytes<N>(), L.stream>>>(mb, mc, a);
+    return L.end();
+}
+
+template <int N>
 cudaError_t forward_n(const Prob& pb, const Args& a, Launch& L) {
     CUtensorMap mx, mb, mc;
     if (!make_map(&mx, a.x, pb.T, pb.H, kP) || !make_map(&mb, a.B, pb.T, pb.G, N) ||
@@ -1492,6 +1631,7 @@ cudaError_t forward_n(const Prob& pb, const Args& a, Launch& L) {
         return cudaErrorInvalidValue;
     cudaError_t e = launch_seg_table(pb, a, L);
     if (e != cudaSuccess) return e;
+    if ((e = launch_l0<N>(pb, a, L, mb, mc)) != cudaSuccess) return e;
     const dim3 grid((unsigned)pb.nseg_max, pb.H / 2);
     e = set_smem(tc_seg_state_kernel<N, 0>, state_smem_bytes(N));
     if (e != cudaSuccess) return e;
@@ -1517,6 +1657,7 @@ cudaError_t backward_n(const Prob& pb, const Args& a, Launch& L) {
         return cudaErrorInvalidValue;
     cudaError_t e = launch_seg_table(pb, a, L);
     if (e != cudaSuccess) return e;
+    if ((e = launch_l0<N>(pb, a, L, mb, mc)) != cudaSuccess) return e;
     const dim3 grid((unsigned)pb.nseg_max, pb.H / 2);
     e = set_smem(tc_seg_state_kernel<N, 0>, state_smem_bytes(N));
     if (e != cudaSuccess) return e;

@@ -79,6 +79,16 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, u
         "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2)
         : "memory");
 }
+// Contiguous global -> shared copy (both addresses 16-byte aligned, bytes a multiple
+// of 16), completing on the mbarrier like a tensor copy.
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes,
+                                          uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
 __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void* src, int c0,
                                              int c1, int c2) {
     asm volatile(
@@ -178,8 +188,43 @@ __device__ __forceinline__ void tmem_ld16x2(uint32_t taddr, uint32_t* r) {
           "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
         : "r"(taddr), "n"(OFF));
 }
+// Inverse of tmem_ld16: thread i of the warp writes lane (quadrant base + i),
+// columns [col, col + 16).
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+        "r"(r[15])
+        : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() {
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
 __device__ __forceinline__ void tmem_wait_ld() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+// The registers a tcgen05.ld writes hold their values only once tcgen05.wait::ld has
+// returned, a dependency the compiler cannot see: to it they are defined by the load
+// itself, and arithmetic on them could be scheduled ahead of the wait.  Passing them
+// through an (empty) asm statement after the wait, as read-write operands, makes every
+// later use depend on that statement, which keeps its place after the wait.
+__device__ __forceinline__ void reg_dep16(uint32_t* r) {
+    asm volatile(""
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
+                   "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),
+                   "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15])
+                 :
+                 : "memory");
+}
+// Waits for this thread's TMEM loads and orders the uses of the K registers at r after it.
+template <int K>
+__device__ __forceinline__ void tmem_wait_ld_regs(uint32_t* r) {
+    static_assert(K % 16 == 0, "whole 16-register groups");
+    tmem_wait_ld();
+#pragma unroll
+    for (int i = 0; i < K; i += 16) reg_dep16(r + i);
 }
 
 // Shared-memory matrix descriptor, 128-byte swizzle (bf16 operands).
