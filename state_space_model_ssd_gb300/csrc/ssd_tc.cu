@@ -362,29 +362,36 @@ constexpr int l0_smem_bytes() {
 }
 
 // ================================================================ chunk walk
-// Warps: 0 = TMA producer (x, B, C and the chunk's L0 tile), 1 = MMA issuer, 2..17 =
-// four compute warpgroups, each with its own task so that the tasks of neighbouring
-// chunks overlap:
+// x streams from HBM through a ring of kXS slots, refilled kXS - 1 chunks ahead of its
+// use (the load latency under full traffic is a few chunk periods); B, C and the L0
+// tile, shared by all heads of a group and mostly served by L2, use a ring of two.
+// Warps: 0 = TMA producer (x, B, C and the chunk's L0 tile), 1 = MMA issuer of the
+// state chain (G4), 18 = MMA issuer of the y path (G2, G3), 2..17 = four compute
+// warpgroups, each with its own task so that the tasks of neighbouring chunks overlap:
 //   warpgroup 0     factors of the next chunk, x -> g x of the current one;
 //   warpgroup 1     the y epilogue;
 //   warpgroups 2-3  the state update Hs <- gamma (Hs + S) and the G3 operand.
 // The groups hand work to each other and to the MMA warp through mbarriers only.
 constexpr int kCT = 256;  // compute threads of the backward walks (two warpgroups)
-constexpr int kWalkThreads = 64 + 4 * 128;
+constexpr int kWalkThreads = 64 + 4 * 128 + 32;
 constexpr int kFS = 4;    // factor slots (chunk c uses slot c % kFS)
+constexpr int kXS = 4;    // x slots (chunk c uses slot c % kXS)
 
 template <int N>
 struct WalkLayout {
-    static constexpr int STAGE = 16384 + 2 * N * 128 + 8192;  // X h0 | X h1 | B | C | L0
-    static constexpr int L0_IN_STAGE = 16384 + 2 * N * 128;
-    static constexpr int OFF_STAGE = 0;
-    static constexpr int OFF_H = 2 * STAGE;                 // 2 x (N/64) x 16K
+    static constexpr int XSLOT = 16384;                     // X h0 | X h1
+    static constexpr int BCSLOT = 2 * N * 128 + 8192;       // B | C | L0
+    static constexpr int C_IN_BC = N * 128;
+    static constexpr int L0_IN_BC = 2 * N * 128;
+    static constexpr int OFF_X = 0;
+    static constexpr int OFF_BC = kXS * XSLOT;
+    static constexpr int OFF_H = OFF_BC + 2 * BCSLOT;       // 2 x (N/64) x 16K
     static constexpr int HBUF = (N / 64) * 16384;
     static constexpr int OFF_F = OFF_H + 2 * HBUF;          // f, g: [slot][head][64] each
     static constexpr int OFF_SC = OFF_F + 2 * kFS * 2 * 64 * 4;  // half: [slot][head][4]
     static constexpr int OFF_RED = OFF_SC + kFS * 2 * 4 * 4;     // [4]
     static constexpr int OFF_BAR = OFF_RED + 64;
-    static constexpr int NBAR = 32;
+    static constexpr int NBAR = 40;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr int TOTAL = OFF_MISC + 16 + 1024;  // + alignment slack
 };
@@ -416,11 +423,13 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
     float* scal = reinterpret_cast<float*>(sm + Lay::OFF_SC);  // [slot][head][4]: half
     float* red = reinterpret_cast<float*>(sm + Lay::OFF_RED);
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + Lay::OFF_BAR);
-    uint64_t* full = bars + 0;        // [2] TMA stage landed
-    uint64_t* empty = bars + 2;       // [2] stage consumed by the MMAs
-    uint64_t* xg_ready = bars + 6;    // [2] x scaled in place (warpgroup 0)
-    uint64_t* s_full = bars + 10;     // S accumulated
-    uint64_t* s_free = bars + 11;     // S read by the state warps
+    uint64_t* full_x = bars + 0;      // [kXS] x of a chunk landed
+    uint64_t* empty_x = bars + 4;     // [kXS] x read by the MMAs
+    uint64_t* xg_ready = bars + 8;    // [kXS] x scaled in place (warpgroup 0)
+    uint64_t* full_bc = bars + 28;    // [2] B, C, L0 of a chunk landed
+    uint64_t* empty_bc = bars + 30;   // [2] B, C, L0 read by the MMAs
+    uint64_t* s_full = bars + 32;     // S accumulated
+    uint64_t* s_free = bars + 33;     // S read by the state warps
     uint64_t* y_full = bars + 12;     // [2] Y accumulated
     uint64_t* y_free = bars + 14;     // [2] Y read by warpgroup 1
     uint64_t* h_ready = bars + 16;    // [2] G3 operand written (state warps)
@@ -432,10 +441,14 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     if (tid == 0) {
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(&full[i], 1);
-            mbar_init(&empty[i], 1);
+        for (int i = 0; i < kXS; ++i) {
+            mbar_init(&full_x[i], 1);
+            mbar_init(&empty_x[i], 2);  // read by G4 and G2 (two issuing threads)
             mbar_init(&xg_ready[i], 128);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&full_bc[i], 1);
+            mbar_init(&empty_bc[i], 2);  // B read by G4, C and L0 by G2 / G3
             mbar_init(&y_full[i], 1);
             mbar_init(&y_free[i], 128);
             mbar_init(&h_ready[i], 256);
@@ -463,58 +476,86 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
         // ------------------------------------------------ TMA producer
         if (lane == 0) {
             const int cps = a.Ls / kQ;
+            auto load_x = [&](int cc) {
+                const int xs = cc % kXS;
+                unsigned char* st = sm + Lay::OFF_X + xs * Lay::XSLOT;
+                const int tok = (int)(si.start + (long long)cc * kQ);
+                mbar_expect_tx(&full_x[xs], Lay::XSLOT);
+                tma_load_3d(st, &map_x, &full_x[xs], 0, h0, tok);
+                tma_load_3d(st + 8192, &map_x, &full_x[xs], 0, h0 + 1, tok);
+            };
+            for (int cc = 0; cc < kXS - 1 && cc < nchunks; ++cc) load_x(cc);
             for (int c = 0; c < nchunks; ++c) {
-                const int s = c & 1;
-                if (c >= 2 && !wait_or_abort(&empty[s], ((c >> 1) - 1) & 1, abort_flag, a.hdr))
+                const int b = c & 1;
+                // B, C and L0 of chunk c, into the slot chunk c - 2 used
+                if (c >= 2 && !wait_or_abort(&empty_bc[b], ((c >> 1) - 1) & 1, abort_flag, a.hdr))
                     break;
-                unsigned char* st = sm + Lay::OFF_STAGE + s * Lay::STAGE;
+                unsigned char* st = sm + Lay::OFF_BC + b * Lay::BCSLOT;
                 const int tok = (int)(si.start + (long long)c * kQ);
-                mbar_expect_tx(&full[s], Lay::STAGE);
-                tma_load_3d(st, &map_x, &full[s], 0, h0, tok);
-                tma_load_3d(st + 8192, &map_x, &full[s], 0, h0 + 1, tok);
+                mbar_expect_tx(&full_bc[b], Lay::BCSLOT);
                 for (int nb = 0; nb < N / 64; ++nb) {
-                    tma_load_3d(st + 16384 + nb * 8192, &map_b, &full[s], nb * 64, g, tok);
-                    tma_load_3d(st + 16384 + N * 128 + nb * 8192, &map_c, &full[s], nb * 64, g,
+                    tma_load_3d(st + nb * 8192, &map_b, &full_bc[b], nb * 64, g, tok);
+                    tma_load_3d(st + Lay::C_IN_BC + nb * 8192, &map_c, &full_bc[b], nb * 64, g,
                                 tok);
                 }
-                bulk_load(st + Lay::L0_IN_STAGE,
-                          a.l0 + (((long long)seg * cps + c) * a.G + g) * 8192, 8192, &full[s]);
+                bulk_load(st + Lay::L0_IN_BC,
+                          a.l0 + (((long long)seg * cps + c) * a.G + g) * 8192, 8192, &full_bc[b]);
+                // x of chunk c + kXS - 1, into the slot chunk c - 1 used
+                const int cx = c + kXS - 1;
+                if (cx < nchunks) {
+                    if (cx >= kXS &&
+                        !wait_or_abort(&empty_x[cx % kXS], ((cx / kXS) - 1) & 1, abort_flag, a.hdr))
+                        break;
+                    load_x(cx);
+                }
             }
         }
     } else if (warp == 1) {
-        // ------------------------------------------------ MMA issuer
+        // ------------------------------------------------ MMA issuer: state chain
         if (lane == 0) {
-            const uint32_t id_y = idesc_bf16(64, 128, 0, 1);
-            const uint32_t id_h = idesc_bf16(64, 128, 0, 0);
             const uint32_t id_s = idesc_bf16(128, N, 1, 1);
             for (int c = 0; c < nchunks; ++c) {
                 const int s = c & 1, ph = (c >> 1) & 1;
-                const bool last = (c == nchunks - 1);
-                if (!wait_or_abort(&full[s], ph, abort_flag, a.hdr)) break;
-                tc_fence_after();
-                const uint32_t xs = smem_u32(sm + Lay::OFF_STAGE + s * Lay::STAGE);
-                const uint32_t bs = xs + 16384;
-                const uint32_t cs = bs + N * 128;
-                const uint32_t l0 = xs + Lay::L0_IN_STAGE;
-                if (!wait_or_abort(&xg_ready[s], ph, abort_flag, a.hdr)) break;
-                tc_fence_after();
-                // G4: Hs_c + S_c in the state columns (not needed after the last chunk)
-                if (!last) {
+                const int xsl = c % kXS, xph = (c / kXS) & 1;
+                if (c < nchunks - 1) {  // G4: Hs_c + S_c in the state columns
+                    if (!wait_or_abort(&full_bc[s], ph, abort_flag, a.hdr)) break;
+                    if (!wait_or_abort(&xg_ready[xsl], xph, abort_flag, a.hdr)) break;
                     if (!wait_or_abort(s_free, c & 1, abort_flag, a.hdr)) break;
                     tc_fence_after();
+                    const uint32_t xs = smem_u32(sm + Lay::OFF_X + xsl * Lay::XSLOT);
+                    const uint32_t bs = smem_u32(sm + Lay::OFF_BC + s * Lay::BCSLOT);
 #pragma unroll
                     for (int k = 0; k < kQ / 16; ++k)
                         mma_bf16(tmem + kColS, sw128_desc(xs + k * 2048, 8192, 1024),
                                  sw128_desc(bs + k * 2048, 8192, 1024), id_s, 1u);
                     mma_commit(s_full);
                 }
-                // G2: diagonal block
+                mma_commit(&empty_x[xsl]);
+                mma_commit(&empty_bc[s]);
+            }
+        }
+    } else if (warp == 18) {
+        // ------------------------------------------------ MMA issuer: y path
+        if (lane == 0) {
+            const uint32_t id_y = idesc_bf16(64, 128, 0, 1);
+            const uint32_t id_h = idesc_bf16(64, 128, 0, 0);
+            for (int c = 0; c < nchunks; ++c) {
+                const int s = c & 1, ph = (c >> 1) & 1;
+                const int xsl = c % kXS, xph = (c / kXS) & 1;
+                if (!wait_or_abort(&full_bc[s], ph, abort_flag, a.hdr)) break;
+                if (!wait_or_abort(&xg_ready[xsl], xph, abort_flag, a.hdr)) break;
                 if (c >= 2 && !wait_or_abort(&y_free[s], ph ^ 1, abort_flag, a.hdr)) break;
                 tc_fence_after();
+                const uint32_t xs = smem_u32(sm + Lay::OFF_X + xsl * Lay::XSLOT);
+                const uint32_t bs = smem_u32(sm + Lay::OFF_BC + s * Lay::BCSLOT);
+                const uint32_t cs = bs + Lay::C_IN_BC;
+                const uint32_t l0 = bs + Lay::L0_IN_BC;
+                // G2: diagonal block
 #pragma unroll
                 for (int k = 0; k < kQ / 16; ++k)
                     mma_bf16(tmem + col_y(s), sw128_desc(l0 + k * 32, 16, 1024),
                              sw128_desc(xs + k * 2048, 8192, 1024), id_y, k > 0 ? 1u : 0u);
+                mma_commit(&empty_x[xsl]);
                 // G3: state entering the chunk
                 if (!wait_or_abort(&h_ready[s], ph, abort_flag, a.hdr)) break;
                 tc_fence_after();
@@ -528,7 +569,7 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
                 }
                 mma_commit(&y_full[s]);
                 mma_commit(&h_free[s]);
-                mma_commit(&empty[s]);
+                mma_commit(&empty_bc[s]);
             }
         }
     } else {
@@ -570,10 +611,10 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
             };
             factors(0, load_raw(0));
             for (int c = 0; c < nchunks; ++c) {
-                const int s = c & 1, ph = (c >> 1) & 1;
+                const int xsl = c % kXS, xph = (c / kXS) & 1;
                 const float raw_next = load_raw(c + 1);
-                if (wait_or_abort(&full[s], ph, abort_flag, a.hdr)) {
-                    uint4* xs = reinterpret_cast<uint4*>(sm + Lay::OFF_STAGE + s * Lay::STAGE);
+                if (wait_or_abort(&full_x[xsl], xph, abort_flag, a.hdr)) {
+                    uint4* xs = reinterpret_cast<uint4*>(sm + Lay::OFF_X + xsl * Lay::XSLOT);
                     const float* gv = gbuf + (c % kFS) * 128;
 #pragma unroll
                     for (int i = 0; i < 8; ++i) {
@@ -582,7 +623,7 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
                     }
                 }
                 fence_proxy_async();
-                mbar_arrive(&xg_ready[s]);
+                mbar_arrive(&xg_ready[xsl]);
                 if (c + 1 < nchunks) {
                     const int cn = c + 1;
                     if (cn >= kFS)

@@ -16,6 +16,7 @@ constexpr int kQ = 64;                 // chunk length
 constexpr int kP = 64;                 // head dimension
 constexpr float kMaxChunkDecay = 160.f;
 constexpr uint64_t kWaitNs = 2000000000ull;
+constexpr uint32_t kSleepHintNs = 20000;  // longest suspension per check of a wait
 
 // ---------------------------------------------------------------- host: tensor maps
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
@@ -74,12 +75,12 @@ __device__ __forceinline__ void named_sync(int id, int nthreads) {
 // Bounded wait that also gives up as soon as another thread has aborted.
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity,
                                               volatile int* abort_flag, WsHeader* hdr) {
-    if (*abort_flag) return false;
     if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
     const uint64_t t0 = globaltimer_ns();
     while (true) {
-        for (int i = 0; i < 32; ++i)
-            if (mbar_try_wait(bar, parity)) return true;
+        // suspended in hardware between checks (woken when the phase completes)
+        if (mbar_try_wait_sleep(bar, parity, kSleepHintNs)) return true;
         if (*abort_flag) return false;
         if (globaltimer_ns() - t0 > kWaitNs) {
             *abort_flag = 1;

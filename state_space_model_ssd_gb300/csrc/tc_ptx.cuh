@@ -48,6 +48,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
+// As mbar_try_wait, but lets the hardware suspend the thread for up to hint_ns while
+// the phase is incomplete (it resumes as soon as the phase completes), so waiting
+// warps do not compete for issue slots with the warps doing work.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity,
+                                                    uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
 // Waits for the phase with the given parity to complete.  Gives up after
 // `limit_ns` nanoseconds and returns false, so a lost arrival never hangs the
 // GPU; the caller records a timeout status and winds down.
