@@ -1279,19 +1279,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     uint64_t* full = bars + 0;      // [2]
     uint64_t* empty = bars + 2;     // [2]
     uint64_t* xg_ready = bars + 4;
-    uint64_t* d1_full = bars + 5;
+    uint64_t* l0_full = bars + 5;   // the chunk's L0 tile landed (T1)
     uint64_t* p2_full = bars + 6;
-    uint64_t* e_ready = bars + 7;   // L0T and P2m tiles written, D1/P2 TMEM read
+    uint64_t* e_ready = bars + 7;   // P2m tiles written, P2 TMEM read
     uint64_t* s_full = bars + 8;
     uint64_t* s_free = bars + 9;
     uint64_t* o_full = bars + 11;   // DX and dB accumulated
     uint64_t* o_free = bars + 12;
     uint64_t* g_ready = bars + 13;  // [2], one per state operand buffer
+    uint64_t* l0_free = bars + 15;  // DX of the chunk done: T1 may be refilled
     uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + Lay::OFF_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tslot + 1);
-    // TMEM columns: D1 0..63, P2 64..191, (S' aliases 0..N-1 once D1/P2 are read), DX 192..319,
-    // dB 320..320+N-1
-    const uint32_t T_D1 = 0, T_P2 = 64, T_SP = 0, T_DX = 192, T_DB = 320;
+    // TMEM columns: S' 0..127, P2 128..255, DX 256..383, dB 384..511
+    const uint32_t T_P2 = 128, T_SP = 0, T_DX = 256, T_DB = 384;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     if (tid == 0) {
@@ -1300,7 +1300,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             mbar_init(&empty[i], kCT);
         }
         mbar_init(xg_ready, kCT);
-        mbar_init(d1_full, 1);
+        mbar_init(l0_full, 1);
+        mbar_init(l0_free, 1);
         mbar_init(p2_full, 1);
         mbar_init(e_ready, kCT);
         mbar_init(s_full, 1);
@@ -1323,6 +1324,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
     if (warp == 0) {
         if (lane == 0) {
+            const int cps = a.Ls / kQ;
             for (int it = 0; it < nchunks; ++it) {
                 const int c = nchunks - 1 - it, s = it & 1;
                 if (it >= 2 && !wait_or_abort(&empty[s], ((it >> 1) - 1) & 1, abort_flag, a.hdr))
@@ -1339,13 +1341,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     tma_load_3d(st + 32768 + N * 128 + nb * 8192, &map_c, &full[s], nb * 64, g,
                                 tok);
                 }
+                // the chunk's L0 tile (read as L0^T) into T1, once DX of the previous chunk
+                // has read it
+                if (it >= 1 && !wait_or_abort(l0_free, (it - 1) & 1, abort_flag, a.hdr)) break;
+                mbar_expect_tx(l0_full, 8192);
+                bulk_load(sm + Lay::OFF_T1, a.l0 + (((long long)seg * cps + c) * a.G + g) * 8192,
+                          8192, l0_full);
             }
         }
     } else if (warp == 1) {
         if (lane == 0) {
-            const uint32_t id_cb = idesc_bf16(64, 64, 0, 0);
+            const uint32_t id_p2 = idesc_bf16(64, 64, 0, 0);
             const uint32_t id_sp = idesc_bf16(128, N, 1, 1);
-            const uint32_t id_dx1 = idesc_bf16(64, 128, 0, 1);
+            const uint32_t id_dx1 = idesc_bf16(64, 128, 1, 1);
             const uint32_t id_dx2 = idesc_bf16(64, 128, 0, 0);
             const uint32_t id_db = idesc_bf16(64, N, 0, 1);
             for (int it = 0; it < nchunks; ++it) {
@@ -1355,24 +1363,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 tc_fence_after();
                 const uint32_t xs = smem_u32(sm + Lay::OFF_STAGE + s * Lay::STAGE);
                 const uint32_t ys = xs + 16384, bs = xs + 32768, cs = bs + N * 128;
-                // L0T[t, u] = B_t . C_u
-#pragma unroll
-                for (int k = 0; k < N / 16; ++k)
-                    mma_bf16(tmem + T_D1, kdesc(bs, k, 8192), kdesc(cs, k, 8192), id_cb,
-                             k > 0 ? 1u : 0u);
-                mma_commit(d1_full);
                 if (!wait_or_abort(xg_ready, pi, abort_flag, a.hdr)) break;
                 tc_fence_after();
-#pragma unroll
-                for (int h = 0; h < 2; ++h)
-#pragma unroll
-                    for (int k = 0; k < 4; ++k)
-                        mma_bf16(tmem + T_P2 + h * 64, kdesc(xs + h * 8192, k, 0),
-                                 kdesc(ys + h * 8192, k, 0), id_cb, k > 0 ? 1u : 0u);
-                mma_commit(p2_full);
-                if (!wait_or_abort(e_ready, pi, abort_flag, a.hdr)) break;
-                tc_fence_after();
-                // S' = dyf^T C (adjoint contribution of the chunk), into the freed D1/P2 columns
+                // S' = dyf^T C (adjoint contribution of the chunk; not needed for the first)
                 if (it < nchunks - 1) {
 #pragma unroll
                     for (int k = 0; k < 4; ++k)
@@ -1380,9 +1373,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                                  k > 0 ? 1u : 0u);
                 }
                 mma_commit(s_full);
+#pragma unroll
+                for (int h = 0; h < 2; ++h)
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        mma_bf16(tmem + T_P2 + h * 64, kdesc(xs + h * 8192, k, 0),
+                                 kdesc(ys + h * 8192, k, 0), id_p2, k > 0 ? 1u : 0u);
+                mma_commit(p2_full);
+                if (!wait_or_abort(e_ready, pi, abort_flag, a.hdr)) break;
                 const int cb = (nchunks - 1 - it) & 1;  // state operand buffer of this chunk
                 if (!wait_or_abort(&g_ready[cb], ph, abort_flag, a.hdr)) break;
                 if (it >= 1 && !wait_or_abort(o_free, pi ^ 1, abort_flag, a.hdr)) break;
+                if (!wait_or_abort(l0_full, it & 1, abort_flag, a.hdr)) break;
                 tc_fence_after();
                 const uint32_t l0 = smem_u32(sm + Lay::OFF_T1);
                 const uint32_t p2m = smem_u32(sm + Lay::OFF_T0);
@@ -1390,7 +1392,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 // DX = L0T dyf + B Gs^T
 #pragma unroll
                 for (int k = 0; k < 4; ++k)
-                    mma_bf16(tmem + T_DX, kdesc(l0, k, 0), mdesc(ys, k, 8192), id_dx1,
+                    mma_bf16(tmem + T_DX, mdesc(l0, k, 0), mdesc(ys, k, 8192), id_dx1,
                              k > 0 ? 1u : 0u);
 #pragma unroll
                 for (int k = 0; k < N / 16; ++k)
@@ -1408,6 +1410,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                                  mdesc(gb + h * 8192, k, 16384), id_db, 1u);
                 }
                 mma_commit(o_full);
+                mma_commit(l0_free);
             }
         }
     } else {
@@ -1485,24 +1488,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             }
             const float raw_next = bwd_load_raw(a, si, h0, c - 1, nchunks, ct);
             const float rv = (t < vc) ? a.rtok[(tok0 + t) * a.H + h0 + wg] : 0.f;
-            // B: L0T and the factors of the next chunk (warpgroup 0), the masked P2 tiles
-            // (warpgroup 1, both heads)
-            if (wg == 0) {
-                const bool ok = wait_or_abort(d1_full, pi, abort_flag, a.hdr);
-                tc_fence_after();
-                masked_tile(tq + T_D1, sm + Lay::OFF_T1, t, hf, ok, false);
-                tc_fence_before();
-                fence_proxy_async();
-                mbar_arrive(e_ready);
-                if (c > 0) bwd_factors_wg0(F, si, a, h0, c - 1, raw_next, ct, lane);
-            } else {
+            // B: the masked P2 tile of head wg; then warpgroup 0 makes the factors of the
+            // next chunk
+            {
                 const bool ok = wait_or_abort(p2_full, pi, abort_flag, a.hdr);
                 tc_fence_after();
-                masked_tile(tq + T_P2, sm + Lay::OFF_T0, t, hf, ok, false);
-                masked_tile(tq + T_P2 + 64, sm + Lay::OFF_T0 + 8192, t, hf, ok, false);
+                masked_tile(tq + T_P2 + wg * 64, sm + Lay::OFF_T0 + wg * 8192, t, hf, ok, false);
                 tc_fence_before();
                 fence_proxy_async();
                 mbar_arrive(e_ready);
+                if (wg == 0 && c > 0) bwd_factors_wg0(F, si, a, h0, c - 1, raw_next, ct, lane);
             }
             named_sync(1, kCT);  // the next chunk's factors are visible
             // C: adjoint chain, Gs for the previous chunk
