@@ -846,33 +846,6 @@ __device__ __forceinline__ void bwd_factors(const ChunkFactors& F, const SegInfo
     named_sync(1, kCT);
 }
 
-// The same factors computed by warpgroup 0 alone (threads ct < 128); the caller
-// orders the writes against later readers with a block-wide barrier.
-__device__ __forceinline__ void bwd_factors_wg0(const ChunkFactors& F, const SegInfo& si,
-                                                const Args& a, int h0, int cc, float rawv, int ct,
-                                                int lane) {
-    const int head = ct >> 6, t = ct & 63;
-    const int vc = min(kQ, si.len - cc * kQ);
-    float d = 0.f;
-    if (t < vc) d = softplus_f(rawv + a.delta_init);
-    float inc = warp_scan(d, lane);
-    const int hw = (ct >> 5) & 1;
-    if (lane == 31) F.red[head * 2 + hw] = inc;
-    named_sync(2 + head, 64);
-    if (hw) inc += F.red[head * 2];
-    const float send = F.red[head * 2] + F.red[head * 2 + 1];
-    const float half = 0.5f * send;
-    const int b = cc & 1;
-    F.fbuf[(b * 2 + head) * 64 + t] = (t < vc) ? expf(half - inc) : 0.f;
-    F.gbuf[(b * 2 + head) * 64 + t] = d * expf(inc - half);
-    F.dbuf[(b * 2 + head) * 64 + t] = d;
-    if (t == 0) {
-        F.scal[(b * 2 + head) * 4 + 0] = half;
-        if (send > kMaxChunkDecay) set_status(a.hdr, SSD_ERR_DEVICE);
-    }
-    named_sync(2 + head, 64);  // red is reused by the next call
-}
-
 __device__ __forceinline__ float bwd_load_raw(const Args& a, const SegInfo& si, int h0, int cc,
                                               int nchunks, int ct) {
     const int head = ct >> 6, t = ct & 63;
@@ -1250,14 +1223,43 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 }
 
 // ---------------------------------------------------------------- dX / dB walk
+// Chunks in reverse order.  Warps: 0 = TMA producer (x, dy, B, C; the chunk's L0 tile),
+// 1 = MMA issuer of S' and P2, 18 = MMA issuer of DX and dB, 2..17 = four compute
+// warpgroups with one task each:
+//   warpgroup 0     factors of the next chunk, x -> g x and dy -> f dy in place;
+//   warpgroup 1     the masked P2 tiles, then dx = g DX, q = xg . DX and d_raw;
+//   warpgroups 2-3  the adjoint chain in TMEM (S' accumulates onto Gs there; these
+//                   warps rescale it by gamma), its bf16 operand, and the partial dB
+//                   tiles, added into the fp32 accumulator by TMA reduce-add.
+constexpr int kDxThreads = 64 + 4 * 128 + 32;
+constexpr int kDFS = 4;  // factor slots (processing index it uses slot it % kDFS)
+
 template <int N>
-__global__ void __launch_bounds__(kBwdThreads, 1)
+struct DxLayout {
+    static constexpr int STAGE = 32768 + 2 * N * 128;       // x h0 | x h1 | dy h0 | dy h1 | B | C
+    static constexpr int OFF_STAGE = 0;
+    static constexpr int OFF_P2M = 2 * STAGE;                // masked P2, 2 x 8K
+    static constexpr int OFF_L0 = OFF_P2M + 16384;           // L0 tile (read as L0^T), 8K
+    static constexpr int OFF_G = OFF_L0 + 8192;              // bf16 Gs operand, (N/64) x 16K
+    static constexpr int OFF_DB = OFF_G + (N / 64) * 16384;  // fp32 dB staging, (N/32) x 8K
+    static constexpr int OFF_F = OFF_DB + N * 256;           // f, g, delta: [slot][head][64]
+    static constexpr int OFF_SC = OFF_F + 3 * kDFS * 2 * 64 * 4;  // half: [slot][head][4]
+    static constexpr int OFF_RQ = OFF_SC + kDFS * 2 * 4 * 4;      // [2 head][4 quadrant]
+    static constexpr int OFF_RED = OFF_RQ + 64;                   // [16]
+    static constexpr int OFF_BAR = OFF_RED + 64;
+    static constexpr int NBAR = 40;
+    static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+    static constexpr int TOTAL = OFF_MISC + 16 + 1024;
+};
+
+template <int N>
+__global__ void __launch_bounds__(kDxThreads, 1)
     tc_bwd_dxdb_kernel(const __grid_constant__ CUtensorMap map_x,
                        const __grid_constant__ CUtensorMap map_dy,
                        const __grid_constant__ CUtensorMap map_b,
                        const __grid_constant__ CUtensorMap map_c,
                        const __grid_constant__ CUtensorMap map_acc, Args a) {
-    using Lay = BwdLayout<N>;
+    using Lay = DxLayout<N>;
     const int seg = blockIdx.x;
     const int h0 = blockIdx.y * 2;
     if (seg >= a.hdr->nseg) return;
@@ -1268,48 +1270,62 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     extern __shared__ __align__(1024) unsigned char smraw[];
     unsigned char* sm = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smraw) + 1023) & ~(uintptr_t)1023);
-    ChunkFactors F;
-    F.fbuf = reinterpret_cast<float*>(sm + Lay::OFF_F);
-    F.gbuf = F.fbuf + 256;
-    F.dbuf = F.gbuf + 256;
-    F.scal = reinterpret_cast<float*>(sm + Lay::OFF_SC);
-    F.red = reinterpret_cast<float*>(sm + Lay::OFF_RED);
-    float* rqs = reinterpret_cast<float*>(sm + Lay::OFF_RQ);  // [2 head][64]: r - q of the chunk
+    float* fbuf = reinterpret_cast<float*>(sm + Lay::OFF_F);  // [slot][head][64]
+    float* gbuf = fbuf + kDFS * 128;
+    float* dbuf = gbuf + kDFS * 128;
+    float* scal = reinterpret_cast<float*>(sm + Lay::OFF_SC);  // [slot][head][4]: half
+    float* rqs = reinterpret_cast<float*>(sm + Lay::OFF_RQ);   // [2 head][4]
+    float* red = reinterpret_cast<float*>(sm + Lay::OFF_RED);  // 0..3 factors, 8..15 kseg
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + Lay::OFF_BAR);
-    uint64_t* full = bars + 0;      // [2]
-    uint64_t* empty = bars + 2;     // [2]
-    uint64_t* xg_ready = bars + 4;
-    uint64_t* l0_full = bars + 5;   // the chunk's L0 tile landed (T1)
-    uint64_t* p2_full = bars + 6;
-    uint64_t* e_ready = bars + 7;   // P2m tiles written, P2 TMEM read
-    uint64_t* s_full = bars + 8;
-    uint64_t* s_free = bars + 9;
-    uint64_t* o_full = bars + 11;   // DX and dB accumulated
-    uint64_t* o_free = bars + 12;
-    uint64_t* g_ready = bars + 13;  // [2], one per state operand buffer
-    uint64_t* l0_free = bars + 15;  // DX of the chunk done: T1 may be refilled
+    uint64_t* full = bars + 0;        // [2] stage landed
+    uint64_t* empty = bars + 2;       // [2] stage read by the MMAs and by the q epilogue
+    uint64_t* xg_ready = bars + 4;    // [2] x, dy scaled in place (warpgroup 0)
+    uint64_t* l0_full = bars + 6;     // L0 tile landed
+    uint64_t* l0_free = bars + 7;     // DX has read the L0 tile
+    uint64_t* s_full = bars + 8;      // S' accumulated onto Gs
+    uint64_t* s_free = bars + 9;      // Gs rescaled in TMEM (state warps)
+    uint64_t* p2_full = bars + 10;    // P2 accumulated
+    uint64_t* e_ready = bars + 11;    // P2 read from TMEM and masked into P2M (warpgroup 1)
+    uint64_t* p2m_free = bars + 12;   // dB has read P2M
+    uint64_t* g_ready = bars + 13;    // bf16 Gs operand written (state warps)
+    uint64_t* g_free = bars + 14;     // DX and dB have read the Gs operand
+    uint64_t* dx_full = bars + 15;    // DX accumulated
+    uint64_t* dx_free = bars + 16;    // DX read (warpgroup 1)
+    uint64_t* db_full = bars + 17;    // dB accumulated
+    uint64_t* db_free = bars + 18;    // dB read (state warps)
+    uint64_t* kseg_ready = bars + 19; // boundary term written (state warps)
+    uint64_t* fac_full = bars + 20;   // [kDFS]
+    uint64_t* fac_empty = bars + 24;  // [kDFS]
     uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + Lay::OFF_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tslot + 1);
-    // TMEM columns: S' 0..127, P2 128..255, DX 256..383, dB 384..511
-    const uint32_t T_P2 = 128, T_SP = 0, T_DX = 256, T_DB = 384;
+    // TMEM columns: Gs (+ S') 0..127, P2 128..255 (2 x 64), DX 256..383, dB 384..511
+    const uint32_t T_G = 0, T_P2 = 128, T_DX = 256, T_DB = 384;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     if (tid == 0) {
         for (int i = 0; i < 2; ++i) {
             mbar_init(&full[i], 1);
-            mbar_init(&empty[i], kCT);
+            mbar_init(&empty[i], 1 + 128);
+            mbar_init(&xg_ready[i], 128);
         }
-        mbar_init(xg_ready, kCT);
         mbar_init(l0_full, 1);
         mbar_init(l0_free, 1);
-        mbar_init(p2_full, 1);
-        mbar_init(e_ready, kCT);
         mbar_init(s_full, 1);
-        mbar_init(s_free, kCT);
-        mbar_init(&g_ready[0], kCT);
-        mbar_init(&g_ready[1], kCT);
-        mbar_init(o_full, 1);
-        mbar_init(o_free, kCT);
+        mbar_init(s_free, 256);
+        mbar_init(p2_full, 1);
+        mbar_init(e_ready, 128);
+        mbar_init(p2m_free, 1);
+        mbar_init(g_ready, 256);
+        mbar_init(g_free, 1);
+        mbar_init(dx_full, 1);
+        mbar_init(dx_free, 128);
+        mbar_init(db_full, 1);
+        mbar_init(db_free, 256);
+        mbar_init(kseg_ready, 256);
+        for (int i = 0; i < kDFS; ++i) {
+            mbar_init(&fac_full[i], 128);
+            mbar_init(&fac_empty[i], 128 + 256);
+        }
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -1323,6 +1339,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint32_t tmem = *tslot;
 
     if (warp == 0) {
+        // ------------------------------------------------ TMA producer
         if (lane == 0) {
             const int cps = a.Ls / kQ;
             for (int it = 0; it < nchunks; ++it) {
@@ -1341,38 +1358,34 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     tma_load_3d(st + 32768 + N * 128 + nb * 8192, &map_c, &full[s], nb * 64, g,
                                 tok);
                 }
-                // the chunk's L0 tile (read as L0^T) into T1, once DX of the previous chunk
-                // has read it
                 if (it >= 1 && !wait_or_abort(l0_free, (it - 1) & 1, abort_flag, a.hdr)) break;
                 mbar_expect_tx(l0_full, 8192);
-                bulk_load(sm + Lay::OFF_T1, a.l0 + (((long long)seg * cps + c) * a.G + g) * 8192,
+                bulk_load(sm + Lay::OFF_L0, a.l0 + (((long long)seg * cps + c) * a.G + g) * 8192,
                           8192, l0_full);
             }
         }
     } else if (warp == 1) {
+        // ------------------------------------------------ MMA issuer: S', P2
         if (lane == 0) {
             const uint32_t id_p2 = idesc_bf16(64, 64, 0, 0);
             const uint32_t id_sp = idesc_bf16(128, N, 1, 1);
-            const uint32_t id_dx1 = idesc_bf16(64, 128, 1, 1);
-            const uint32_t id_dx2 = idesc_bf16(64, 128, 0, 0);
-            const uint32_t id_db = idesc_bf16(64, N, 0, 1);
             for (int it = 0; it < nchunks; ++it) {
-                const int s = it & 1, ph = (it >> 1) & 1, pi = it & 1;
-                if (!wait_or_abort(&full[s], ph, abort_flag, a.hdr)) break;
-                if (it >= 1 && !wait_or_abort(s_free, pi ^ 1, abort_flag, a.hdr)) break;
-                tc_fence_after();
+                const int s = it & 1, ph = (it >> 1) & 1;
+                if (!wait_or_abort(&xg_ready[s], ph, abort_flag, a.hdr)) break;
                 const uint32_t xs = smem_u32(sm + Lay::OFF_STAGE + s * Lay::STAGE);
-                const uint32_t ys = xs + 16384, bs = xs + 32768, cs = bs + N * 128;
-                if (!wait_or_abort(xg_ready, pi, abort_flag, a.hdr)) break;
-                tc_fence_after();
-                // S' = dyf^T C (adjoint contribution of the chunk; not needed for the first)
+                const uint32_t ys = xs + 16384, cs = xs + 32768 + N * 128;
+                // S' = dyf^T C onto Gs (not needed for the segment's first chunk)
                 if (it < nchunks - 1) {
+                    if (!wait_or_abort(s_free, it & 1, abort_flag, a.hdr)) break;
+                    tc_fence_after();
 #pragma unroll
                     for (int k = 0; k < 4; ++k)
-                        mma_bf16(tmem + T_SP, mdesc(ys, k, 8192), mdesc(cs, k, 8192), id_sp,
-                                 k > 0 ? 1u : 0u);
+                        mma_bf16(tmem + T_G, mdesc(ys, k, 8192), mdesc(cs, k, 8192), id_sp, 1u);
+                    mma_commit(s_full);
                 }
-                mma_commit(s_full);
+                // P2_h = xg_h dyf_h^T, once warpgroup 1 has read the previous P2
+                if (it >= 1 && !wait_or_abort(e_ready, (it - 1) & 1, abort_flag, a.hdr)) break;
+                tc_fence_after();
 #pragma unroll
                 for (int h = 0; h < 2; ++h)
 #pragma unroll
@@ -1380,16 +1393,27 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                         mma_bf16(tmem + T_P2 + h * 64, kdesc(xs + h * 8192, k, 0),
                                  kdesc(ys + h * 8192, k, 0), id_p2, k > 0 ? 1u : 0u);
                 mma_commit(p2_full);
-                if (!wait_or_abort(e_ready, pi, abort_flag, a.hdr)) break;
-                const int cb = (nchunks - 1 - it) & 1;  // state operand buffer of this chunk
-                if (!wait_or_abort(&g_ready[cb], ph, abort_flag, a.hdr)) break;
-                if (it >= 1 && !wait_or_abort(o_free, pi ^ 1, abort_flag, a.hdr)) break;
+            }
+        }
+    } else if (warp == 18) {
+        // ------------------------------------------------ MMA issuer: DX, dB
+        if (lane == 0) {
+            const uint32_t id_dx1 = idesc_bf16(64, 128, 1, 1);
+            const uint32_t id_dx2 = idesc_bf16(64, 128, 0, 0);
+            const uint32_t id_db = idesc_bf16(64, N, 0, 1);
+            const uint32_t l0 = smem_u32(sm + Lay::OFF_L0);
+            const uint32_t p2m = smem_u32(sm + Lay::OFF_P2M);
+            const uint32_t gb = smem_u32(sm + Lay::OFF_G);
+            for (int it = 0; it < nchunks; ++it) {
+                const int s = it & 1, ph = (it >> 1) & 1;
+                if (!wait_or_abort(&xg_ready[s], ph, abort_flag, a.hdr)) break;
+                if (!wait_or_abort(g_ready, it & 1, abort_flag, a.hdr)) break;
                 if (!wait_or_abort(l0_full, it & 1, abort_flag, a.hdr)) break;
+                if (it >= 1 && !wait_or_abort(dx_free, (it - 1) & 1, abort_flag, a.hdr)) break;
                 tc_fence_after();
-                const uint32_t l0 = smem_u32(sm + Lay::OFF_T1);
-                const uint32_t p2m = smem_u32(sm + Lay::OFF_T0);
-                const uint32_t gb = smem_u32(sm + Lay::OFF_S + cb * Lay::SBUF);
-                // DX = L0T dyf + B Gs^T
+                const uint32_t xs = smem_u32(sm + Lay::OFF_STAGE + s * Lay::STAGE);
+                const uint32_t ys = xs + 16384, bs = xs + 32768, cs = bs + N * 128;
+                // DX = L0^T dyf + B Gs^T
 #pragma unroll
                 for (int k = 0; k < 4; ++k)
                     mma_bf16(tmem + T_DX, mdesc(l0, k, 0), mdesc(ys, k, 8192), id_dx1,
@@ -1397,7 +1421,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
                 for (int k = 0; k < N / 16; ++k)
                     mma_bf16(tmem + T_DX, kdesc(bs, k, 8192), kdesc(gb, k, 16384), id_dx2, 1u);
+                mma_commit(dx_full);
+                mma_commit(l0_free);
                 // dB = sum_h P2m_h C + xg_h Gs_h
+                if (!wait_or_abort(e_ready, it & 1, abort_flag, a.hdr)) break;
+                if (it >= 1 && !wait_or_abort(db_free, (it - 1) & 1, abort_flag, a.hdr)) break;
+                tc_fence_after();
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
 #pragma unroll
@@ -1409,147 +1438,134 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                         mma_bf16(tmem + T_DB, kdesc(xs + h * 8192, k, 0),
                                  mdesc(gb + h * 8192, k, 16384), id_db, 1u);
                 }
-                mma_commit(o_full);
-                mma_commit(l0_free);
+                mma_commit(db_full);
+                mma_commit(g_free);
+                mma_commit(p2m_free);
+                mma_commit(&empty[s]);
             }
         }
     } else {
-        const int ct = tid - 64;
+        const int ct = tid - 64;  // 0..511
         const int wg = ct >> 7;
         const int q = warp & 3;
-        const int r = 32 * q + lane;
-        const int rh = r >> 6, rp = r & 63;
-        const int t = 16 * q + (lane & 15);  // M=64 row (token)
-        const int hf = lane >> 4;            // M=64 column half of this lane
-        constexpr int NH = N / 2;
-        const int n0 = wg * NH;
         const uint32_t tq = tmem + ((uint32_t)(32 * q) << 16);
-        float Gs[NH];
-        float carry = 0.f;  // sum of (r - q) over the later chunks of the segment, head wg
-
-        // prologue: adjoint arriving at the segment end, factors of the last chunk, and
-        // kseg = <G_seg, H_end>: the pairs (s, u) of the quadratic form with s in or
-        // before this segment and u after it, which equals the sum over later tokens of
-        // r_u - q_u (both states come from the fp32 scans)
-        const int clast = nchunks - 1;
-        bwd_factors(F, si, a, h0, clast, bwd_load_raw(a, si, h0, clast, nchunks, ct), ct, lane);
-        {
-            const float sc = expf(-F.scal[((clast & 1) * 2 + rh) * 4 + 0]);
-            const float* Gin = a.adj + (((long long)seg * a.H + h0 + rh) * kP + rp) * N + n0;
-            const bool more = !(si.flags & SEG_LAST);
-            const float* Hend = a.A + (((long long)(seg + 1) * a.H + h0 + rh) * kP + rp) * N + n0;
-            float kp = 0.f;
-#pragma unroll
-            for (int i = 0; i < NH; i += 4) {
-                const float4 v = *reinterpret_cast<const float4*>(Gin + i);
-                if (more) {
-                    const float4 w = *reinterpret_cast<const float4*>(Hend + i);
-                    kp += v.x * w.x + v.y * w.y + v.z * w.z + v.w * w.w;
+        const int tt = 16 * q + (lane & 15);  // M=64 accumulator row (token)
+        const int hf = lane >> 4;             // M=64 column half of this lane
+        if (wg == 0) {
+            // ------------------------------------------------ factors, scaling
+            // thread (head, t); factors of processing index j (chunk nchunks - 1 - j) go
+            // to slot j % kDFS: f(t) = exp(s_t - m) (0 past the chunk's tokens),
+            // g(t) = delta_t exp(m - s_t), delta, half = -m
+            const int head = ct >> 6, t = ct & 63, hw = (ct >> 5) & 1;
+            auto load_raw = [&](int j) -> float {
+                const int cc = nchunks - 1 - j;
+                if (j >= nchunks || t >= si.len - cc * kQ) return 0.f;
+                return a.raw[(si.start + (long long)cc * kQ + t) * a.H + h0 + head];
+            };
+            auto factors = [&](int j, float rawv) {
+                const int cc = nchunks - 1 - j;
+                const int vc = min(kQ, si.len - cc * kQ);
+                float d = 0.f;
+                if (t < vc) d = softplus_f(rawv + a.delta_init);
+                float inc = warp_scan(d, lane);
+                if (lane == 31) red[head * 2 + hw] = inc;
+                named_sync(2 + head, 64);
+                if (hw) inc += red[head * 2];
+                const float send = red[head * 2] + red[head * 2 + 1];
+                const float half = 0.5f * send;
+                const int sl = j % kDFS;
+                fbuf[(sl * 2 + head) * 64 + t] = (t < vc) ? expf(half - inc) : 0.f;
+                gbuf[(sl * 2 + head) * 64 + t] = d * expf(inc - half);
+                dbuf[(sl * 2 + head) * 64 + t] = d;
+                if (t == 0) {
+                    scal[(sl * 2 + head) * 4 + 0] = half;
+                    if (send > kMaxChunkDecay) set_status(a.hdr, SSD_ERR_DEVICE);
                 }
-                Gs[i] = v.x * sc;
-                Gs[i + 1] = v.y * sc;
-                Gs[i + 2] = v.z * sc;
-                Gs[i + 3] = v.w * sc;
-            }
-            kp = warp_sum(kp);
-            if (lane == 0) F.red[8 + wg * 4 + q] = kp;  // partial of head q / 2
-        }
-        named_sync(1, kCT);
-        // for head wg (the head this warpgroup's dx rows belong to), summed in a fixed order
-        const float kseg = (F.red[8 + 2 * wg] + F.red[9 + 2 * wg]) +
-                           (F.red[12 + 2 * wg] + F.red[13 + 2 * wg]);
-        write_state<NH>(sm + Lay::OFF_S + (clast & 1) * Lay::SBUF, Gs, r, n0);
-        fence_proxy_async();
-        mbar_arrive(&g_ready[clast & 1]);
-        int pending_empty = -1;  // thread 0: stage whose reduce-add may still read shared memory
-
-        // stage x / dy scaling of chunk index `j` (processing order) into its stage
-        auto scale_chunk_tiles = [&](int j) {
-            const int cj = nchunks - 1 - j, sj = j & 1;
-            if (wait_or_abort(&full[sj], (j >> 1) & 1, abort_flag, a.hdr))
-                bwd_scale_stage(sm + Lay::OFF_STAGE + sj * Lay::STAGE, F.gbuf + (cj & 1) * 128,
-                                F.fbuf + (cj & 1) * 128, ct);
-            fence_proxy_async();
-            mbar_arrive(xg_ready);
-        };
-        scale_chunk_tiles(0);
-
-        for (int it = 0; it < nchunks; ++it) {
-            const int c = nchunks - 1 - it;
-            const int s = it & 1, ph = (it >> 1) & 1, pi = it & 1, fb = c & 1;
-            const int vc = min(kQ, si.len - c * kQ);
-            const long long tok0 = si.start + (long long)c * kQ;
-            unsigned char* st = sm + Lay::OFF_STAGE + s * Lay::STAGE;
-            // release the previous chunk's stage once its dB reduce-add has read it
-            if (ct == 0 && pending_empty >= 0) {
-                tma_store_wait_read<0>();
-                mbar_arrive(&empty[pending_empty]);
-                pending_empty = -1;
-            }
-            const float raw_next = bwd_load_raw(a, si, h0, c - 1, nchunks, ct);
-            const float rv = (t < vc) ? a.rtok[(tok0 + t) * a.H + h0 + wg] : 0.f;
-            // B: the masked P2 tile of head wg; then warpgroup 0 makes the factors of the
-            // next chunk
-            {
-                const bool ok = wait_or_abort(p2_full, pi, abort_flag, a.hdr);
-                tc_fence_after();
-                masked_tile(tq + T_P2 + wg * 64, sm + Lay::OFF_T0 + wg * 8192, t, hf, ok, false);
-                tc_fence_before();
-                fence_proxy_async();
-                mbar_arrive(e_ready);
-                if (wg == 0 && c > 0) bwd_factors_wg0(F, si, a, h0, c - 1, raw_next, ct, lane);
-            }
-            named_sync(1, kCT);  // the next chunk's factors are visible
-            // C: adjoint chain, Gs for the previous chunk
-            if (c > 0) {
-                const bool ok = wait_or_abort(s_full, pi, abort_flag, a.hdr);
-                tc_fence_after();
-                const float gam = expf(-(F.scal[(fb * 2 + rh) * 4] + F.scal[((fb ^ 1) * 2 + rh) * 4]));
-#pragma unroll
-                for (int c0 = 0; c0 < NH; c0 += 32) {
-                    uint32_t v[32];
-                    tmem_ld16(tq + T_SP + n0 + c0, *reinterpret_cast<uint32_t(*)[16]>(&v[0]));
-                    tmem_ld16(tq + T_SP + n0 + c0 + 16, *reinterpret_cast<uint32_t(*)[16]>(&v[16]));
-                    tmem_wait_ld_regs<32>(v);
-                    if (ok) {
-#pragma unroll
-                        for (int u = 0; u < 32; ++u) Gs[c0 + u] = gam * (Gs[c0 + u] + __uint_as_float(v[u]));
+                // every factor of the chunk is written before this warpgroup scales with
+                // them, and red is read before the next call rewrites it
+                named_sync(4, 128);
+                mbar_arrive(&fac_full[sl]);
+            };
+            factors(0, load_raw(0));
+            for (int it = 0; it < nchunks; ++it) {
+                const int s = it & 1, ph = (it >> 1) & 1, sl = it % kDFS;
+                const float raw_next = load_raw(it + 1);
+                if (wait_or_abort(&full[s], ph, abort_flag, a.hdr)) {
+                    uint4* xs = reinterpret_cast<uint4*>(sm + Lay::OFF_STAGE + s * Lay::STAGE);
+                    const float* gv = gbuf + sl * 128;
+                    const float* fv = fbuf + sl * 128;
+#pragma unroll 4
+                    for (int i = 0; i < 16; ++i) {
+                        const int idx = ct + 128 * i;  // [x h0 | x h1 | dy h0 | dy h1] 16-byte chunks
+                        const int tile = idx >> 9, hh = tile & 1, row = (idx >> 3) & 63;
+                        const float sc = (tile < 2) ? gv[hh * 64 + row] : fv[hh * 64 + row];
+                        xs[idx] = scale_chunk(xs[idx], sc);
                     }
                 }
-                tc_fence_before();
-            }
-            mbar_arrive(s_free);
-            // the previous chunk's state operand, in the other buffer (its previous reader,
-            // chunk c + 1's DX/dB, completed before the last epilogue)
-            if (c > 0) {
-                write_state<NH>(sm + Lay::OFF_S + ((c - 1) & 1) * Lay::SBUF, Gs, r, n0);
                 fence_proxy_async();
-                mbar_arrive(&g_ready[(c - 1) & 1]);
+                mbar_arrive(&xg_ready[s]);
+                if (it + 1 < nchunks) {
+                    const int jn = it + 1;
+                    if (jn >= kDFS)
+                        wait_or_abort(&fac_empty[jn % kDFS], ((jn / kDFS) - 1) & 1, abort_flag,
+                                      a.hdr);
+                    factors(jn, raw_next);
+                }
             }
-            // A for the next chunk: its tiles are scaled while this chunk's DX/dB MMAs run
-            if (it + 1 < nchunks) scale_chunk_tiles(it + 1);
-            // D: dx (head wg), q, dB (columns of this warpgroup), partial d_raw; lane half
-            // hf takes half of the dx columns and half of the dB columns
-            {
-                const bool ok = wait_or_abort(o_full, pi, abort_flag, a.hdr);
-                tc_fence_after();
-                const float gt = F.gbuf[(fb * 2 + wg) * 64 + (t & 63)];
-                const float dt = F.dbuf[(fb * 2 + wg) * 64 + (t & 63)];
-                const unsigned char* xrow = st + wg * 8192 + (t & 63) * 128;  // xg of head wg, row t
-                __nv_bfloat16* dxrow =
-                    static_cast<__nv_bfloat16*>(a.dx) + ((tok0 + t) * a.H + h0 + wg) * kP;
-                float qv = 0.f;
+        } else if (wg == 1) {
+            // ------------------------------------------------ P2 masks, dx, d_raw
+            // thread (token tt, head hf)
+            const float* rtok = a.rtok;
+            float carry = 0.f;  // sum of (r - q) over the later chunks of the segment, head hf
+            wait_or_abort(kseg_ready, 0, abort_flag, a.hdr);
+            const float kseg = (red[8 + 2 * hf] + red[9 + 2 * hf]) +
+                               (red[12 + 2 * hf] + red[13 + 2 * hf]);
+            for (int it = 0; it < nchunks; ++it) {
+                const int c = nchunks - 1 - it;
+                const int s = it & 1, sl = it % kDFS;
+                const int vc = min(kQ, si.len - c * kQ);
+                const long long tok0 = si.start + (long long)c * kQ;
+                const float rv = (tt < vc) ? rtok[(tok0 + tt) * a.H + h0 + hf] : 0.f;
+                // P2 of both heads (columns 32 hf' .. of head h in lane half hf'): masked to
+                // u >= t, bf16 into P2M once dB of the previous chunk has read it
                 {
-                    const int c0 = 32 * hf;
+                    bool ok = wait_or_abort(p2_full, it & 1, abort_flag, a.hdr);
+                    if (it >= 1)
+                        ok = wait_or_abort(p2m_free, (it - 1) & 1, abort_flag, a.hdr) && ok;
+                    tc_fence_after();
+                    masked_tile(tq + T_P2, sm + Lay::OFF_P2M, tt, hf, ok, false);
+                    masked_tile(tq + T_P2 + 64, sm + Lay::OFF_P2M + 8192, tt, hf, ok, false);
+                    tc_fence_before();
+                    fence_proxy_async();
+                    mbar_arrive(e_ready);
+                }
+                // dx = g DX and q = xg . DX for (token tt, head hf)
+                bool ok = wait_or_abort(&fac_full[sl], (it / kDFS) & 1, abort_flag, a.hdr);
+                ok = wait_or_abort(dx_full, it & 1, abort_flag, a.hdr) && ok;
+                tc_fence_after();
+                const float gt = gbuf[(sl * 2 + hf) * 64 + tt];
+                const float dt = dbuf[(sl * 2 + hf) * 64 + tt];
+                mbar_arrive(&fac_empty[sl]);
+                const unsigned char* xrow =
+                    sm + Lay::OFF_STAGE + s * Lay::STAGE + hf * 8192 + tt * 128;  // xg, row tt
+                __nv_bfloat16* dxrow =
+                    static_cast<__nv_bfloat16*>(a.dx) + ((tok0 + tt) * a.H + h0 + hf) * kP;
+                float qv = 0.f;
+#pragma unroll
+                for (int j = 0; j < 64; j += 32) {
                     uint32_t v[32];
-                    tmem_ld16x2<32>(tq + T_DX + wg * 64, &v[0]);
-                    tmem_ld16x2<32>(tq + T_DX + wg * 64 + 16, &v[16]);
+                    tmem_ld16x2<64>(tq + T_DX + j, &v[0]);
+                    tmem_ld16x2<64>(tq + T_DX + j + 16, &v[16]);
                     tmem_wait_ld_regs<32>(v);
+                    if (j == 32) {
+                        tc_fence_before();
+                        mbar_arrive(dx_free);
+                    }
                     if (ok) {
 #pragma unroll
                         for (int e = 0; e < 32; e += 8) {
                             const uint4 w = *reinterpret_cast<const uint4*>(
-                                xrow + ((((c0 + e) >> 3) ^ t) & 7) * 16);
+                                xrow + ((((j + e) >> 3) ^ tt) & 7) * 16);
                             const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
                             for (int i = 0; i < 4; ++i) {
@@ -1559,10 +1575,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                                 qv = fmaf(xf.y, __uint_as_float(v[e + 2 * i + 1]), qv);
                             }
                         }
-                        if (t < vc) {
+                        if (tt < vc) {
 #pragma unroll
                             for (int e = 0; e < 32; e += 8)
-                                *reinterpret_cast<uint4*>(dxrow + c0 + e) = make_uint4(
+                                *reinterpret_cast<uint4*>(dxrow + j + e) = make_uint4(
                                     pack_bf16(gt * __uint_as_float(v[e]), gt * __uint_as_float(v[e + 1])),
                                     pack_bf16(gt * __uint_as_float(v[e + 2]), gt * __uint_as_float(v[e + 3])),
                                     pack_bf16(gt * __uint_as_float(v[e + 4]), gt * __uint_as_float(v[e + 5])),
@@ -1570,67 +1586,167 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                         }
                     }
                 }
-                qv += __shfl_xor_sync(0xffffffffu, qv, 16);
-                // the partial dB tiles go into this stage's x / dy tiles once every thread
-                // has read its x row for q above and every MMA of the chunk is done
-                unsigned char* rtiles = st;
-                named_sync(1, kCT);
-                constexpr int HW = NH / 2;               // dB columns per lane half
-                constexpr int STEP = HW >= 32 ? 32 : 16;  // two loads in flight when possible
-#pragma unroll
-                for (int c0 = 0; c0 < HW; c0 += STEP) {
-                    uint32_t v[STEP];
-                    tmem_ld16x2<HW>(tq + T_DB + n0 + c0, &v[0]);
-                    if constexpr (STEP == 32) tmem_ld16x2<HW>(tq + T_DB + n0 + c0 + 16, &v[16]);
-                    tmem_wait_ld_regs<STEP>(v);
-                    {  // partial dB; rows past the chunk's tokens add zero
-                        const int n = n0 + HW * hf + c0;
-                        float val[STEP];
-#pragma unroll
-                        for (int u = 0; u < STEP; ++u) val[u] = (ok && t < vc) ? __uint_as_float(v[u]) : 0.f;
-                        stage_row16(rtiles, t, n, val);
-                        if constexpr (STEP == 32) stage_row16(rtiles, t, n + 16, val + 16);
-                    }
-                }
-                tc_fence_before();
-                mbar_arrive(o_free);
-                fence_proxy_async();
-                named_sync(1, kCT);
-                if (ct == 0) {
-                    for (int j = 0; j < N / 32; ++j)
-                        tma_reduce_add_3d(&map_acc, rtiles + j * 8192, j * 32, g, (int)tok0);
-                    tma_store_commit();
-                    pending_empty = s;  // released once the reduce-add has read the tiles
-                }
-                // q = xg . DX (xg = g x, so q = x . dx); x.(G B) = q / delta
+                mbar_arrive(&empty[s]);  // this warpgroup is done with the stage's xg rows
+                // d_raw = sigmoid(z) (q / delta - sum_{u >= t in the segment} (r - q) - kseg):
+                // suffix sums over the chunk's rows u >= t (16 rows per warp and head, then
+                // the later warps' totals), plus the later chunks' carry
                 const float xgb = (dt > 1e-30f) ? qv / dt : 0.f;
-                // suffix sums of (r - q) over the chunk's rows u >= t: a reverse scan over
-                // the 16 rows of this quadrant, plus the totals of the later quadrants
-                float suf = (t < vc) ? (rv - qv) : 0.f;
+                float suf = (ok && tt < vc) ? (rv - qv) : 0.f;
 #pragma unroll
                 for (int o = 1; o < 16; o <<= 1) {
                     const float nb = __shfl_down_sync(0xffffffffu, suf, o, 16);
                     if ((lane & 15) + o < 16) suf += nb;
                 }
-                if (lane == 0) rqs[wg * 4 + q] = suf;
-                named_sync(1, kCT);
+                if ((lane & 15) == 0) rqs[hf * 4 + q] = suf;
+                named_sync(6, 128);
                 float later = 0.f, tot = 0.f;
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
-                    const float x = rqs[wg * 4 + k];
+                    const float x = rqs[hf * 4 + k];
                     tot += x;
                     if (k > q) later += x;
                 }
+                named_sync(6, 128);  // rqs is rewritten by the next chunk
                 suf += later;
-                // d raw = sigmoid(raw + delta_init) d delta, sigmoid = 1 - exp(-delta)
-                if (ok && hf == 0 && t < vc)
-                    a.draw[(tok0 + t) * a.H + h0 + wg] = -expm1f(-dt) * (xgb - (carry + suf + kseg));
+                if (ok && tt < vc)
+                    a.draw[(tok0 + tt) * a.H + h0 + hf] =
+                        -expm1f(-dt) * (xgb - (carry + suf + kseg));
                 carry += tot;
-                if (ct != 0) mbar_arrive(&empty[s]);
             }
-            named_sync(1, kCT);  // rqs reuse
+        } else {
+            // ------------------------------------------------ adjoint chain, dB tiles
+            // Gs rows r = (head, p), columns [n0, n0 + N / 2) of this warpgroup; the state is
+            // kept as Gs_c = exp(s_end - m_c) G_c and rewritten in TMEM as
+            //   Gs_{c-1} = exp(-(half_c + half_{c-1})) (Gs_c + S'_c)
+            constexpr int NH = N / 2;
+            const int sct = ct - 256;         // 0..255
+            const int r = 32 * q + lane;
+            const int rh = r >> 6, rp = r & 63;
+            const int n0 = (wg - 2) * NH;
+            const uint32_t tcol = tq + T_G + n0;
+            uint32_t hp[NH / 2];  // bf16 pairs of the next chunk's operand
+            auto write_g = [&]() {
+                unsigned char* row = sm + Lay::OFF_G + r * 128;
+#pragma unroll
+                for (int c8 = 0; c8 < NH; c8 += 8) {
+                    const int n = n0 + c8;
+                    *reinterpret_cast<uint4*>(row + (n >> 6) * 16384 +
+                                              (((((n & 63) >> 3) ^ r) & 7) << 4)) =
+                        make_uint4(hp[c8 / 2], hp[c8 / 2 + 1], hp[c8 / 2 + 2], hp[c8 / 2 + 3]);
+                }
+                fence_proxy_async();
+                mbar_arrive(g_ready);
+            };
+            {
+                // adjoint arriving at the segment end, and kseg = <G_seg, H_end>: the pairs of
+                // the quadratic form with one end in or before this segment and the other
+                // after it (both states from the fp32 scans)
+                wait_or_abort(&fac_full[0], 0, abort_flag, a.hdr);
+                const float sc = expf(-scal[(0 * 2 + rh) * 4 + 0]);
+                const float* Gin = a.adj + (((long long)seg * a.H + h0 + rh) * kP + rp) * N + n0;
+                const bool more = !(si.flags & SEG_LAST);
+                const float* Hend =
+                    a.A + (((long long)(seg + 1) * a.H + h0 + rh) * kP + rp) * N + n0;
+                float kp = 0.f;
+#pragma unroll
+                for (int c0 = 0; c0 < NH; c0 += 16) {
+                    float h[16];
+#pragma unroll
+                    for (int i = 0; i < 16; i += 4) {
+                        const float4 v = *reinterpret_cast<const float4*>(Gin + c0 + i);
+                        if (more) {
+                            const float4 w = *reinterpret_cast<const float4*>(Hend + c0 + i);
+                            kp += v.x * w.x + v.y * w.y + v.z * w.z + v.w * w.w;
+                        }
+                        h[i] = v.x * sc;
+                        h[i + 1] = v.y * sc;
+                        h[i + 2] = v.z * sc;
+                        h[i + 3] = v.w * sc;
+                    }
+                    tmem_st16(tcol + c0, reinterpret_cast<const uint32_t*>(h));
+#pragma unroll
+                    for (int i = 0; i < 16; i += 2) hp[(c0 + i) / 2] = pack_bf16(h[i], h[i + 1]);
+                }
+                kp = warp_sum(kp);
+                if (lane == 0) red[8 + (wg - 2) * 4 + q] = kp;  // partial of head q / 2
+                mbar_arrive(kseg_ready);
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(s_free);
+                write_g();
+            }
+            for (int it = 0; it < nchunks; ++it) {
+                const int c = nchunks - 1 - it;
+                const int sl = it % kDFS, sn = (it + 1) % kDFS;
+                const long long tok0 = si.start + (long long)c * kQ;
+                const int vc = min(kQ, si.len - c * kQ);
+                const bool more = it + 1 < nchunks;
+                // (a) Gs of the next chunk, in TMEM and as bf16 pairs in registers
+                if (more) {
+                    bool ok = wait_or_abort(&fac_full[sn], ((it + 1) / kDFS) & 1, abort_flag, a.hdr);
+                    const float gam = expf(-(scal[(sl * 2 + rh) * 4] + scal[(sn * 2 + rh) * 4]));
+                    ok = wait_or_abort(s_full, it & 1, abort_flag, a.hdr) && ok;
+                    tc_fence_after();
+#pragma unroll
+                    for (int c0 = 0; c0 < NH; c0 += 16) {
+                        uint32_t v[16];
+                        tmem_ld16(tcol + c0, *reinterpret_cast<uint32_t(*)[16]>(&v[0]));
+                        tmem_wait_ld_regs<16>(v);
+                        float h[16];
+#pragma unroll
+                        for (int u = 0; u < 16; ++u) h[u] = ok ? gam * __uint_as_float(v[u]) : 0.f;
+                        tmem_st16(tcol + c0, reinterpret_cast<const uint32_t*>(h));
+#pragma unroll
+                        for (int i = 0; i < 16; i += 2) hp[(c0 + i) / 2] = pack_bf16(h[i], h[i + 1]);
+                    }
+                    tmem_wait_st();
+                    tc_fence_before();
+                    mbar_arrive(s_free);
+                }
+                mbar_arrive(&fac_empty[sl]);
+                // (b) partial dB rows of this chunk -> staging -> reduce-add into the accumulator;
+                // rows past the chunk's tokens add zero
+                {
+                    bool ok = wait_or_abort(db_full, it & 1, abort_flag, a.hdr);
+                    tc_fence_after();
+                    if (sct == 0) tma_store_wait_read<0>();  // previous reduce-add has read staging
+                    named_sync(5, 256);
+                    constexpr int HW = NH / 2;               // dB columns per lane half
+                    constexpr int STEP = HW >= 32 ? 32 : 16;
+                    const int nb0 = (wg - 2) * NH;
+#pragma unroll
+                    for (int c0 = 0; c0 < HW; c0 += STEP) {
+                        uint32_t v[STEP];
+                        tmem_ld16x2<HW>(tq + T_DB + nb0 + c0, &v[0]);
+                        if constexpr (STEP == 32) tmem_ld16x2<HW>(tq + T_DB + nb0 + c0 + 16, &v[16]);
+                        tmem_wait_ld_regs<STEP>(v);
+                        const int n = nb0 + HW * hf + c0;
+                        float val[STEP];
+#pragma unroll
+                        for (int u = 0; u < STEP; ++u)
+                            val[u] = (ok && tt < vc) ? __uint_as_float(v[u]) : 0.f;
+                        stage_row16(sm + Lay::OFF_DB, tt, n, val);
+                        if constexpr (STEP == 32) stage_row16(sm + Lay::OFF_DB, tt, n + 16, val + 16);
+                    }
+                    tc_fence_before();
+                    mbar_arrive(db_free);
+                    fence_proxy_async();
+                    named_sync(5, 256);
+                    if (sct == 0) {
+                        for (int j = 0; j < N / 32; ++j)
+                            tma_reduce_add_3d(&map_acc, sm + Lay::OFF_DB + j * 8192, j * 32, g,
+                                              (int)tok0);
+                        tma_store_commit();
+                    }
+                }
+                // (c) the next chunk's bf16 operand, once DX and dB of this chunk have read it
+                if (more) {
+                    wait_or_abort(g_free, it & 1, abort_flag, a.hdr);
+                    write_g();
+                }
+            }
+            if (sct == 0) tma_store_wait_all<0>();
         }
-        if (ct == 0) tma_store_wait_all<0>();
     }
     tc_fence_before();
     __syncthreads();
@@ -1713,11 +1829,12 @@ cudaError_t backward_n(const Prob& pb, const Args& a, Launch& L) {
     tc_bwd_dc_kernel<N><<<grid, kBwdThreads, BwdLayout<N>::TOTAL, L.stream>>>(mx, mdy, mb, mc, mdc,
                                                                              a);
     if ((e = L.end()) != cudaSuccess) return e;
-    e = set_smem(tc_bwd_dxdb_kernel<N>, BwdLayout<N>::TOTAL);
+    static_assert(DxLayout<N>::TOTAL <= 232448, "dx/dB walk shared memory");
+    e = set_smem(tc_bwd_dxdb_kernel<N>, DxLayout<N>::TOTAL);
     if (e != cudaSuccess) return e;
     L.begin("tc_bwd_dxdb");
-    tc_bwd_dxdb_kernel<N><<<grid, kBwdThreads, BwdLayout<N>::TOTAL, L.stream>>>(mx, mdy, mb, mc,
-                                                                               mdb, a);
+    tc_bwd_dxdb_kernel<N><<<grid, kDxThreads, DxLayout<N>::TOTAL, L.stream>>>(mx, mdy, mb, mc,
+                                                                             mdb, a);
     if ((e = L.end()) != cudaSuccess) return e;
     return launch_dbc_convert(pb, a, L);
 }
