@@ -151,10 +151,13 @@ Layout make_layout(const Prob& b, bool bwd) {
         l.rtok = off;
         off = align_up(off + sizeof(float) * (size_t)b.T * b.H);
     }
-    l.l0 = 0;
+    l.l0 = l.fac = 0;
     if (b.tc) {  // one 64 x 64 bf16 tile per chunk slot of every segment and group
         l.l0 = off;
         off = align_up(off + (size_t)8192 * b.nseg_max * (b.Ls / b.Q) * b.G);
+        // one factor record per chunk slot and head
+        l.fac = off;
+        off = align_up(off + sizeof(float) * kFacRec * b.nseg_max * (b.Ls / b.Q) * b.H);
     }
     l.total = off;
     return l;
@@ -179,6 +182,7 @@ Args make_args(const Prob& b, const Layout& l, void* ws) {
         a.rtok = reinterpret_cast<float*>(base + l.rtok);
     }
     if (l.l0) a.l0 = reinterpret_cast<unsigned char*>(base + l.l0);
+    if (l.fac) a.fac = reinterpret_cast<float*>(base + l.fac);
     a.T = b.T;
     a.rowlen = b.rowlen;
     a.nseg_max = b.nseg_max;

@@ -46,7 +46,7 @@ struct Prob {
 
 // Byte offsets of the workspace regions.
 struct Layout {
-    size_t header, segtab, A, lam, adj, rq, rqsuf, dbacc, dcacc, rtok, l0, total;
+    size_t header, segtab, A, lam, adj, rq, rqsuf, dbacc, dcacc, rtok, l0, fac, total;
 };
 
 // Everything a kernel needs; passed by value.
@@ -74,11 +74,17 @@ struct Args {
     float* dcacc;   // [T][G][N] fp32
     float* rtok;    // [T][H] fp32: dy_t . y_t per token and head (tensor-core backward)
     unsigned char* l0;  // tensor-core path: [nseg_max][Ls / Q][G] 8 KB tiles, masked C B^T per chunk
+    float* fac;         // tensor-core path: [nseg_max][Ls / Q][H] chunk factor records (kFacRec floats)
     long long T, rowlen;
     long long nseg_max;
     int nseq, H, P, N, G, Q, Ls;
     float delta_init;
 };
+
+// Chunk factor record of one chunk and head (tensor-core path, chunk length 64):
+// f[64], g[64], delta[64], half, then padding to a multiple of 16 bytes.
+constexpr int kFacRec = 196;
+enum { FAC_F = 0, FAC_G = 64, FAC_D = 128, FAC_HALF = 192 };
 
 // Launch bookkeeping: counts kernels and, when profiling is on, brackets
 // each launch with events on the launch stream.

@@ -361,20 +361,58 @@ constexpr int l0_smem_bytes() {
     return 2 * (2 * N * 128) + 8 * 8 + 16 + 1024;
 }
 
+// ================================================================ chunk factors
+// Per chunk (up to 64 tokens of one segment) and head: delta_t = softplus(raw_t +
+// delta_init), the chunk-local log-decay s_t = -sum_{k<=t} delta_k, the reference point
+// m = s_end / 2, and f(t) = exp(s_t - m) (zero past the chunk's tokens), g(t) = delta_t
+// exp(m - s_t), half = -m.  With them exp(s_t - s_s) = f(t) g(s) / delta_s keeps every
+// exponent within |s_end| / 2.  The walks of both passes copy these records instead of
+// recomputing them.  One CTA per chunk slot and pair of heads.
+constexpr int kFacThreads = 128;
+
+__global__ void __launch_bounds__(kFacThreads) tc_factors_kernel(Args a) {
+    const int cps = a.Ls / kQ;
+    const int seg = blockIdx.x / cps, c = blockIdx.x % cps;
+    if (seg >= a.hdr->nseg) return;
+    const SegInfo si = a.segtab[seg];
+    if (c >= (si.len + kQ - 1) / kQ) return;
+    __shared__ float red[4];
+    const int ct = threadIdx.x, lane = ct & 31, head = ct >> 6, t = ct & 63;
+    const int hw = (ct >> 5) & 1;
+    const int h = blockIdx.y * 2 + head;  // the head count is even on this path
+    const int vc = min(kQ, si.len - c * kQ);
+    float d = 0.f;
+    if (t < vc) d = softplus_f(a.raw[(si.start + (long long)c * kQ + t) * a.H + h] + a.delta_init);
+    float inc = warp_scan(d, lane);
+    if (lane == 31) red[head * 2 + hw] = inc;
+    __syncthreads();
+    if (hw) inc += red[head * 2];
+    const float send = red[head * 2] + red[head * 2 + 1];  // sum of delta over the chunk
+    const float half = 0.5f * send;
+    float* rec = a.fac + ((long long)(seg * cps + c) * a.H + h) * kFacRec;
+    rec[FAC_F + t] = (t < vc) ? expf(half - inc) : 0.f;
+    rec[FAC_G + t] = d * expf(inc - half);
+    rec[FAC_D + t] = d;
+    if (t < 4) rec[FAC_HALF + t] = (t == 0) ? half : 0.f;
+    if (t == 0 && send > kMaxChunkDecay) set_status(a.hdr, SSD_ERR_DEVICE);
+}
+
 // ================================================================ chunk walk
 // x streams from HBM through a ring of kXS slots, refilled kXS - 1 chunks ahead of its
 // use (the load latency under full traffic is a few chunk periods); B, C and the L0
 // tile, shared by all heads of a group and mostly served by L2, use a ring of two.
-// Warps: 0 = TMA producer (x, B, C and the chunk's L0 tile), 1 = MMA issuer of the
-// state chain (G4), 18 = MMA issuer of the y path (G2, G3), 2..17 = four compute
-// warpgroups, each with its own task so that the tasks of neighbouring chunks overlap:
-//   warpgroup 0     factors of the next chunk, x -> g x of the current one;
+// Warps: 0 = TMA producer (x, B, C, the chunk's L0 tile and factor records), 1 = MMA
+// issuer of the state chain (G4), 18 = MMA issuer of the y path (G2, G3), 2..17 = four
+// compute warpgroups, each with its own task so that the tasks of neighbouring chunks
+// overlap:
+//   warpgroup 0     x -> g x;
 //   warpgroup 1     the y epilogue;
 //   warpgroups 2-3  the state update Hs <- gamma (Hs + S) and the G3 operand.
 // The groups hand work to each other and to the MMA warp through mbarriers only.
 constexpr int kCT = 256;  // compute threads of the backward walks (two warpgroups)
 constexpr int kWalkThreads = 64 + 4 * 128 + 32;
-constexpr int kFS = 4;    // factor slots (chunk c uses slot c % kFS)
+constexpr int kFS = 6;    // factor record slots (chunk c uses slot c % kFS)
+constexpr int kFSlot = 2 * kFacRec * 4;  // the records of the CTA's two heads
 constexpr int kXS = 4;    // x slots (chunk c uses slot c % kXS)
 
 template <int N>
@@ -387,11 +425,9 @@ struct WalkLayout {
     static constexpr int OFF_BC = kXS * XSLOT;
     static constexpr int OFF_H = OFF_BC + 2 * BCSLOT;       // 2 x (N/64) x 16K
     static constexpr int HBUF = (N / 64) * 16384;
-    static constexpr int OFF_F = OFF_H + 2 * HBUF;          // f, g: [slot][head][64] each
-    static constexpr int OFF_SC = OFF_F + 2 * kFS * 2 * 64 * 4;  // half: [slot][head][4]
-    static constexpr int OFF_RED = OFF_SC + kFS * 2 * 4 * 4;     // [4]
-    static constexpr int OFF_BAR = OFF_RED + 64;
-    static constexpr int NBAR = 40;
+    static constexpr int OFF_F = OFF_H + 2 * HBUF;          // factor records [slot][head]
+    static constexpr int OFF_BAR = OFF_F + kFS * kFSlot;
+    static constexpr int NBAR = 48;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr int TOTAL = OFF_MISC + 16 + 1024;  // + alignment slack
 };
@@ -418,10 +454,10 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
     extern __shared__ __align__(1024) unsigned char smraw[];
     unsigned char* sm = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smraw) + 1023) & ~(uintptr_t)1023);
-    float* fbuf = reinterpret_cast<float*>(sm + Lay::OFF_F);   // [slot][head][64]
-    float* gbuf = fbuf + kFS * 2 * 64;                         // [slot][head][64]
-    float* scal = reinterpret_cast<float*>(sm + Lay::OFF_SC);  // [slot][head][4]: half
-    float* red = reinterpret_cast<float*>(sm + Lay::OFF_RED);
+    // factor record of (slot, head): f[64], g[64], delta[64], half
+    auto frec = [&](int sl, int head) -> const float* {
+        return reinterpret_cast<const float*>(sm + Lay::OFF_F + sl * kFSlot) + head * kFacRec;
+    };
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + Lay::OFF_BAR);
     uint64_t* full_x = bars + 0;      // [kXS] x of a chunk landed
     uint64_t* empty_x = bars + 4;     // [kXS] x read by the MMAs
@@ -434,8 +470,8 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
     uint64_t* y_free = bars + 14;     // [2] Y read by warpgroup 1
     uint64_t* h_ready = bars + 16;    // [2] G3 operand written (state warps)
     uint64_t* h_free = bars + 18;     // [2] G3 operand read by the MMAs
-    uint64_t* fac_full = bars + 20;   // [kFS] factors of a chunk written (warpgroup 0)
-    uint64_t* fac_empty = bars + 24;  // [kFS] factors of a chunk no longer needed
+    uint64_t* fac_full = bars + 34;   // [kFS] factor records of a chunk landed
+    uint64_t* fac_empty = bars + 40;  // [kFS] factor records of a chunk no longer needed
     uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + Lay::OFF_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tslot + 1);
 
@@ -457,8 +493,8 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
         mbar_init(s_full, 1);
         mbar_init(s_free, 256);
         for (int i = 0; i < kFS; ++i) {
-            mbar_init(&fac_full[i], 128);
-            mbar_init(&fac_empty[i], 128 + 256);
+            mbar_init(&fac_full[i], 1);
+            mbar_init(&fac_empty[i], 128 + 128 + 256);
         }
         *abort_flag = 0;
         fence_mbar_init();
@@ -484,6 +520,15 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
                 tma_load_3d(st, &map_x, &full_x[xs], 0, h0, tok);
                 tma_load_3d(st + 8192, &map_x, &full_x[xs], 0, h0 + 1, tok);
             };
+            // the factor records of chunk cc (both heads, contiguous) into slot cc % kFS
+            auto load_fac = [&](int cc) {
+                const int fs = cc % kFS;
+                mbar_expect_tx(&fac_full[fs], kFSlot);
+                bulk_load(sm + Lay::OFF_F + fs * kFSlot,
+                          a.fac + ((long long)(seg * cps + cc) * a.H + h0) * kFacRec, kFSlot,
+                          &fac_full[fs]);
+            };
+            for (int cc = 0; cc < 2 && cc < nchunks; ++cc) load_fac(cc);
             for (int cc = 0; cc < kXS - 1 && cc < nchunks; ++cc) load_x(cc);
             for (int c = 0; c < nchunks; ++c) {
                 const int b = c & 1;
@@ -507,6 +552,14 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
                         !wait_or_abort(&empty_x[cx % kXS], ((cx / kXS) - 1) & 1, abort_flag, a.hdr))
                         break;
                     load_x(cx);
+                }
+                // factor records of chunk c + 2, into the slot chunk c + 2 - kFS used
+                const int cf = c + 2;
+                if (cf < nchunks) {
+                    if (cf >= kFS &&
+                        !wait_or_abort(&fac_empty[cf % kFS], ((cf / kFS) - 1) & 1, abort_flag, a.hdr))
+                        break;
+                    load_fac(cf);
                 }
             }
         }
@@ -578,59 +631,25 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
         const int q = warp & 3;         // TMEM lane quadrant
         const uint32_t trow = tmem + ((uint32_t)(32 * q) << 16);
         if (wg == 0) {
-            // ------------------------------------------------ factors, x -> g x
-            // thread (head, t): f(t) = exp(s_t - m), g(t) = delta_t exp(m - s_t),
-            // half = -m = (sum of delta) / 2, for chunk cc into slot cc % kFS
-            const int head = ct >> 6, t = ct & 63, hw = (ct >> 5) & 1;
-            auto load_raw = [&](int cc) -> float {
-                if (cc >= nchunks || t >= si.len - cc * kQ) return 0.f;
-                return a.raw[(si.start + (long long)cc * kQ + t) * a.H + h0 + head];
-            };
-            auto factors = [&](int cc, float rawv) {
-                const int vc = min(kQ, si.len - cc * kQ);
-                float d = 0.f;
-                if (t < vc) d = softplus_f(rawv + a.delta_init);
-                float inc = warp_scan(d, lane);
-                if (lane == 31) red[head * 2 + hw] = inc;
-                named_sync(2 + head, 64);
-                if (hw) inc += red[head * 2];
-                const float send = red[head * 2] + red[head * 2 + 1];  // sum of delta
-                const float half = 0.5f * send;
-                const int sl = cc % kFS;
-                fbuf[(sl * 2 + head) * 64 + t] = expf(half - inc);
-                gbuf[(sl * 2 + head) * 64 + t] = d * expf(inc - half);
-                if (t == 0) {
-                    scal[(sl * 2 + head) * 4 + 0] = half;
-                    if (send > kMaxChunkDecay) set_status(a.hdr, SSD_ERR_DEVICE);
-                }
-                // every g of the chunk is written before this warpgroup scales x with it
-                // (each thread reads rows other threads wrote), and red is read before the
-                // next call rewrites it
-                named_sync(4, 128);
-                mbar_arrive(&fac_full[sl]);
-            };
-            factors(0, load_raw(0));
+            // ------------------------------------------------ x -> g x
             for (int c = 0; c < nchunks; ++c) {
-                const int xsl = c % kXS, xph = (c / kXS) & 1;
-                const float raw_next = load_raw(c + 1);
-                if (wait_or_abort(&full_x[xsl], xph, abort_flag, a.hdr)) {
+                const int xsl = c % kXS, xph = (c / kXS) & 1, fs = c % kFS;
+                bool ok = wait_or_abort(&fac_full[fs], (c / kFS) & 1, abort_flag, a.hdr);
+                ok = wait_or_abort(&full_x[xsl], xph, abort_flag, a.hdr) && ok;
+                if (ok) {
                     uint4* xs = reinterpret_cast<uint4*>(sm + Lay::OFF_X + xsl * Lay::XSLOT);
-                    const float* gv = gbuf + (c % kFS) * 128;
+                    const float* g0 = frec(fs, 0) + FAC_G;
+                    const float* g1 = frec(fs, 1) + FAC_G;
 #pragma unroll
                     for (int i = 0; i < 8; ++i) {
                         const int idx = ct + 128 * i;  // head = idx / 512, row = (idx / 8) % 64
-                        xs[idx] = scale_chunk(xs[idx], gv[((idx >> 9) << 6) + ((idx >> 3) & 63)]);
+                        const int row = (idx >> 3) & 63;
+                        xs[idx] = scale_chunk(xs[idx], (idx >> 9) ? g1[row] : g0[row]);
                     }
                 }
                 fence_proxy_async();
                 mbar_arrive(&xg_ready[xsl]);
-                if (c + 1 < nchunks) {
-                    const int cn = c + 1;
-                    if (cn >= kFS)
-                        wait_or_abort(&fac_empty[cn % kFS], ((cn / kFS) - 1) & 1, abort_flag,
-                                      a.hdr);
-                    factors(cn, raw_next);
-                }
+                mbar_arrive(&fac_empty[fs]);
             }
         } else if (wg == 1) {
             // ------------------------------------------------ the y epilogue
@@ -644,7 +663,7 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
                 bool ok = wait_or_abort(&fac_full[sl], (cc / kFS) & 1, abort_flag, a.hdr);
                 ok = wait_or_abort(&y_full[s], ph, abort_flag, a.hdr) && ok;
                 tc_fence_after();
-                const float fv = fbuf[(sl * 2 + hf) * 64 + tt];
+                const float fv = frec(sl, hf)[FAC_F + tt];
                 mbar_arrive(&fac_empty[sl]);
                 uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.y) +
                                                       ((tok0 + tt) * a.H + h0 + hf) * kP);
@@ -698,7 +717,7 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
             };
             {
                 wait_or_abort(&fac_full[0], 0, abort_flag, a.hdr);
-                const float sc0 = expf(-scal[(0 * 2 + rh) * 4 + 0]);  // exp(m_0)
+                const float sc0 = expf(-frec(0, rh)[FAC_HALF]);  // exp(m_0)
                 const float* Hin = a.A + (((long long)seg * a.H + h0 + rh) * kP + rp) * N + n0;
 #pragma unroll
                 for (int c0 = 0; c0 < NH; c0 += 32) {
@@ -724,7 +743,7 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
             for (int c = 0; c + 1 < nchunks; ++c) {
                 const int sl = c % kFS, sn = (c + 1) % kFS;
                 bool ok = wait_or_abort(&fac_full[sn], ((c + 1) / kFS) & 1, abort_flag, a.hdr);
-                const float gam = expf(-(scal[(sl * 2 + rh) * 4] + scal[(sn * 2 + rh) * 4]));
+                const float gam = expf(-(frec(sl, rh)[FAC_HALF] + frec(sn, rh)[FAC_HALF]));
                 // the G3 operand buffer of chunk c + 1 was last read by G3 of chunk c - 1
                 if (c >= 1)
                     wait_or_abort(&h_free[(c + 1) & 1], ((c - 1) >> 1) & 1, abort_flag, a.hdr);
@@ -1223,16 +1242,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 }
 
 // ---------------------------------------------------------------- dX / dB walk
-// Chunks in reverse order.  Warps: 0 = TMA producer (x, dy, B, C; the chunk's L0 tile),
-// 1 = MMA issuer of S' and P2, 18 = MMA issuer of DX and dB, 2..17 = four compute
-// warpgroups with one task each:
-//   warpgroup 0     factors of the next chunk, x -> g x and dy -> f dy in place;
+// Chunks in reverse order.  Warps: 0 = TMA producer (x, dy, B, C; the chunk's L0 tile
+// and factor records), 1 = MMA issuer of S' and P2, 18 = MMA issuer of DX and dB,
+// 2..17 = four compute warpgroups with one task each:
+//   warpgroup 0     x -> g x and dy -> f dy in place, one chunk ahead;
 //   warpgroup 1     the masked P2 tiles, then dx = g DX, q = xg . DX and d_raw;
 //   warpgroups 2-3  the adjoint chain in TMEM (S' accumulates onto Gs there; these
 //                   warps rescale it by gamma), its bf16 operand, and the partial dB
 //                   tiles, added into the fp32 accumulator by TMA reduce-add.
 constexpr int kDxThreads = 64 + 4 * 128 + 32;
-constexpr int kDFS = 4;  // factor slots (processing index it uses slot it % kDFS)
+constexpr int kDFS = 4;  // factor record slots (processing index it uses slot it % kDFS)
 
 template <int N>
 struct DxLayout {
@@ -1242,9 +1261,8 @@ struct DxLayout {
     static constexpr int OFF_L0 = OFF_P2M + 16384;           // L0 tile (read as L0^T), 8K
     static constexpr int OFF_G = OFF_L0 + 8192;              // bf16 Gs operand, (N/64) x 16K
     static constexpr int OFF_DB = OFF_G + (N / 64) * 16384;  // fp32 dB staging, (N/32) x 8K
-    static constexpr int OFF_F = OFF_DB + N * 256;           // f, g, delta: [slot][head][64]
-    static constexpr int OFF_SC = OFF_F + 3 * kDFS * 2 * 64 * 4;  // half: [slot][head][4]
-    static constexpr int OFF_RQ = OFF_SC + kDFS * 2 * 4 * 4;      // [2 head][4 quadrant]
+    static constexpr int OFF_F = OFF_DB + N * 256;           // factor records [slot][head]
+    static constexpr int OFF_RQ = OFF_F + kDFS * kFSlot;          // [2 head][4 quadrant]
     static constexpr int OFF_RED = OFF_RQ + 64;                   // [16]
     static constexpr int OFF_BAR = OFF_RED + 64;
     static constexpr int NBAR = 40;
@@ -1270,12 +1288,12 @@ __global__ void __launch_bounds__(kDxThreads, 1)
     extern __shared__ __align__(1024) unsigned char smraw[];
     unsigned char* sm = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smraw) + 1023) & ~(uintptr_t)1023);
-    float* fbuf = reinterpret_cast<float*>(sm + Lay::OFF_F);  // [slot][head][64]
-    float* gbuf = fbuf + kDFS * 128;
-    float* dbuf = gbuf + kDFS * 128;
-    float* scal = reinterpret_cast<float*>(sm + Lay::OFF_SC);  // [slot][head][4]: half
+    // factor record of (slot, head): f[64], g[64], delta[64], half
+    auto frec = [&](int sl, int head) -> const float* {
+        return reinterpret_cast<const float*>(sm + Lay::OFF_F + sl * kFSlot) + head * kFacRec;
+    };
     float* rqs = reinterpret_cast<float*>(sm + Lay::OFF_RQ);   // [2 head][4]
-    float* red = reinterpret_cast<float*>(sm + Lay::OFF_RED);  // 0..3 factors, 8..15 kseg
+    float* red = reinterpret_cast<float*>(sm + Lay::OFF_RED);  // 8..15: kseg partials
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + Lay::OFF_BAR);
     uint64_t* full = bars + 0;        // [2] stage landed
     uint64_t* empty = bars + 2;       // [2] stage read by the MMAs and by the q epilogue
@@ -1323,8 +1341,8 @@ __global__ void __launch_bounds__(kDxThreads, 1)
         mbar_init(db_free, 256);
         mbar_init(kseg_ready, 256);
         for (int i = 0; i < kDFS; ++i) {
-            mbar_init(&fac_full[i], 128);
-            mbar_init(&fac_empty[i], 128 + 256);
+            mbar_init(&fac_full[i], 1);
+            mbar_init(&fac_empty[i], 128 + 128 + 256);
         }
         *abort_flag = 0;
         fence_mbar_init();
@@ -1342,6 +1360,15 @@ __global__ void __launch_bounds__(kDxThreads, 1)
         // ------------------------------------------------ TMA producer
         if (lane == 0) {
             const int cps = a.Ls / kQ;
+            // the factor records of processing index j (both heads) into slot j % kDFS
+            auto load_fac = [&](int j) {
+                const int fs = j % kDFS, cc = nchunks - 1 - j;
+                mbar_expect_tx(&fac_full[fs], kFSlot);
+                bulk_load(sm + Lay::OFF_F + fs * kFSlot,
+                          a.fac + ((long long)(seg * cps + cc) * a.H + h0) * kFacRec, kFSlot,
+                          &fac_full[fs]);
+            };
+            for (int j = 0; j < 2 && j < nchunks; ++j) load_fac(j);
             for (int it = 0; it < nchunks; ++it) {
                 const int c = nchunks - 1 - it, s = it & 1;
                 if (it >= 2 && !wait_or_abort(&empty[s], ((it >> 1) - 1) & 1, abort_flag, a.hdr))
@@ -1362,6 +1389,13 @@ __global__ void __launch_bounds__(kDxThreads, 1)
                 mbar_expect_tx(l0_full, 8192);
                 bulk_load(sm + Lay::OFF_L0, a.l0 + (((long long)seg * cps + c) * a.G + g) * 8192,
                           8192, l0_full);
+                const int jf = it + 2;
+                if (jf < nchunks) {
+                    if (jf >= kDFS && !wait_or_abort(&fac_empty[jf % kDFS], ((jf / kDFS) - 1) & 1,
+                                                     abort_flag, a.hdr))
+                        break;
+                    load_fac(jf);
+                }
             }
         }
     } else if (warp == 1) {
@@ -1452,65 +1486,29 @@ __global__ void __launch_bounds__(kDxThreads, 1)
         const int tt = 16 * q + (lane & 15);  // M=64 accumulator row (token)
         const int hf = lane >> 4;             // M=64 column half of this lane
         if (wg == 0) {
-            // ------------------------------------------------ factors, scaling
-            // thread (head, t); factors of processing index j (chunk nchunks - 1 - j) go
-            // to slot j % kDFS: f(t) = exp(s_t - m) (0 past the chunk's tokens),
-            // g(t) = delta_t exp(m - s_t), delta, half = -m
-            const int head = ct >> 6, t = ct & 63, hw = (ct >> 5) & 1;
-            auto load_raw = [&](int j) -> float {
-                const int cc = nchunks - 1 - j;
-                if (j >= nchunks || t >= si.len - cc * kQ) return 0.f;
-                return a.raw[(si.start + (long long)cc * kQ + t) * a.H + h0 + head];
-            };
-            auto factors = [&](int j, float rawv) {
-                const int cc = nchunks - 1 - j;
-                const int vc = min(kQ, si.len - cc * kQ);
-                float d = 0.f;
-                if (t < vc) d = softplus_f(rawv + a.delta_init);
-                float inc = warp_scan(d, lane);
-                if (lane == 31) red[head * 2 + hw] = inc;
-                named_sync(2 + head, 64);
-                if (hw) inc += red[head * 2];
-                const float send = red[head * 2] + red[head * 2 + 1];
-                const float half = 0.5f * send;
-                const int sl = j % kDFS;
-                fbuf[(sl * 2 + head) * 64 + t] = (t < vc) ? expf(half - inc) : 0.f;
-                gbuf[(sl * 2 + head) * 64 + t] = d * expf(inc - half);
-                dbuf[(sl * 2 + head) * 64 + t] = d;
-                if (t == 0) {
-                    scal[(sl * 2 + head) * 4 + 0] = half;
-                    if (send > kMaxChunkDecay) set_status(a.hdr, SSD_ERR_DEVICE);
-                }
-                // every factor of the chunk is written before this warpgroup scales with
-                // them, and red is read before the next call rewrites it
-                named_sync(4, 128);
-                mbar_arrive(&fac_full[sl]);
-            };
-            factors(0, load_raw(0));
-            for (int it = 0; it < nchunks; ++it) {
-                const int s = it & 1, ph = (it >> 1) & 1, sl = it % kDFS;
-                const float raw_next = load_raw(it + 1);
-                if (wait_or_abort(&full[s], ph, abort_flag, a.hdr)) {
+            // ------------------------------------------------ scaling
+            // x -> g x, dy -> f dy for processing index j (one chunk ahead of the masks)
+            auto scale = [&](int j) {
+                const int s = j & 1, fs = j % kDFS;
+                bool ok = wait_or_abort(&fac_full[fs], (j / kDFS) & 1, abort_flag, a.hdr);
+                ok = wait_or_abort(&full[s], (j >> 1) & 1, abort_flag, a.hdr) && ok;
+                if (ok) {
                     uint4* xs = reinterpret_cast<uint4*>(sm + Lay::OFF_STAGE + s * Lay::STAGE);
-                    const float* gv = gbuf + sl * 128;
-                    const float* fv = fbuf + sl * 128;
 #pragma unroll 4
                     for (int i = 0; i < 16; ++i) {
                         const int idx = ct + 128 * i;  // [x h0 | x h1 | dy h0 | dy h1] 16-byte chunks
-                        const int tile = idx >> 9, hh = tile & 1, row = (idx >> 3) & 63;
-                        const float sc = (tile < 2) ? gv[hh * 64 + row] : fv[hh * 64 + row];
-                        xs[idx] = scale_chunk(xs[idx], sc);
+                        const int tile = idx >> 9, row = (idx >> 3) & 63;
+                        const float* rec = frec(fs, tile & 1);
+                        xs[idx] = scale_chunk(xs[idx], (tile < 2) ? rec[FAC_G + row] : rec[FAC_F + row]);
                     }
                 }
                 fence_proxy_async();
                 mbar_arrive(&xg_ready[s]);
-                if (it + 1 < nchunks) {
-                    const int jn = it + 1;
-                    if (jn >= kDFS)
-                        wait_or_abort(&fac_empty[jn % kDFS], ((jn / kDFS) - 1) & 1, abort_flag,
-                                      a.hdr);
-                    factors(jn, raw_next);
-                }
+                mbar_arrive(&fac_empty[fs]);
+            };
+            scale(0);
+            for (int it = 0; it < nchunks; ++it) {
+                if (it + 1 < nchunks) scale(it + 1);
             }
         } else if (wg == 1) {
             // ------------------------------------------------ P2 masks, dx, d_raw
@@ -1526,25 +1524,24 @@ __global__ void __launch_bounds__(kDxThreads, 1)
                 const int vc = min(kQ, si.len - c * kQ);
                 const long long tok0 = si.start + (long long)c * kQ;
                 const float rv = (tt < vc) ? rtok[(tok0 + tt) * a.H + h0 + hf] : 0.f;
-                // P2 of both heads (columns 32 hf' .. of head h in lane half hf'): masked to
-                // u >= t, bf16 into P2M once dB of the previous chunk has read it
                 {
-                    bool ok = wait_or_abort(p2_full, it & 1, abort_flag, a.hdr);
-                    if (it >= 1)
-                        ok = wait_or_abort(p2m_free, (it - 1) & 1, abort_flag, a.hdr) && ok;
-                    tc_fence_after();
-                    masked_tile(tq + T_P2, sm + Lay::OFF_P2M, tt, hf, ok, false);
-                    masked_tile(tq + T_P2 + 64, sm + Lay::OFF_P2M + 8192, tt, hf, ok, false);
-                    tc_fence_before();
-                    fence_proxy_async();
-                    mbar_arrive(e_ready);
+                // P2 of both heads masked to u >= t, bf16 into P2M once dB of the previous
+                // chunk has read it (thread (token tt, column half hf) of each tile)
+                bool okm = wait_or_abort(p2_full, it & 1, abort_flag, a.hdr);
+                if (it >= 1) okm = wait_or_abort(p2m_free, (it - 1) & 1, abort_flag, a.hdr) && okm;
+                tc_fence_after();
+                masked_tile(tq + T_P2, sm + Lay::OFF_P2M, tt, hf, okm, false);
+                masked_tile(tq + T_P2 + 64, sm + Lay::OFF_P2M + 8192, tt, hf, okm, false);
+                tc_fence_before();
+                fence_proxy_async();
+                mbar_arrive(e_ready);
                 }
                 // dx = g DX and q = xg . DX for (token tt, head hf)
                 bool ok = wait_or_abort(&fac_full[sl], (it / kDFS) & 1, abort_flag, a.hdr);
                 ok = wait_or_abort(dx_full, it & 1, abort_flag, a.hdr) && ok;
                 tc_fence_after();
-                const float gt = gbuf[(sl * 2 + hf) * 64 + tt];
-                const float dt = dbuf[(sl * 2 + hf) * 64 + tt];
+                const float gt = frec(sl, hf)[FAC_G + tt];
+                const float dt = frec(sl, hf)[FAC_D + tt];
                 mbar_arrive(&fac_empty[sl]);
                 const unsigned char* xrow =
                     sm + Lay::OFF_STAGE + s * Lay::STAGE + hf * 8192 + tt * 128;  // xg, row tt
@@ -1642,7 +1639,7 @@ __global__ void __launch_bounds__(kDxThreads, 1)
                 // the quadratic form with one end in or before this segment and the other
                 // after it (both states from the fp32 scans)
                 wait_or_abort(&fac_full[0], 0, abort_flag, a.hdr);
-                const float sc = expf(-scal[(0 * 2 + rh) * 4 + 0]);
+                const float sc = expf(-frec(0, rh)[FAC_HALF]);
                 const float* Gin = a.adj + (((long long)seg * a.H + h0 + rh) * kP + rp) * N + n0;
                 const bool more = !(si.flags & SEG_LAST);
                 const float* Hend =
@@ -1684,7 +1681,7 @@ __global__ void __launch_bounds__(kDxThreads, 1)
                 // (a) Gs of the next chunk, in TMEM and as bf16 pairs in registers
                 if (more) {
                     bool ok = wait_or_abort(&fac_full[sn], ((it + 1) / kDFS) & 1, abort_flag, a.hdr);
-                    const float gam = expf(-(scal[(sl * 2 + rh) * 4] + scal[(sn * 2 + rh) * 4]));
+                    const float gam = expf(-(frec(sl, rh)[FAC_HALF] + frec(sn, rh)[FAC_HALF]));
                     ok = wait_or_abort(s_full, it & 1, abort_flag, a.hdr) && ok;
                     tc_fence_after();
 #pragma unroll
@@ -1704,7 +1701,13 @@ __global__ void __launch_bounds__(kDxThreads, 1)
                     mbar_arrive(s_free);
                 }
                 mbar_arrive(&fac_empty[sl]);
-                // (b) partial dB rows of this chunk -> staging -> reduce-add into the accumulator;
+                // (b) the next chunk's bf16 operand, as soon as DX and dB of this chunk have read
+                // the current one (DX of the next chunk waits for it)
+                if (more) {
+                    wait_or_abort(g_free, it & 1, abort_flag, a.hdr);
+                    write_g();
+                }
+                // (c) partial dB rows of this chunk -> staging -> reduce-add into the accumulator;
                 // rows past the chunk's tokens add zero
                 {
                     bool ok = wait_or_abort(db_full, it & 1, abort_flag, a.hdr);
@@ -1739,11 +1742,6 @@ __global__ void __launch_bounds__(kDxThreads, 1)
                         tma_store_commit();
                     }
                 }
-                // (c) the next chunk's bf16 operand, once DX and dB of this chunk have read it
-                if (more) {
-                    wait_or_abort(g_free, it & 1, abort_flag, a.hdr);
-                    write_g();
-                }
             }
             if (sct == 0) tma_store_wait_all<0>();
         }
@@ -1775,6 +1773,13 @@ cudaError_t launch_l0(const Prob& pb, const Args& a, Launch& L, const CUtensorMa
     return L.end();
 }
 
+cudaError_t launch_factors(const Prob& pb, const Args& a, Launch& L) {
+    const dim3 grid((unsigned)(pb.nseg_max * (pb.Ls / kQ)), pb.H / 2);
+    L.begin("tc_factors");
+    tc_factors_kernel<<<grid, kFacThreads, 0, L.stream>>>(a);
+    return L.end();
+}
+
 template <int N>
 cudaError_t forward_n(const Prob& pb, const Args& a, Launch& L) {
     CUtensorMap mx, mb, mc;
@@ -1784,6 +1789,7 @@ cudaError_t forward_n(const Prob& pb, const Args& a, Launch& L) {
     cudaError_t e = launch_seg_table(pb, a, L);
     if (e != cudaSuccess) return e;
     if ((e = launch_l0<N>(pb, a, L, mb, mc)) != cudaSuccess) return e;
+    if ((e = launch_factors(pb, a, L)) != cudaSuccess) return e;
     const dim3 grid((unsigned)pb.nseg_max, pb.H / 2);
     e = set_smem(tc_seg_state_kernel<N, 0>, state_smem_bytes(N));
     if (e != cudaSuccess) return e;
@@ -1810,6 +1816,7 @@ cudaError_t backward_n(const Prob& pb, const Args& a, Launch& L) {
     cudaError_t e = launch_seg_table(pb, a, L);
     if (e != cudaSuccess) return e;
     if ((e = launch_l0<N>(pb, a, L, mb, mc)) != cudaSuccess) return e;
+    if ((e = launch_factors(pb, a, L)) != cudaSuccess) return e;
     const dim3 grid((unsigned)pb.nseg_max, pb.H / 2);
     e = set_smem(tc_seg_state_kernel<N, 0>, state_smem_bytes(N));
     if (e != cudaSuccess) return e;
