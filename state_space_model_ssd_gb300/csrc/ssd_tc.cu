@@ -69,8 +69,8 @@ __global__ void __launch_bounds__(kStateThreads, 2)
         (reinterpret_cast<uintptr_t>(smraw) + 1023) & ~(uintptr_t)1023);
     unsigned char* stages = sm;
     float* wts = reinterpret_cast<float*>(sm + kStateStages * SB);   // [2][kWPad]
-    float* red = wts + 2 * kWPad;                                   // [8]
-    uint64_t* full = reinterpret_cast<uint64_t*>(red + 8);
+    float* csc = wts + 2 * kWPad;                                   // [2 head][16 chunk]
+    uint64_t* full = reinterpret_cast<uint64_t*>(csc + 32);
     uint64_t* empty = full + kStateStages;
     uint64_t* ready = empty + kStateStages;
     uint64_t* done = ready + kStateStages;
@@ -133,56 +133,46 @@ __global__ void __launch_bounds__(kStateThreads, 2)
             mma_commit(done);
         }
     } else {
-        // ---- compute warps: per-token weights relative to the segment end
-        const int ct = tid - 64;            // 0..255; the first 128 compute the weights
-        const int head = (ct >> 6) & 1;     // 0..1
-        const int j = ct & 63;              // 64 threads per head
-        const int per = (si.len + 63) / 64; // consecutive tokens per thread
-        const int t_lo = j * per;
-        if (ct < 128) {
+        // ---- compute warps: per-token weights from the chunk factor records.  With the
+        // records' g(t) = delta_t exp(inc_t - half_c) and f(t) = exp(half_c - inc_t)
+        // (inc_t = sum of delta over the chunk up to t, half_c = half the chunk's sum):
+        //   MODE 0: w_t = delta_t exp(-(sum of delta over (t, end]))
+        //              = g(t) exp(-half_c - 2 sum_{chunks c' > c} half_c'),
+        //   MODE 1: w_t = exp(-(sum of delta over [start, t]))
+        //              = f(t) exp(-half_c - 2 sum_{chunks c' < c} half_c').
+        const int ct = tid - 64;            // 0..255
+        const int cps = a.Ls / kQ;
+        if (ct < 32) {
+            const int head = ct >> 4, c = ct & 15;
+            const float hv = (c < nchunks)
+                                 ? a.fac[((long long)(seg * cps + c) * a.H + h0 + head) * kFacRec + FAC_HALF]
+                                 : 0.f;
+            // inclusive prefix over the head's 16 chunks (lanes 16 head .. 16 head + 15)
+            float pre = hv;
+#pragma unroll
+            for (int o = 1; o < 16; o <<= 1) {
+                const float nb = __shfl_up_sync(0xffffffffu, pre, o, 16);
+                if ((lane & 15) >= o) pre += nb;
+            }
+            const float tot = __shfl_sync(0xffffffffu, pre, 15, 16);
+            csc[head * 16 + c] = MODE == 0 ? expf(-hv - 2.f * (tot - pre)) : expf(-hv - 2.f * (pre - hv));
+            if (MODE == 0 && c == 0) a.lam[(long long)seg * a.H + h0 + head] = -2.f * tot;
+        }
+        named_sync(2, 256);
         {
-            // delta for the whole segment (2 heads x len tokens); unconditional loads
-            // (index clamped into the segment) so that all of them are in flight together
-            float v[2 * kMaxSeg / 128];
+            // 2 heads x len tokens; loads issued together, index clamped into the segment
+            float v[2 * kMaxSeg / 256];
 #pragma unroll
-            for (int k = 0; k < 2 * kMaxSeg / 128; ++k) {
-                const int i = ct + 128 * k, t = min(i >> 1, si.len - 1);
-                v[k] = __ldg(a.raw + (si.start + t) * a.H + h0 + (i & 1));
+            for (int k = 0; k < 2 * kMaxSeg / 256; ++k) {
+                const int i = ct + 256 * k, head = i >> 10, t = min(i & (kMaxSeg - 1), si.len - 1);
+                v[k] = __ldg(a.fac + ((long long)(seg * cps + (t >> 6)) * a.H + h0 + head) * kFacRec +
+                             (MODE == 0 ? FAC_G : FAC_F) + (t & 63));
             }
 #pragma unroll
-            for (int k = 0; k < 2 * kMaxSeg / 128; ++k) {
-                const int i = ct + 128 * k, t = i >> 1;
-                wts[(i & 1) * kWPad + widx(t)] =
-                    (t < si.len) ? softplus_f(v[k] + a.delta_init) : 0.f;
+            for (int k = 0; k < 2 * kMaxSeg / 256; ++k) {
+                const int i = ct + 256 * k, head = i >> 10, t = i & (kMaxSeg - 1);
+                if (t < si.len) wts[head * kWPad + widx(t)] = v[k] * csc[head * 16 + (t >> 6)];
             }
-        }
-        named_sync(1, 128);
-        float loc = 0.f;
-        for (int i = 0; i < per; ++i) {
-            const int t = t_lo + i;
-            if (t < kMaxSeg) loc += wts[head * kWPad + widx(t)];
-        }
-        // exclusive prefix of the per-thread sums across the head's 64 threads
-        float inc = warp_scan(loc, lane);
-        const int hw = (ct >> 5) & 1;  // warp within the head
-        if (lane == 31) red[head * 2 + hw] = inc;
-        named_sync(1, 128);
-        float excl = inc - loc + (hw ? red[head * 2] : 0.f);
-        const float total = red[head * 2] + red[head * 2 + 1];
-        // MODE 0: w_t = delta_t exp(-(sum of delta over (t, end]));
-        // MODE 1: w_t = exp(-(sum of delta over [start, t]))
-        float run = excl;
-        for (int i = 0; i < per; ++i) {
-            const int t = t_lo + i;
-            if (t < si.len) {
-                const float d = wts[head * kWPad + widx(t)];
-                run += d;
-                wts[head * kWPad + widx(t)] = MODE == 0 ? d * expf(run - total) : expf(-run);
-            } else if (t < kMaxSeg) {
-                wts[head * kWPad + widx(t)] = 0.f;
-            }
-        }
-        if (MODE == 0 && j == 0) a.lam[(long long)seg * a.H + h0 + head] = -total;
         }
         named_sync(2, 256);  // the weights are visible to all compute warps
         // ---- scale x by the weights in place, chunk by chunk
@@ -825,8 +815,7 @@ __device__ __forceinline__ uint64_t mdesc(uint32_t base, int k16, uint32_t lbo) 
     return sw128_desc(base + k16 * 2048, lbo, 1024);
 }
 
-// Per-chunk factors shared by both backward kernels (threads ct < 128 compute;
-// all kCT compute threads must call).
+// Per-chunk factors of the dC walk, two chunk buffers (copied from the records).
 struct ChunkFactors {
     float* fbuf;  // [2][2][64]
     float* gbuf;
@@ -835,41 +824,37 @@ struct ChunkFactors {
     float* red;
 };
 
-__device__ __forceinline__ void bwd_factors(const ChunkFactors& F, const SegInfo& si,
-                                            const Args& a, int h0, int cc, float rawv, int ct,
-                                            int lane) {
+// Thread ct < 128's values (head ct / 64, token ct % 64) of chunk cc's factor records,
+// loaded early so that the copy into shared memory does not wait for memory.
+struct FacVals {
+    float f, g, d, half;
+};
+__device__ __forceinline__ FacVals load_fac_vals(const Args& a, int seg, int h0, int cc,
+                                                 int nchunks, int ct) {
+    FacVals v = {0.f, 0.f, 0.f, 0.f};
+    if (ct < 128 && cc >= 0 && cc < nchunks) {
+        const int head = ct >> 6, t = ct & 63;
+        const float* rec =
+            a.fac + ((long long)(seg * (a.Ls / kQ) + cc) * a.H + h0 + head) * kFacRec;
+        v.f = rec[FAC_F + t];
+        v.g = rec[FAC_G + t];
+        v.d = rec[FAC_D + t];
+        v.half = rec[FAC_HALF];
+    }
+    return v;
+}
+// Stores chunk cc's factors into buffer cc & 1 (all kCT compute threads must call).
+__device__ __forceinline__ void bwd_factors(const ChunkFactors& F, const FacVals& v, int cc,
+                                            int ct) {
     named_sync(1, kCT);
     if (ct < 128) {
-        const int head = ct >> 6, t = ct & 63;
-        const int vc = min(kQ, si.len - cc * kQ);
-        float d = 0.f;
-        if (t < vc) d = softplus_f(rawv + a.delta_init);
-        float inc = warp_scan(d, lane);
-        const int hw = (ct >> 5) & 1;
-        if (lane == 31) F.red[head * 2 + hw] = inc;
-        named_sync(2 + head, 64);
-        if (hw) inc += F.red[head * 2];
-        const float send = F.red[head * 2] + F.red[head * 2 + 1];
-        const float half = 0.5f * send;
-        const int b = cc & 1;
-        // rows past the chunk's valid tokens (another sequence, or past T) get zero
-        // weight on both sides: f for dy, g (through delta = 0) for x
-        F.fbuf[(b * 2 + head) * 64 + t] = (t < vc) ? expf(half - inc) : 0.f;
-        F.gbuf[(b * 2 + head) * 64 + t] = d * expf(inc - half);
-        F.dbuf[(b * 2 + head) * 64 + t] = d;
-        if (t == 0) {
-            F.scal[(b * 2 + head) * 4 + 0] = half;
-            if (send > kMaxChunkDecay) set_status(a.hdr, SSD_ERR_DEVICE);
-        }
+        const int head = ct >> 6, t = ct & 63, b = cc & 1;
+        F.fbuf[(b * 2 + head) * 64 + t] = v.f;
+        F.gbuf[(b * 2 + head) * 64 + t] = v.g;
+        F.dbuf[(b * 2 + head) * 64 + t] = v.d;
+        if (t == 0) F.scal[(b * 2 + head) * 4 + 0] = v.half;
     }
     named_sync(1, kCT);
-}
-
-__device__ __forceinline__ float bwd_load_raw(const Args& a, const SegInfo& si, int h0, int cc,
-                                              int nchunks, int ct) {
-    const int head = ct >> 6, t = ct & 63;
-    if (ct >= 128 || cc < 0 || cc >= nchunks || t >= si.len - cc * kQ) return 0.f;
-    return a.raw[(si.start + (long long)cc * kQ + t) * a.H + h0 + head];
 }
 
 // x -> g x and dy -> f dy in place (the 4 bf16 tiles at the start of a stage).
@@ -1089,7 +1074,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const uint32_t tq = tmem + ((uint32_t)(32 * q) << 16);
         float Hs[NH];
 
-        bwd_factors(F, si, a, h0, 0, bwd_load_raw(a, si, h0, 0, nchunks, ct), ct, lane);
+        bwd_factors(F, load_fac_vals(a, seg, h0, 0, nchunks, ct), 0, ct);
         {
             const float sc0 = expf(-F.scal[(0 * 2 + rh) * 4 + 0]);
             const float* Hin = a.A + (((long long)seg * a.H + h0 + rh) * kP + rp) * N + n0;
@@ -1113,7 +1098,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             const int vc = min(kQ, si.len - c * kQ);
             const long long tok0 = si.start + (long long)c * kQ;
             unsigned char* st = sm + Lay::OFF_STAGE + s * Lay::STAGE;
-            const float raw_next = bwd_load_raw(a, si, h0, c + 1, nchunks, ct);
+            const FacVals fac_next = load_fac_vals(a, seg, h0, c + 1, nchunks, ct);
             // A: scale x and dy in place
             if (wait_or_abort(&full[s], ph, abort_flag, a.hdr))
                 bwd_scale_stage(st, F.gbuf + s * 128, F.fbuf + s * 128, ct);
@@ -1129,7 +1114,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             }
             // C: chunk state -> Hs for the next chunk (kept in registers until dC is done)
             if (!last) {
-                bwd_factors(F, si, a, h0, c + 1, raw_next, ct, lane);
+                bwd_factors(F, fac_next, c + 1, ct);
                 const bool ok = wait_or_abort(s_full, pc, abort_flag, a.hdr);
                 tc_fence_after();
                 const float gam = expf(-(F.scal[(s * 2 + rh) * 4] + F.scal[((s ^ 1) * 2 + rh) * 4]));
@@ -1506,10 +1491,7 @@ __global__ void __launch_bounds__(kDxThreads, 1)
                 mbar_arrive(&xg_ready[s]);
                 mbar_arrive(&fac_empty[fs]);
             };
-            scale(0);
-            for (int it = 0; it < nchunks; ++it) {
-                if (it + 1 < nchunks) scale(it + 1);
-            }
+            for (int j = 0; j < nchunks; ++j) scale(j);
         } else if (wg == 1) {
             // ------------------------------------------------ P2 masks, dx, d_raw
             // thread (token tt, head hf)
@@ -1752,7 +1734,7 @@ __global__ void __launch_bounds__(kDxThreads, 1)
 }
 
 constexpr int state_smem_bytes(int N) {
-    return kStateStages * StateSmem::stage_bytes(N) + 2 * kWPad * 4 + 32 + 3 * kStateStages * 8 +
+    return kStateStages * StateSmem::stage_bytes(N) + 2 * kWPad * 4 + 32 * 4 + 3 * kStateStages * 8 +
            8 + 16 + 1024;
 }
 
