@@ -1,8 +1,9 @@
 """Benchmark of the SSD scan on GB300: one JSON line on stdout (rank 0).
 
 A step is one pass of the whole hot path on one batch: ssd_forward followed by
-ssd_backward (chunk cumsum, chunk state, state passing, chunk scan and their
-backward) on the mamba-2.8b-layer training workload: batch 1, L = 32768,
+ssd_backward_after_forward, which takes the forward's segment states from the shared
+workspace (chunk cumsum, chunk state, state passing, chunk scan and their backward)
+on the mamba-2.8b-layer training workload: batch 1, L = 32768,
 80 heads x P = 64, N = 128, chunk 64, bf16 x/B/C/dy, fp32 raw_dt.  Inputs are
 synthetic and seeded (state_space_model_ssd_gb300.inputs); they are larger
 than L2, so no flush is needed between steps.
@@ -274,7 +275,7 @@ def gpu_arm(args, w, rank, world, dist):
             mid.record(stream)
         if w.backward:
             ssd.backward(dv["x"], dv["raw_dt"], dv["B"], dv["C"], dv["dy"], w.delta_init,
-                         w.chunk_size, cu, out=grads, workspace=ws)
+                         w.chunk_size, cu, out=grads, workspace=ws, after_forward=True)
             n += ssd.last_launch_count()
         return n
 

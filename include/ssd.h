@@ -52,7 +52,9 @@ typedef enum {
     SSD_ERR_INVALID_ARG = 1,   /* null pointer, bad size or inconsistent problem */
     SSD_ERR_UNSUPPORTED = 2,   /* valid problem outside the supported shape set */
     SSD_ERR_ALIGNMENT = 3,     /* a pointer is not 16-byte aligned (workspace: 256) */
-    SSD_ERR_WORKSPACE = 4,     /* workspace missing or smaller than ssd_workspace_size() */
+    SSD_ERR_WORKSPACE = 4,     /* workspace missing or smaller than ssd_workspace_size(); as a
+                                  device status: the workspace does not hold the forward that
+                                  ssd_backward_after_forward was told to reuse */
     SSD_ERR_CUDA = 5,          /* a CUDA runtime call failed (launch error) */
     SSD_ERR_TIMEOUT = 6,       /* a bounded device-side wait gave up (device status) */
     SSD_ERR_DEVICE = 7         /* device-side check failed, e.g. bad cu_seqlens (device status) */
@@ -106,6 +108,24 @@ ssd_status_t ssd_backward(const ssd_problem_t* prob, const void* x, const float*
                           const void* B, const void* C, const int32_t* cu_seqlens,
                           const void* dy, void* dx, float* d_raw_dt, void* dB, void* dC,
                           void* workspace, size_t workspace_bytes, void* stream);
+
+/* ssd_backward for the workspace that the preceding ssd_forward call used, on the same
+ * stream, with the same problem and the same x, raw_dt, B, C (and cu_seqlens) buffers,
+ * whose contents have not changed since.  On the tensor-core path it takes the
+ * forward's segment table, masked C B^T tiles, chunk factors and segment states from the
+ * workspace instead of recomputing them (activations saved by the forward, in the
+ * sense of page "Mamba-2架构与LaCT并行计算技术解析" §4.1); the results are those of
+ * ssd_backward.  The forward records its problem and input pointers in the workspace;
+ * if they differ from this call's, the device status becomes SSD_ERR_WORKSPACE and no
+ * gradient is computed (ssd_device_status reports it).  Buffer contents are not
+ * compared: changing them between the two calls gives the gradient at the old inputs.
+ * The forward's own device status is kept.  On the SIMT path this call is ssd_backward.
+ * workspace: >= ssd_workspace_size(prob, 1) bytes, passed to the forward as well. */
+ssd_status_t ssd_backward_after_forward(const ssd_problem_t* prob, const void* x,
+                                        const float* raw_dt, const void* B, const void* C,
+                                        const int32_t* cu_seqlens, const void* dy, void* dx,
+                                        float* d_raw_dt, void* dB, void* dC, void* workspace,
+                                        size_t workspace_bytes, void* stream);
 
 /* Size of the device scratch array that ssd_forward_noalloc works in. */
 #define SSD_NOALLOC_SCRATCH_BYTES (64u << 20)

@@ -127,8 +127,10 @@ def forward(x, raw_dt, B, C, delta_init: float, chunk_size: int = 64, cu_seqlens
 
 
 def backward(x, raw_dt, B, C, dy, delta_init: float, chunk_size: int = 64, cu_seqlens=None,
-             out=None, workspace=None, stream=None):
-    """Runs ssd_backward.  Returns a dict ``dx, d_raw_dt, dB, dC``."""
+             out=None, workspace=None, stream=None, after_forward: bool = False):
+    """Runs ssd_backward, or ssd_backward_after_forward when ``after_forward`` is set
+    (``workspace`` must then be the one the preceding forward on these inputs used).
+    Returns a dict ``dx, d_raw_dt, dB, dC``."""
     torch = _torch()
     dev = x.device
     _check_tensor(x, "x")
@@ -142,13 +144,16 @@ def backward(x, raw_dt, B, C, dy, delta_init: float, chunk_size: int = 64, cu_se
     if out is None:
         out = {"dx": torch.empty_like(x), "d_raw_dt": torch.empty_like(raw_dt),
                "dB": torch.empty_like(B), "dC": torch.empty_like(C)}
+    if after_forward and workspace is None:
+        raise ValueError("after_forward needs the forward's workspace")
     ws = _workspace(workspace_size(prob, True), dev, workspace)
+    name = "ssd_backward_after_forward" if after_forward else "ssd_backward"
     with torch.cuda.device(dev):
-        st = _lib.lib().ssd_backward(ctypes.byref(prob), _ptr(x), _ptr(raw_dt), _ptr(B),
-                                     _ptr(C), _ptr(cu_seqlens), _ptr(dy), _ptr(out["dx"]),
-                                     _ptr(out["d_raw_dt"]), _ptr(out["dB"]), _ptr(out["dC"]),
-                                     _ptr(ws), ws.numel(), _stream(stream))
-    check(st, "ssd_backward")
+        st = getattr(_lib.lib(), name)(ctypes.byref(prob), _ptr(x), _ptr(raw_dt), _ptr(B),
+                                       _ptr(C), _ptr(cu_seqlens), _ptr(dy), _ptr(out["dx"]),
+                                       _ptr(out["d_raw_dt"]), _ptr(out["dB"]), _ptr(out["dC"]),
+                                       _ptr(ws), ws.numel(), _stream(stream))
+    check(st, name)
     return out
 
 

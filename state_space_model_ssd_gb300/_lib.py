@@ -52,6 +52,8 @@ _SIGS = {
     "ssd_forward": (ctypes.c_int, [_PP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _SZ, _VP]),
     "ssd_backward": (ctypes.c_int, [_PP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP,
                                     _VP, _SZ, _VP]),
+    "ssd_backward_after_forward": (ctypes.c_int, [_PP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP,
+                                                  _VP, _VP, _VP, _SZ, _VP]),
     "ssd_forward_noalloc": (ctypes.c_int, [_PP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP]),
     "ssd_device_status": (ctypes.c_int, [_VP, _VP, ctypes.POINTER(ctypes.c_int32)]),
     "ssd_dispatch_path": (ctypes.c_char_p, [_PP, ctypes.c_int]),

@@ -136,6 +136,16 @@ Layout make_layout(const Prob& b, bool bwd) {
     off = align_up(off + sizeof(float) * (size_t)b.nseg_max * b.H * PN);
     l.lam = off;
     off = align_up(off + sizeof(float) * (size_t)b.nseg_max * b.H);
+    // regions both passes use come first, so that a forward's workspace is a prefix of
+    // the backward's (ssd_backward_after_forward reuses it)
+    l.l0 = l.fac = 0;
+    if (b.tc) {  // one 64 x 64 bf16 tile per chunk slot of every segment and group
+        l.l0 = off;
+        off = align_up(off + (size_t)8192 * b.nseg_max * (b.Ls / b.Q) * b.G);
+        // one factor record per chunk slot and head
+        l.fac = off;
+        off = align_up(off + sizeof(float) * kFacRec * b.nseg_max * (b.Ls / b.Q) * b.H);
+    }
     l.adj = l.rq = l.rqsuf = l.dbacc = l.dcacc = l.rtok = 0;
     if (bwd) {
         l.adj = off;
@@ -150,14 +160,6 @@ Layout make_layout(const Prob& b, bool bwd) {
         off = align_up(off + sizeof(float) * (size_t)b.T * b.G * b.N);
         l.rtok = off;
         off = align_up(off + sizeof(float) * (size_t)b.T * b.H);
-    }
-    l.l0 = l.fac = 0;
-    if (b.tc) {  // one 64 x 64 bf16 tile per chunk slot of every segment and group
-        l.l0 = off;
-        off = align_up(off + (size_t)8192 * b.nseg_max * (b.Ls / b.Q) * b.G);
-        // one factor record per chunk slot and head
-        l.fac = off;
-        off = align_up(off + sizeof(float) * kFacRec * b.nseg_max * (b.Ls / b.Q) * b.H);
     }
     l.total = off;
     return l;
@@ -194,6 +196,7 @@ Args make_args(const Prob& b, const Layout& l, void* ws) {
     a.Q = b.Q;
     a.Ls = b.Ls;
     a.delta_init = b.delta_init;
+    a.dtype = b.dtype;
     return a;
 }
 
@@ -248,7 +251,8 @@ const char* ssd_status_string(ssd_status_t s) {
         case SSD_ERR_INVALID_ARG: return "invalid argument";
         case SSD_ERR_UNSUPPORTED: return "unsupported problem shape";
         case SSD_ERR_ALIGNMENT: return "misaligned pointer";
-        case SSD_ERR_WORKSPACE: return "workspace missing or too small";
+        case SSD_ERR_WORKSPACE:
+            return "workspace missing or too small, or not holding the matching forward";
         case SSD_ERR_CUDA: return "CUDA runtime error";
         case SSD_ERR_TIMEOUT: return "device-side wait timed out";
         case SSD_ERR_DEVICE: return "device-side check failed";
@@ -315,10 +319,15 @@ ssd_status_t ssd_forward(const ssd_problem_t* prob, const void* x, const float* 
     return e == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
 }
 
-ssd_status_t ssd_backward(const ssd_problem_t* prob, const void* x, const float* raw_dt,
-                          const void* B, const void* C, const int32_t* cu_seqlens,
-                          const void* dy, void* dx, float* d_raw_dt, void* dB, void* dC,
-                          void* workspace, size_t workspace_bytes, void* stream) {
+}  // extern "C"
+
+namespace {
+
+ssd_status_t backward_impl(const ssd_problem_t* prob, const void* x, const float* raw_dt,
+                           const void* B, const void* C, const int32_t* cu_seqlens,
+                           const void* dy, void* dx, float* d_raw_dt, void* dB, void* dC,
+                           void* workspace, size_t workspace_bytes, void* stream,
+                           bool after_forward) {
     g_last_launches = 0;
     Prob b;
     Layout l;
@@ -343,16 +352,41 @@ ssd_status_t ssd_backward(const ssd_problem_t* prob, const void* x, const float*
     a.draw = d_raw_dt;
     a.dB = dB;
     a.dC = dC;
-    if (cudaMemsetAsync(a.hdr, 0, sizeof(WsHeader), s) != cudaSuccess) return SSD_ERR_CUDA;
+    // the tensor-core path can take the forward's segment table, tiles, factors and
+    // segment states from the workspace (its header is then kept, status included)
+    const bool reuse = after_forward && b.tc;
+    if (!reuse && cudaMemsetAsync(a.hdr, 0, sizeof(WsHeader), s) != cudaSuccess)
+        return SSD_ERR_CUDA;
     const size_t nbc = sizeof(float) * (size_t)b.T * b.G * b.N;
     if (cudaMemsetAsync(a.dbacc, 0, nbc, s) != cudaSuccess ||
         cudaMemsetAsync(a.dcacc, 0, nbc, s) != cudaSuccess)
         return SSD_ERR_CUDA;
     Launch L;
     L.stream = s;
-    cudaError_t e = b.tc ? tc_backward(b, a, L) : simt_backward(b, a, L);
+    cudaError_t e = b.tc ? tc_backward(b, a, L, reuse) : simt_backward(b, a, L);
     g_last_launches = L.count;
     return e == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+ssd_status_t ssd_backward(const ssd_problem_t* prob, const void* x, const float* raw_dt,
+                          const void* B, const void* C, const int32_t* cu_seqlens,
+                          const void* dy, void* dx, float* d_raw_dt, void* dB, void* dC,
+                          void* workspace, size_t workspace_bytes, void* stream) {
+    return backward_impl(prob, x, raw_dt, B, C, cu_seqlens, dy, dx, d_raw_dt, dB, dC, workspace,
+                         workspace_bytes, stream, false);
+}
+
+ssd_status_t ssd_backward_after_forward(const ssd_problem_t* prob, const void* x,
+                                        const float* raw_dt, const void* B, const void* C,
+                                        const int32_t* cu_seqlens, const void* dy, void* dx,
+                                        float* d_raw_dt, void* dB, void* dC, void* workspace,
+                                        size_t workspace_bytes, void* stream) {
+    return backward_impl(prob, x, raw_dt, B, C, cu_seqlens, dy, dx, d_raw_dt, dB, dC, workspace,
+                         workspace_bytes, stream, true);
 }
 
 ssd_status_t ssd_device_status(const void* workspace, void* stream, int32_t* device_status) {

@@ -26,7 +26,14 @@ enum { SEG_FIRST = 1, SEG_LAST = 2 };
 struct WsHeader {
     int status;   // first device-side error code (0 = none)
     int nseg;     // segments actually present
-    int pad[62];
+    // What the segment table was built for (written with it): the problem's sizes and
+    // the input pointers.  ssd_backward_after_forward checks it before reusing the
+    // forward's segment table, C B^T tiles, chunk factors and segment states.
+    int sig_valid;
+    int sig_dims[7];            // H, P, N, G, Ls, dtype, delta_init (bits)
+    long long sig_T;
+    const void* sig_ptr[5];     // x, raw_dt, B, C, cu_seqlens
+    int pad[42];
 };
 static_assert(sizeof(WsHeader) == 256, "WsHeader layout");
 
@@ -79,6 +86,7 @@ struct Args {
     long long nseg_max;
     int nseq, H, P, N, G, Q, Ls;
     float delta_init;
+    int dtype;
 };
 
 // Chunk factor record of one chunk and head (tensor-core path, chunk length 64):
@@ -100,11 +108,16 @@ cudaError_t simt_forward(const Prob& pb, const Args& a, Launch& L);
 cudaError_t simt_backward(const Prob& pb, const Args& a, Launch& L);
 // Tensor-core path (bf16, P = 64, N in {64, 128}, Q = 64, an even number of heads per group).
 cudaError_t tc_forward(const Prob& pb, const Args& a, Launch& L);
-cudaError_t tc_backward(const Prob& pb, const Args& a, Launch& L);
+// reuse_forward: the workspace holds the forward's segment table, C B^T tiles, chunk
+// factors and segment states for these inputs (checked on the device).
+cudaError_t tc_backward(const Prob& pb, const Args& a, Launch& L, bool reuse_forward = false);
 bool tc_supported(int dtype, int P, int N, int Q, int H, int G);
 
 // Shared small kernels (segment table, state scans, gradient epilogues).
 cudaError_t launch_seg_table(const Prob& pb, const Args& a, Launch& L);
+// Checks that the workspace's segment table was built for this problem and these inputs;
+// otherwise records SSD_ERR_WORKSPACE and empties the table, so that no kernel does work.
+cudaError_t launch_forward_match(const Prob& pb, const Args& a, Launch& L);
 cudaError_t launch_state_scan(const Prob& pb, const Args& a, Launch& L, bool write_final);
 cudaError_t launch_adjoint_scan(const Prob& pb, const Args& a, Launch& L);
 cudaError_t launch_bwd_epilogue(const Prob& pb, const Args& a, Launch& L);

@@ -88,7 +88,40 @@ __global__ void __launch_bounds__(kTableThreads) seg_table_kernel(Args a) {
         if (tid == (int)blockDim.x - 1) base_s += excl + cnt;
         __syncthreads();
     }
-    if (tid == 0) a.hdr->nseg = (int)(base_s < a.nseg_max ? base_s : a.nseg_max);
+    if (tid == 0) {
+        a.hdr->nseg = (int)(base_s < a.nseg_max ? base_s : a.nseg_max);
+        WsHeader* h = a.hdr;
+        h->sig_dims[0] = a.H;
+        h->sig_dims[1] = a.P;
+        h->sig_dims[2] = a.N;
+        h->sig_dims[3] = a.G;
+        h->sig_dims[4] = a.Ls;
+        h->sig_dims[5] = a.dtype;
+        h->sig_dims[6] = __float_as_int(a.delta_init);
+        h->sig_T = a.T;
+        h->sig_ptr[0] = a.x;
+        h->sig_ptr[1] = a.raw;
+        h->sig_ptr[2] = a.B;
+        h->sig_ptr[3] = a.C;
+        h->sig_ptr[4] = a.cu;
+        h->sig_valid = 1;
+    }
+}
+
+// One thread: does the header describe a segment table built for this problem and these
+// inputs?  If not, record SSD_ERR_WORKSPACE and empty the table.
+__global__ void forward_match_kernel(Args a) {
+    WsHeader* h = a.hdr;
+    const bool ok = h->sig_valid == 1 && h->sig_T == a.T && h->sig_dims[0] == a.H &&
+                    h->sig_dims[1] == a.P && h->sig_dims[2] == a.N && h->sig_dims[3] == a.G &&
+                    h->sig_dims[4] == a.Ls && h->sig_dims[5] == a.dtype &&
+                    h->sig_dims[6] == __float_as_int(a.delta_init) && h->sig_ptr[0] == a.x &&
+                    h->sig_ptr[1] == a.raw && h->sig_ptr[2] == a.B && h->sig_ptr[3] == a.C &&
+                    h->sig_ptr[4] == a.cu;
+    if (!ok) {
+        set_status(h, SSD_ERR_WORKSPACE);
+        h->nseg = 0;
+    }
 }
 
 constexpr int kScanThreads = 128;
@@ -222,6 +255,13 @@ cudaError_t launch_seg_table(const Prob& pb, const Args& a, Launch& L) {
     (void)pb;
     L.begin("seg_table");
     seg_table_kernel<<<1, kTableThreads, 0, L.stream>>>(a);
+    return L.end();
+}
+
+cudaError_t launch_forward_match(const Prob& pb, const Args& a, Launch& L) {
+    (void)pb;
+    L.begin("forward_match");
+    forward_match_kernel<<<1, 1, 0, L.stream>>>(a);
     return L.end();
 }
 

@@ -1789,23 +1789,29 @@ cudaError_t forward_n(const Prob& pb, const Args& a, Launch& L) {
 }
 
 template <int N>
-cudaError_t backward_n(const Prob& pb, const Args& a, Launch& L) {
+cudaError_t backward_n(const Prob& pb, const Args& a, Launch& L, bool reuse_forward) {
     CUtensorMap mx, mdy, mb, mc, mdb, mdc;
     if (!make_map(&mx, a.x, pb.T, pb.H, kP) || !make_map(&mdy, a.dy, pb.T, pb.H, kP) ||
         !make_map(&mb, a.B, pb.T, pb.G, N) || !make_map(&mc, a.C, pb.T, pb.G, N) ||
         !make_map_f32(&mdb, a.dbacc, pb.T, pb.G, N) || !make_map_f32(&mdc, a.dcacc, pb.T, pb.G, N))
         return cudaErrorInvalidValue;
-    cudaError_t e = launch_seg_table(pb, a, L);
-    if (e != cudaSuccess) return e;
-    if ((e = launch_l0<N>(pb, a, L, mb, mc)) != cudaSuccess) return e;
-    if ((e = launch_factors(pb, a, L)) != cudaSuccess) return e;
     const dim3 grid((unsigned)pb.nseg_max, pb.H / 2);
-    e = set_smem(tc_seg_state_kernel<N, 0>, state_smem_bytes(N));
-    if (e != cudaSuccess) return e;
-    L.begin("tc_fwd_state");
-    tc_seg_state_kernel<N, 0><<<grid, kStateThreads, state_smem_bytes(N), L.stream>>>(mx, mb, a);
-    if ((e = L.end()) != cudaSuccess) return e;
-    if ((e = launch_state_scan(pb, a, L, false)) != cudaSuccess) return e;
+    cudaError_t e;
+    if (reuse_forward) {
+        // the forward's segment table, tiles, factors and segment states are in the
+        // workspace; only check that they were made for these inputs
+        if ((e = launch_forward_match(pb, a, L)) != cudaSuccess) return e;
+    } else {
+        if ((e = launch_seg_table(pb, a, L)) != cudaSuccess) return e;
+        if ((e = launch_l0<N>(pb, a, L, mb, mc)) != cudaSuccess) return e;
+        if ((e = launch_factors(pb, a, L)) != cudaSuccess) return e;
+        e = set_smem(tc_seg_state_kernel<N, 0>, state_smem_bytes(N));
+        if (e != cudaSuccess) return e;
+        L.begin("tc_fwd_state");
+        tc_seg_state_kernel<N, 0><<<grid, kStateThreads, state_smem_bytes(N), L.stream>>>(mx, mb, a);
+        if ((e = L.end()) != cudaSuccess) return e;
+        if ((e = launch_state_scan(pb, a, L, false)) != cudaSuccess) return e;
+    }
     e = set_smem(tc_seg_state_kernel<N, 1>, state_smem_bytes(N));
     if (e != cudaSuccess) return e;
     L.begin("tc_bwd_adj_state");
@@ -1839,8 +1845,9 @@ cudaError_t tc_forward(const Prob& pb, const Args& a, Launch& L) {
     return pb.N == 128 ? forward_n<128>(pb, a, L) : forward_n<64>(pb, a, L);
 }
 
-cudaError_t tc_backward(const Prob& pb, const Args& a, Launch& L) {
-    return pb.N == 128 ? backward_n<128>(pb, a, L) : backward_n<64>(pb, a, L);
+cudaError_t tc_backward(const Prob& pb, const Args& a, Launch& L, bool reuse_forward) {
+    return pb.N == 128 ? backward_n<128>(pb, a, L, reuse_forward)
+                       : backward_n<64>(pb, a, L, reuse_forward);
 }
 
 }  // namespace ssd
