@@ -434,12 +434,28 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
                        const __grid_constant__ CUtensorMap map_b,
                        const __grid_constant__ CUtensorMap map_c, Args a) {
     using Lay = WalkLayout<N>;
-    const int seg = blockIdx.x;
-    const int h0 = blockIdx.y * 2;
-    if (seg >= a.hdr->nseg) return;
-    const SegInfo si = a.segtab[seg];
-    const int g = h0 / (a.H / a.G);
-    const int nchunks = (si.len + kQ - 1) / kQ;
+    // Persistent: the CTA takes items (segment, pair of heads) blockIdx.x, + gridDim.x, ...
+    // in segment-major order (neighbouring CTAs share B, C and the L0 tiles in L2).  Every
+    // role walks the same items; rings and mbarrier phases run on the CTA's global chunk
+    // count gc, so the next item's copies start while the current item's last chunks run.
+    const int nseg = a.hdr->nseg;
+    const int npairs = a.H / 2;
+    const int nitems = nseg * npairs;
+    if ((int)blockIdx.x >= nitems) return;
+    const int cps = a.Ls / kQ;
+    struct Item {
+        int seg, h0, g, nchunks;
+        SegInfo si;
+    };
+    auto item_of = [&](int it) -> Item {
+        Item r;
+        r.seg = it / npairs;
+        r.h0 = (it % npairs) * 2;
+        r.g = r.h0 / (a.H / a.G);
+        r.si = a.segtab[r.seg];
+        r.nchunks = (r.si.len + kQ - 1) / kQ;
+        return r;
+    };
 
     extern __shared__ __align__(1024) unsigned char smraw[];
     unsigned char* sm = reinterpret_cast<unsigned char*>(
@@ -501,55 +517,49 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
     if (warp == 0) {
         // ------------------------------------------------ TMA producer
         if (lane == 0) {
-            const int cps = a.Ls / kQ;
-            auto load_x = [&](int cc) {
-                const int xs = cc % kXS;
-                unsigned char* st = sm + Lay::OFF_X + xs * Lay::XSLOT;
-                const int tok = (int)(si.start + (long long)cc * kQ);
-                mbar_expect_tx(&full_x[xs], Lay::XSLOT);
-                tma_load_3d(st, &map_x, &full_x[xs], 0, h0, tok);
-                tma_load_3d(st + 8192, &map_x, &full_x[xs], 0, h0 + 1, tok);
-            };
-            // the factor records of chunk cc (both heads, contiguous) into slot cc % kFS
-            auto load_fac = [&](int cc) {
-                const int fs = cc % kFS;
-                mbar_expect_tx(&fac_full[fs], kFSlot);
-                bulk_load(sm + Lay::OFF_F + fs * kFSlot,
-                          a.fac + ((long long)(seg * cps + cc) * a.H + h0) * kFacRec, kFSlot,
-                          &fac_full[fs]);
-            };
-            for (int cc = 0; cc < 2 && cc < nchunks; ++cc) load_fac(cc);
-            for (int cc = 0; cc < kXS - 1 && cc < nchunks; ++cc) load_x(cc);
-            for (int c = 0; c < nchunks; ++c) {
-                const int b = c & 1;
-                // B, C and L0 of chunk c, into the slot chunk c - 2 used
-                if (c >= 2 && !wait_or_abort(&empty_bc[b], ((c >> 1) - 1) & 1, abort_flag, a.hdr))
-                    break;
-                unsigned char* st = sm + Lay::OFF_BC + b * Lay::BCSLOT;
-                const int tok = (int)(si.start + (long long)c * kQ);
-                mbar_expect_tx(&full_bc[b], Lay::BCSLOT);
-                for (int nb = 0; nb < N / 64; ++nb) {
-                    tma_load_3d(st + nb * 8192, &map_b, &full_bc[b], nb * 64, g, tok);
-                    tma_load_3d(st + Lay::C_IN_BC + nb * 8192, &map_c, &full_bc[b], nb * 64, g,
-                                tok);
-                }
-                bulk_load(st + Lay::L0_IN_BC,
-                          a.l0 + (((long long)seg * cps + c) * a.G + g) * 8192, 8192, &full_bc[b]);
-                // x of chunk c + kXS - 1, into the slot chunk c - 1 used
-                const int cx = c + kXS - 1;
-                if (cx < nchunks) {
-                    if (cx >= kXS &&
-                        !wait_or_abort(&empty_x[cx % kXS], ((cx / kXS) - 1) & 1, abort_flag, a.hdr))
+            int gc = 0;
+            bool stop = false;
+            for (int it = blockIdx.x; it < nitems && !stop; it += gridDim.x) {
+                const Item I = item_of(it);
+                for (int c = 0; c < I.nchunks; ++c, ++gc) {
+                    const int tok = (int)(I.si.start + (long long)c * kQ);
+                    // factor records (slot ring of kFS), x (ring of kXS), B / C / L0 (ring of 2)
+                    const int fs = gc % kFS;
+                    if (gc >= kFS &&
+                        !wait_or_abort(&fac_empty[fs], ((gc / kFS) - 1) & 1, abort_flag, a.hdr)) {
+                        stop = true;
                         break;
-                    load_x(cx);
-                }
-                // factor records of chunk c + 2, into the slot chunk c + 2 - kFS used
-                const int cf = c + 2;
-                if (cf < nchunks) {
-                    if (cf >= kFS &&
-                        !wait_or_abort(&fac_empty[cf % kFS], ((cf / kFS) - 1) & 1, abort_flag, a.hdr))
+                    }
+                    mbar_expect_tx(&fac_full[fs], kFSlot);
+                    bulk_load(sm + Lay::OFF_F + fs * kFSlot,
+                              a.fac + ((long long)(I.seg * cps + c) * a.H + I.h0) * kFacRec, kFSlot,
+                              &fac_full[fs]);
+                    const int xs = gc % kXS;
+                    if (gc >= kXS &&
+                        !wait_or_abort(&empty_x[xs], ((gc / kXS) - 1) & 1, abort_flag, a.hdr)) {
+                        stop = true;
                         break;
-                    load_fac(cf);
+                    }
+                    unsigned char* sx = sm + Lay::OFF_X + xs * Lay::XSLOT;
+                    mbar_expect_tx(&full_x[xs], Lay::XSLOT);
+                    tma_load_3d(sx, &map_x, &full_x[xs], 0, I.h0, tok);
+                    tma_load_3d(sx + 8192, &map_x, &full_x[xs], 0, I.h0 + 1, tok);
+                    const int b = gc & 1;
+                    if (gc >= 2 &&
+                        !wait_or_abort(&empty_bc[b], ((gc >> 1) - 1) & 1, abort_flag, a.hdr)) {
+                        stop = true;
+                        break;
+                    }
+                    unsigned char* st = sm + Lay::OFF_BC + b * Lay::BCSLOT;
+                    mbar_expect_tx(&full_bc[b], Lay::BCSLOT);
+                    for (int nb = 0; nb < N / 64; ++nb) {
+                        tma_load_3d(st + nb * 8192, &map_b, &full_bc[b], nb * 64, I.g, tok);
+                        tma_load_3d(st + Lay::C_IN_BC + nb * 8192, &map_c, &full_bc[b], nb * 64,
+                                    I.g, tok);
+                    }
+                    bulk_load(st + Lay::L0_IN_BC,
+                              a.l0 + (((long long)I.seg * cps + c) * a.G + I.g) * 8192, 8192,
+                              &full_bc[b]);
                 }
             }
         }
@@ -557,24 +567,36 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
         // ------------------------------------------------ MMA issuer: state chain
         if (lane == 0) {
             const uint32_t id_s = idesc_bf16(128, N, 1, 1);
-            for (int c = 0; c < nchunks; ++c) {
-                const int s = c & 1, ph = (c >> 1) & 1;
-                const int xsl = c % kXS, xph = (c / kXS) & 1;
-                if (c < nchunks - 1) {  // G4: Hs_c + S_c in the state columns
-                    if (!wait_or_abort(&full_bc[s], ph, abort_flag, a.hdr)) break;
-                    if (!wait_or_abort(&xg_ready[xsl], xph, abort_flag, a.hdr)) break;
-                    if (!wait_or_abort(s_free, c & 1, abort_flag, a.hdr)) break;
-                    tc_fence_after();
-                    const uint32_t xs = smem_u32(sm + Lay::OFF_X + xsl * Lay::XSLOT);
-                    const uint32_t bs = smem_u32(sm + Lay::OFF_BC + s * Lay::BCSLOT);
+            int gc = 0;
+            bool stop = false;
+            for (int it = blockIdx.x; it < nitems && !stop; it += gridDim.x) {
+                const Item I = item_of(it);
+                for (int c = 0; c < I.nchunks; ++c, ++gc) {
+                    const int s = gc & 1, ph = (gc >> 1) & 1;
+                    const int xsl = gc % kXS, xph = (gc / kXS) & 1;
+                    // One s_free and one s_full phase per chunk, also where no G4 is issued
+                    // (an item's last chunk), so that this warp and the state warps stay in
+                    // step: a parity wait must never be two phases behind its barrier.  The
+                    // slot waits keep the "slot read" arrivals below from running ahead.
+                    if (!wait_or_abort(&full_bc[s], ph, abort_flag, a.hdr) ||
+                        !wait_or_abort(&xg_ready[xsl], xph, abort_flag, a.hdr) ||
+                        !wait_or_abort(s_free, gc & 1, abort_flag, a.hdr)) {
+                        stop = true;
+                        break;
+                    }
+                    if (c < I.nchunks - 1) {  // G4: Hs_c + S_c in the state columns
+                        tc_fence_after();
+                        const uint32_t xs = smem_u32(sm + Lay::OFF_X + xsl * Lay::XSLOT);
+                        const uint32_t bs = smem_u32(sm + Lay::OFF_BC + s * Lay::BCSLOT);
 #pragma unroll
-                    for (int k = 0; k < kQ / 16; ++k)
-                        mma_bf16(tmem + kColS, sw128_desc(xs + k * 2048, 8192, 1024),
-                                 sw128_desc(bs + k * 2048, 8192, 1024), id_s, 1u);
+                        for (int k = 0; k < kQ / 16; ++k)
+                            mma_bf16(tmem + kColS, sw128_desc(xs + k * 2048, 8192, 1024),
+                                     sw128_desc(bs + k * 2048, 8192, 1024), id_s, 1u);
+                    }
                     mma_commit(s_full);
+                    mma_commit(&empty_x[xsl]);
+                    mma_commit(&empty_bc[s]);
                 }
-                mma_commit(&empty_x[xsl]);
-                mma_commit(&empty_bc[s]);
             }
         }
     } else if (warp == 18) {
@@ -582,37 +604,48 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
         if (lane == 0) {
             const uint32_t id_y = idesc_bf16(64, 128, 0, 1);
             const uint32_t id_h = idesc_bf16(64, 128, 0, 0);
-            for (int c = 0; c < nchunks; ++c) {
-                const int s = c & 1, ph = (c >> 1) & 1;
-                const int xsl = c % kXS, xph = (c / kXS) & 1;
-                if (!wait_or_abort(&full_bc[s], ph, abort_flag, a.hdr)) break;
-                if (!wait_or_abort(&xg_ready[xsl], xph, abort_flag, a.hdr)) break;
-                if (c >= 2 && !wait_or_abort(&y_free[s], ph ^ 1, abort_flag, a.hdr)) break;
-                tc_fence_after();
-                const uint32_t xs = smem_u32(sm + Lay::OFF_X + xsl * Lay::XSLOT);
-                const uint32_t bs = smem_u32(sm + Lay::OFF_BC + s * Lay::BCSLOT);
-                const uint32_t cs = bs + Lay::C_IN_BC;
-                const uint32_t l0 = bs + Lay::L0_IN_BC;
-                // G2: diagonal block
+            int gc = 0;
+            bool stop = false;
+            for (int it = blockIdx.x; it < nitems && !stop; it += gridDim.x) {
+                const Item I = item_of(it);
+                for (int c = 0; c < I.nchunks; ++c, ++gc) {
+                    const int s = gc & 1, ph = (gc >> 1) & 1;
+                    const int xsl = gc % kXS, xph = (gc / kXS) & 1;
+                    if (!wait_or_abort(&full_bc[s], ph, abort_flag, a.hdr) ||
+                        !wait_or_abort(&xg_ready[xsl], xph, abort_flag, a.hdr) ||
+                        (gc >= 2 && !wait_or_abort(&y_free[s], ph ^ 1, abort_flag, a.hdr))) {
+                        stop = true;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t xs = smem_u32(sm + Lay::OFF_X + xsl * Lay::XSLOT);
+                    const uint32_t bs = smem_u32(sm + Lay::OFF_BC + s * Lay::BCSLOT);
+                    const uint32_t cs = bs + Lay::C_IN_BC;
+                    const uint32_t l0 = bs + Lay::L0_IN_BC;
+                    // G2: diagonal block
 #pragma unroll
-                for (int k = 0; k < kQ / 16; ++k)
-                    mma_bf16(tmem + col_y(s), sw128_desc(l0 + k * 32, 16, 1024),
-                             sw128_desc(xs + k * 2048, 8192, 1024), id_y, k > 0 ? 1u : 0u);
-                mma_commit(&empty_x[xsl]);
-                // G3: state entering the chunk
-                if (!wait_or_abort(&h_ready[s], ph, abort_flag, a.hdr)) break;
-                tc_fence_after();
-                const uint32_t hs = smem_u32(sm + Lay::OFF_H + s * Lay::HBUF);
+                    for (int k = 0; k < kQ / 16; ++k)
+                        mma_bf16(tmem + col_y(s), sw128_desc(l0 + k * 32, 16, 1024),
+                                 sw128_desc(xs + k * 2048, 8192, 1024), id_y, k > 0 ? 1u : 0u);
+                    mma_commit(&empty_x[xsl]);
+                    // G3: state entering the chunk
+                    if (!wait_or_abort(&h_ready[s], ph, abort_flag, a.hdr)) {
+                        stop = true;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t hs = smem_u32(sm + Lay::OFF_H + s * Lay::HBUF);
 #pragma unroll
-                for (int k = 0; k < N / 16; ++k) {
-                    const uint32_t kc = (k >> 2) * 8192 + (k & 3) * 32;
-                    const uint32_t kh = (k >> 2) * 16384 + (k & 3) * 32;
-                    mma_bf16(tmem + col_y(s), sw128_desc(cs + kc, 16, 1024),
-                             sw128_desc(hs + kh, 16, 1024), id_h, 1u);
+                    for (int k = 0; k < N / 16; ++k) {
+                        const uint32_t kc = (k >> 2) * 8192 + (k & 3) * 32;
+                        const uint32_t kh = (k >> 2) * 16384 + (k & 3) * 32;
+                        mma_bf16(tmem + col_y(s), sw128_desc(cs + kc, 16, 1024),
+                                 sw128_desc(hs + kh, 16, 1024), id_h, 1u);
+                    }
+                    mma_commit(&y_full[s]);
+                    mma_commit(&h_free[s]);
+                    mma_commit(&empty_bc[s]);
                 }
-                mma_commit(&y_full[s]);
-                mma_commit(&h_free[s]);
-                mma_commit(&empty_bc[s]);
             }
         }
     } else {
@@ -622,63 +655,70 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
         const uint32_t trow = tmem + ((uint32_t)(32 * q) << 16);
         if (wg == 0) {
             // ------------------------------------------------ x -> g x
-            for (int c = 0; c < nchunks; ++c) {
-                const int xsl = c % kXS, xph = (c / kXS) & 1, fs = c % kFS;
-                bool ok = wait_or_abort(&fac_full[fs], (c / kFS) & 1, abort_flag, a.hdr);
-                ok = wait_or_abort(&full_x[xsl], xph, abort_flag, a.hdr) && ok;
-                if (ok) {
-                    uint4* xs = reinterpret_cast<uint4*>(sm + Lay::OFF_X + xsl * Lay::XSLOT);
-                    const float* g0 = frec(fs, 0) + FAC_G;
-                    const float* g1 = frec(fs, 1) + FAC_G;
+            int gc = 0;
+            for (int it = blockIdx.x; it < nitems; it += gridDim.x) {
+                const Item I = item_of(it);
+                for (int c = 0; c < I.nchunks; ++c, ++gc) {
+                    const int xsl = gc % kXS, xph = (gc / kXS) & 1, fs = gc % kFS;
+                    bool ok = wait_or_abort(&fac_full[fs], (gc / kFS) & 1, abort_flag, a.hdr);
+                    ok = wait_or_abort(&full_x[xsl], xph, abort_flag, a.hdr) && ok;
+                    if (ok) {
+                        uint4* xs = reinterpret_cast<uint4*>(sm + Lay::OFF_X + xsl * Lay::XSLOT);
+                        const float* g0 = frec(fs, 0) + FAC_G;
+                        const float* g1 = frec(fs, 1) + FAC_G;
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        const int idx = ct + 128 * i;  // head = idx / 512, row = (idx / 8) % 64
-                        const int row = (idx >> 3) & 63;
-                        xs[idx] = scale_chunk(xs[idx], (idx >> 9) ? g1[row] : g0[row]);
+                        for (int i = 0; i < 8; ++i) {
+                            const int idx = ct + 128 * i;  // head = idx / 512, row = (idx / 8) % 64
+                            const int row = (idx >> 3) & 63;
+                            xs[idx] = scale_chunk(xs[idx], (idx >> 9) ? g1[row] : g0[row]);
+                        }
                     }
+                    fence_proxy_async();
+                    mbar_arrive(&xg_ready[xsl]);
+                    mbar_arrive(&fac_empty[fs]);
                 }
-                fence_proxy_async();
-                mbar_arrive(&xg_ready[xsl]);
-                mbar_arrive(&fac_empty[fs]);
             }
         } else if (wg == 1) {
             // ------------------------------------------------ the y epilogue
             const int tt = 16 * q + (lane & 15);  // M=64 accumulator row (token)
             const int hf = lane >> 4;             // M=64 column half of this lane
-            // y of chunk cc: lane half hf holds head hf, p = 0..63 of token tt
-            auto drain_y = [&](int cc) {
-                const int s = cc & 1, ph = (cc >> 1) & 1, sl = cc % kFS;
-                const int vc = min(kQ, si.len - cc * kQ);
-                const long long tok0 = si.start + (long long)cc * kQ;
-                bool ok = wait_or_abort(&fac_full[sl], (cc / kFS) & 1, abort_flag, a.hdr);
-                ok = wait_or_abort(&y_full[s], ph, abort_flag, a.hdr) && ok;
-                tc_fence_after();
-                const float fv = frec(sl, hf)[FAC_F + tt];
-                mbar_arrive(&fac_empty[sl]);
-                uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.y) +
-                                                      ((tok0 + tt) * a.H + h0 + hf) * kP);
+            int gc = 0;
+            for (int it = blockIdx.x; it < nitems; it += gridDim.x) {
+                const Item I = item_of(it);
+                for (int c = 0; c < I.nchunks; ++c, ++gc) {
+                    // y of the chunk: lane half hf holds head hf, p = 0..63 of token tt
+                    const int s = gc & 1, ph = (gc >> 1) & 1, sl = gc % kFS;
+                    const int vc = min(kQ, I.si.len - c * kQ);
+                    const long long tok0 = I.si.start + (long long)c * kQ;
+                    bool ok = wait_or_abort(&fac_full[sl], (gc / kFS) & 1, abort_flag, a.hdr);
+                    ok = wait_or_abort(&y_full[s], ph, abort_flag, a.hdr) && ok;
+                    tc_fence_after();
+                    const float fv = frec(sl, hf)[FAC_F + tt];
+                    mbar_arrive(&fac_empty[sl]);
+                    uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.y) +
+                                                          ((tok0 + tt) * a.H + I.h0 + hf) * kP);
 #pragma unroll
-                for (int j = 0; j < 64; j += 32) {
-                    uint32_t v[32];
-                    tmem_ld16x2<64>(trow + col_y(s) + j, &v[0]);
-                    tmem_ld16x2<64>(trow + col_y(s) + j + 16, &v[16]);
-                    tmem_wait_ld_regs<32>(v);
-                    if (j == 32) {
-                        tc_fence_before();
-                        mbar_arrive(&y_free[s]);
-                    }
-                    if (ok && tt < vc) {
+                    for (int j = 0; j < 64; j += 32) {
+                        uint32_t v[32];
+                        tmem_ld16x2<64>(trow + col_y(s) + j, &v[0]);
+                        tmem_ld16x2<64>(trow + col_y(s) + j + 16, &v[16]);
+                        tmem_wait_ld_regs<32>(v);
+                        if (j == 32) {
+                            tc_fence_before();
+                            mbar_arrive(&y_free[s]);
+                        }
+                        if (ok && tt < vc) {
 #pragma unroll
-                        for (int e = 0; e < 32; e += 8)
-                            dst[(j + e) >> 3] = make_uint4(
-                                pack_bf16(fv * __uint_as_float(v[e]), fv * __uint_as_float(v[e + 1])),
-                                pack_bf16(fv * __uint_as_float(v[e + 2]), fv * __uint_as_float(v[e + 3])),
-                                pack_bf16(fv * __uint_as_float(v[e + 4]), fv * __uint_as_float(v[e + 5])),
-                                pack_bf16(fv * __uint_as_float(v[e + 6]), fv * __uint_as_float(v[e + 7])));
+                            for (int e = 0; e < 32; e += 8)
+                                dst[(j + e) >> 3] = make_uint4(
+                                    pack_bf16(fv * __uint_as_float(v[e]), fv * __uint_as_float(v[e + 1])),
+                                    pack_bf16(fv * __uint_as_float(v[e + 2]), fv * __uint_as_float(v[e + 3])),
+                                    pack_bf16(fv * __uint_as_float(v[e + 4]), fv * __uint_as_float(v[e + 5])),
+                                    pack_bf16(fv * __uint_as_float(v[e + 6]), fv * __uint_as_float(v[e + 7])));
+                        }
                     }
                 }
-            };
-            for (int c = 0; c < nchunks; ++c) drain_y(c);
+            }
         } else {
             // ------------------------------------------------ state chain
             // The state is kept pre-scaled for its next chunk, Hs_c = exp(m_c) H_c, in the
@@ -691,9 +731,9 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
             const int rh = r >> 6, rp = r & 63;
             const int n0 = (wg - 2) * NH;
             const uint32_t tcol = trow + kColS + n0;
-            // bf16 of 32 state values (columns n0 + c0 ..) into the G3 operand of chunk cc
-            auto write_h32 = [&](int cc, int c0, const float* h) {
-                unsigned char* hb = sm + Lay::OFF_H + (cc & 1) * Lay::HBUF + r * 128;
+            // bf16 of 32 state values (columns n0 + c0 ..) into the G3 operand of chunk gcc
+            auto write_h32 = [&](int gcc, int c0, const float* h) {
+                unsigned char* hb = sm + Lay::OFF_H + (gcc & 1) * Lay::HBUF + r * 128;
 #pragma unroll
                 for (int c8 = 0; c8 < 32; c8 += 8) {
                     const int n = n0 + c0 + c8;
@@ -705,61 +745,74 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
                                               (((((n & 63) >> 3) ^ r) & 7) << 4)) = v;
                 }
             };
-            {
-                wait_or_abort(&fac_full[0], 0, abort_flag, a.hdr);
-                const float sc0 = expf(-frec(0, rh)[FAC_HALF]);  // exp(m_0)
-                const float* Hin = a.A + (((long long)seg * a.H + h0 + rh) * kP + rp) * N + n0;
+            int gc = 0;
+            for (int it = blockIdx.x; it < nitems; it += gridDim.x) {
+                const Item I = item_of(it);
+                {
+                    // the item's first chunk: state entering the segment; its G3 operand
+                    // buffer was last read by G3 of global chunk gc - 2
+                    wait_or_abort(&fac_full[gc % kFS], (gc / kFS) & 1, abort_flag, a.hdr);
+                    if (gc >= 2)
+                        wait_or_abort(&h_free[gc & 1], ((gc - 2) >> 1) & 1, abort_flag, a.hdr);
+                    const float sc0 = expf(-frec(gc % kFS, rh)[FAC_HALF]);  // exp(m_0)
+                    const float* Hin =
+                        a.A + (((long long)I.seg * a.H + I.h0 + rh) * kP + rp) * N + n0;
 #pragma unroll
-                for (int c0 = 0; c0 < NH; c0 += 32) {
-                    float h[32];
+                    for (int c0 = 0; c0 < NH; c0 += 32) {
+                        float h[32];
 #pragma unroll
-                    for (int i = 0; i < 32; i += 4) {
-                        const float4 v = *reinterpret_cast<const float4*>(Hin + c0 + i);
-                        h[i] = v.x * sc0;
-                        h[i + 1] = v.y * sc0;
-                        h[i + 2] = v.z * sc0;
-                        h[i + 3] = v.w * sc0;
+                        for (int i = 0; i < 32; i += 4) {
+                            const float4 v = *reinterpret_cast<const float4*>(Hin + c0 + i);
+                            h[i] = v.x * sc0;
+                            h[i + 1] = v.y * sc0;
+                            h[i + 2] = v.z * sc0;
+                            h[i + 3] = v.w * sc0;
+                        }
+                        tmem_st16(tcol + c0, reinterpret_cast<const uint32_t*>(&h[0]));
+                        tmem_st16(tcol + c0 + 16, reinterpret_cast<const uint32_t*>(&h[16]));
+                        write_h32(gc, c0, h);
                     }
-                    tmem_st16(tcol + c0, reinterpret_cast<const uint32_t*>(&h[0]));
-                    tmem_st16(tcol + c0 + 16, reinterpret_cast<const uint32_t*>(&h[16]));
-                    write_h32(0, c0, h);
+                    tmem_wait_st();
+                    tc_fence_before();
+                    mbar_arrive(s_free);
+                    fence_proxy_async();
+                    mbar_arrive(&h_ready[gc & 1]);
                 }
-                tmem_wait_st();
-                tc_fence_before();
-                mbar_arrive(s_free);
-                fence_proxy_async();
-                mbar_arrive(&h_ready[0]);
-            }
-            for (int c = 0; c + 1 < nchunks; ++c) {
-                const int sl = c % kFS, sn = (c + 1) % kFS;
-                bool ok = wait_or_abort(&fac_full[sn], ((c + 1) / kFS) & 1, abort_flag, a.hdr);
-                const float gam = expf(-(frec(sl, rh)[FAC_HALF] + frec(sn, rh)[FAC_HALF]));
-                // the G3 operand buffer of chunk c + 1 was last read by G3 of chunk c - 1
-                if (c >= 1)
-                    wait_or_abort(&h_free[(c + 1) & 1], ((c - 1) >> 1) & 1, abort_flag, a.hdr);
-                ok = wait_or_abort(s_full, c & 1, abort_flag, a.hdr) && ok;
-                tc_fence_after();
+                for (int c = 0; c + 1 < I.nchunks; ++c, ++gc) {
+                    const int sl = gc % kFS, sn = (gc + 1) % kFS;
+                    bool ok = wait_or_abort(&fac_full[sn], ((gc + 1) / kFS) & 1, abort_flag, a.hdr);
+                    const float gam = expf(-(frec(sl, rh)[FAC_HALF] + frec(sn, rh)[FAC_HALF]));
+                    // the G3 operand buffer of chunk gc + 1 was last read by G3 of gc - 1
+                    if (gc >= 1)
+                        wait_or_abort(&h_free[(gc + 1) & 1], ((gc - 1) >> 1) & 1, abort_flag,
+                                      a.hdr);
+                    ok = wait_or_abort(s_full, gc & 1, abort_flag, a.hdr) && ok;
+                    tc_fence_after();
 #pragma unroll
-                for (int c0 = 0; c0 < NH; c0 += 32) {
-                    uint32_t v[32];
-                    tmem_ld16(tcol + c0, *reinterpret_cast<uint32_t(*)[16]>(&v[0]));
-                    tmem_ld16(tcol + c0 + 16, *reinterpret_cast<uint32_t(*)[16]>(&v[16]));
-                    tmem_wait_ld_regs<32>(v);
-                    float h[32];
+                    for (int c0 = 0; c0 < NH; c0 += 32) {
+                        uint32_t v[32];
+                        tmem_ld16(tcol + c0, *reinterpret_cast<uint32_t(*)[16]>(&v[0]));
+                        tmem_ld16(tcol + c0 + 16, *reinterpret_cast<uint32_t(*)[16]>(&v[16]));
+                        tmem_wait_ld_regs<32>(v);
+                        float h[32];
 #pragma unroll
-                    for (int u = 0; u < 32; ++u) h[u] = ok ? gam * __uint_as_float(v[u]) : 0.f;
-                    tmem_st16(tcol + c0, reinterpret_cast<const uint32_t*>(&h[0]));
-                    tmem_st16(tcol + c0 + 16, reinterpret_cast<const uint32_t*>(&h[16]));
-                    write_h32(c + 1, c0, h);
+                        for (int u = 0; u < 32; ++u) h[u] = ok ? gam * __uint_as_float(v[u]) : 0.f;
+                        tmem_st16(tcol + c0, reinterpret_cast<const uint32_t*>(&h[0]));
+                        tmem_st16(tcol + c0 + 16, reinterpret_cast<const uint32_t*>(&h[16]));
+                        write_h32(gc + 1, c0, h);
+                    }
+                    tmem_wait_st();
+                    tc_fence_before();
+                    mbar_arrive(s_free);
+                    mbar_arrive(&fac_empty[sl]);
+                    fence_proxy_async();
+                    mbar_arrive(&h_ready[(gc + 1) & 1]);
                 }
-                tmem_wait_st();
-                tc_fence_before();
-                mbar_arrive(s_free);
-                mbar_arrive(&fac_empty[sl]);
-                fence_proxy_async();
-                mbar_arrive(&h_ready[(c + 1) & 1]);
+                // the item's last chunk: no update, but its s_full phase is consumed
+                wait_or_abort(s_full, gc & 1, abort_flag, a.hdr);
+                mbar_arrive(&fac_empty[gc % kFS]);
+                ++gc;
             }
-            mbar_arrive(&fac_empty[(nchunks - 1) % kFS]);
         }
     }
     tc_fence_before();
@@ -1738,6 +1791,15 @@ constexpr int state_smem_bytes(int N) {
            8 + 16 + 1024;
 }
 
+// SMs of the current device (persistent grids take one CTA per SM).
+int sm_count() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1)
+        return 1;
+    return n;
+}
+
 template <typename K>
 cudaError_t set_smem(K kernel, int bytes) {
     return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
@@ -1783,8 +1845,11 @@ cudaError_t forward_n(const Prob& pb, const Args& a, Launch& L) {
     if (e != cudaSuccess) return e;
     e = set_smem(tc_fwd_walk_kernel<N>, WalkLayout<N>::TOTAL);
     if (e != cudaSuccess) return e;
+    // persistent: one CTA per SM, each walking items (segment, pair of heads)
+    const long long items = pb.nseg_max * (pb.H / 2);
+    const dim3 pgrid((unsigned)(items < sm_count() ? items : sm_count()));
     L.begin("tc_fwd_walk");
-    tc_fwd_walk_kernel<N><<<grid, kWalkThreads, WalkLayout<N>::TOTAL, L.stream>>>(mx, mb, mc, a);
+    tc_fwd_walk_kernel<N><<<pgrid, kWalkThreads, WalkLayout<N>::TOTAL, L.stream>>>(mx, mb, mc, a);
     return L.end();
 }
 
