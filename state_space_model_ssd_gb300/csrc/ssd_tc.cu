@@ -1144,19 +1144,31 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         fence_proxy_async();
         mbar_arrive(&h_ready[0]);
         int pending_empty = -1;  // thread 0: stage whose reduce-add may still read shared memory
+        // x -> g x and dy -> f dy of chunk cc in its stage (factors in buffer cc & 1)
+        auto scale_chunk_stage = [&](int cc) {
+            const int sc = cc & 1;
+            if (wait_or_abort(&full[sc], (cc >> 1) & 1, abort_flag, a.hdr))
+                bwd_scale_stage(sm + Lay::OFF_STAGE + sc * Lay::STAGE, F.gbuf + sc * 128,
+                                F.fbuf + sc * 128, ct);
+            fence_proxy_async();
+            mbar_arrive(xg_ready);
+        };
+        scale_chunk_stage(0);
 
         for (int c = 0; c < nchunks; ++c) {
             const int s = c & 1, ph = (c >> 1) & 1, pc = c & 1;
+            // release the previous chunk's stage once its dC reduce-add has read it (the
+            // next chunk's copy into it is waited for before this iteration's epilogue)
+            if (ct == 0 && pending_empty >= 0) {
+                tma_store_wait_read<0>();
+                mbar_arrive(&empty[pending_empty]);
+                pending_empty = -1;
+            }
             const bool last = (c == nchunks - 1);
             const int vc = min(kQ, si.len - c * kQ);
             const long long tok0 = si.start + (long long)c * kQ;
             unsigned char* st = sm + Lay::OFF_STAGE + s * Lay::STAGE;
             const FacVals fac_next = load_fac_vals(a, seg, h0, c + 1, nchunks, ct);
-            // A: scale x and dy in place
-            if (wait_or_abort(&full[s], ph, abort_flag, a.hdr))
-                bwd_scale_stage(st, F.gbuf + s * 128, F.fbuf + s * 128, ct);
-            fence_proxy_async();
-            mbar_arrive(xg_ready);
             // B: W_h = P1_h masked to s <= t (warpgroup h handles head h)
             {
                 const bool ok = wait_or_abort(p1_full, pc, abort_flag, a.hdr);
@@ -1192,6 +1204,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             } else {
                 mbar_arrive(s_free);
             }
+            // A for the next chunk: scaled now, so that its S and P1 MMAs run during this
+            // chunk's epilogue
+            if (!last) scale_chunk_stage(c + 1);
             // D: dC rows (both heads, this warpgroup's column half split over the two lane
             // halves), r partials
             {
@@ -1202,11 +1217,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 // the partial dC tiles go into this stage's x / dy tiles, which every MMA of
                 // the chunk has finished reading
                 unsigned char* rtiles = st;
-                if (ct == 0 && pending_empty >= 0) {
-                    tma_store_wait_read<0>();
-                    mbar_arrive(&empty[pending_empty]);
-                    pending_empty = -1;
-                }
 #pragma unroll
                 for (int c0 = 0; c0 < NH / 2; c0 += 16) {
                     const int n = n0 + (NH / 2) * hf + c0;
