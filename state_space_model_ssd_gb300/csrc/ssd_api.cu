@@ -197,6 +197,7 @@ Args make_args(const Prob& b, const Layout& l, void* ws) {
     a.Ls = b.Ls;
     a.delta_init = b.delta_init;
     a.dtype = b.dtype;
+    a.state_lm = l.l0 ? 1 : 0;
     return a;
 }
 

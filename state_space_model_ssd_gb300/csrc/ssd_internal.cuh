@@ -87,7 +87,18 @@ struct Args {
     int nseq, H, P, N, G, Q, Ls;
     float delta_init;
     int dtype;
+    int state_lm;   // A and adj stored lane-major (tensor-core path), see lm_row
 };
+
+// Segment states A / adj of one (segment, head) are P x N fp32.  The SIMT path keeps
+// them row-major.  The tensor-core path keeps them lane-major: in each block of 32
+// consecutive rows, columns 4k .. 4k+3 of row 32 b + l sit at float offset
+// (32 k + l) * 4 of the block, so the 32 lanes of a warp, which hold 32 consecutive
+// rows of a TMEM accumulator, move 512 contiguous bytes per float4.  lm_row gives
+// float4 0 of row p; float4 k of the row is lm_row(..) + 128 k.
+__host__ __device__ __forceinline__ long long lm_row(int p, int N) {
+    return (long long)(p & ~31) * N + (p & 31) * 4;
+}
 
 // Chunk factor record of one chunk and head (tensor-core path, chunk length 64):
 // f[64], g[64], delta[64], half, then padding to a multiple of 16 bytes.

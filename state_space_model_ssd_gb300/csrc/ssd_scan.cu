@@ -127,7 +127,8 @@ __global__ void forward_match_kernel(Args a) {
 constexpr int kScanThreads = 128;
 constexpr int kScanUnroll = 8;
 
-// Forward scan over segments, per head and per state element (4 per thread).
+// Forward scan over segments, per head and per state element (4 per thread; the
+// scan is the same for either storage order of the states).
 // On entry a.A holds the segment aggregates; on exit the state entering each
 // segment.  Optionally writes the state after the last segment of every
 // sequence to final_state.
@@ -138,6 +139,12 @@ __global__ void __launch_bounds__(kScanThreads) state_scan_kernel(Args a, int wr
     if (e4 >= PN4) return;
     const int nseg = a.hdr->nseg;
     float4* A4 = reinterpret_cast<float4*>(a.A);
+    // row-major float4 index of this thread's four elements (final_state is row-major)
+    int fe4 = e4;
+    if (a.state_lm) {
+        const int N4 = a.N >> 2, blk = e4 / (32 * N4), j = e4 - blk * 32 * N4;
+        fe4 = (blk * 32 + (j & 31)) * N4 + (j >> 5);
+    }
     float4 carry = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int s0 = 0; s0 < nseg; s0 += kScanUnroll) {
         float4 agg[kScanUnroll];
@@ -164,7 +171,7 @@ __global__ void __launch_bounds__(kScanThreads) state_scan_kernel(Args a, int wr
             carry.z = fmaf(dec[u], carry.z, agg[u].z);
             carry.w = fmaf(dec[u], carry.w, agg[u].w);
             if (write_final && (flags[u] & SEG_LAST))
-                reinterpret_cast<float4*>(a.final_state)[((long long)seq[u] * a.H + h) * PN4 + e4] =
+                reinterpret_cast<float4*>(a.final_state)[((long long)seq[u] * a.H + h) * PN4 + fe4] =
                     carry;
         }
     }

@@ -192,14 +192,15 @@ __global__ void __launch_bounds__(kStateThreads, 2)
             fence_proxy_async();
             mbar_arrive(&ready[s]);
         }
-        // ---- epilogue: TMEM -> aggregates A[seg][h][p][n]
+        // ---- epilogue: TMEM -> aggregates A[seg][h] (lane-major: each float4 store of a
+        // warp covers 512 contiguous bytes)
         const bool ok = wait_or_abort(done, 0, abort_flag, a.hdr);
         tc_fence_after();
         const int q = warp & 3;
         const int r = 32 * q + lane;  // accumulator row = (head, p)
         const int cbase = (ct >> 7) * (N / 2);  // each of the two warpgroups takes half the columns
-        float* Arow = (MODE == 0 ? a.A : a.adj) +
-                      (((long long)seg * a.H + h0 + (r >> 6)) * kP + (r & 63)) * N;
+        float* Arow = (MODE == 0 ? a.A : a.adj) + ((long long)seg * a.H + h0 + (r >> 6)) * kP * N +
+                      lm_row(r & 63, N);
 #pragma unroll
         for (int c0 = cbase; c0 < cbase + N / 2; c0 += 16) {
             uint32_t v[16];
@@ -208,7 +209,7 @@ __global__ void __launch_bounds__(kStateThreads, 2)
             if (ok) {
 #pragma unroll
                 for (int i = 0; i < 16; i += 4)
-                    *reinterpret_cast<float4*>(Arow + c0 + i) =
+                    *reinterpret_cast<float4*>(Arow + (c0 + i) * 32) =
                         make_float4(__uint_as_float(v[i]), __uint_as_float(v[i + 1]),
                                     __uint_as_float(v[i + 2]), __uint_as_float(v[i + 3]));
             }
@@ -756,13 +757,13 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
                         wait_or_abort(&h_free[gc & 1], ((gc - 2) >> 1) & 1, abort_flag, a.hdr);
                     const float sc0 = expf(-frec(gc % kFS, rh)[FAC_HALF]);  // exp(m_0)
                     const float* Hin =
-                        a.A + (((long long)I.seg * a.H + I.h0 + rh) * kP + rp) * N + n0;
+                        a.A + ((long long)I.seg * a.H + I.h0 + rh) * kP * N + lm_row(rp, N) + n0 * 32;
 #pragma unroll
                     for (int c0 = 0; c0 < NH; c0 += 32) {
                         float h[32];
 #pragma unroll
                         for (int i = 0; i < 32; i += 4) {
-                            const float4 v = *reinterpret_cast<const float4*>(Hin + c0 + i);
+                            const float4 v = *reinterpret_cast<const float4*>(Hin + (c0 + i) * 32);
                             h[i] = v.x * sc0;
                             h[i + 1] = v.y * sc0;
                             h[i + 2] = v.z * sc0;
@@ -1130,10 +1131,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         bwd_factors(F, load_fac_vals(a, seg, h0, 0, nchunks, ct), 0, ct);
         {
             const float sc0 = expf(-F.scal[(0 * 2 + rh) * 4 + 0]);
-            const float* Hin = a.A + (((long long)seg * a.H + h0 + rh) * kP + rp) * N + n0;
+            const float* Hin =
+                a.A + ((long long)seg * a.H + h0 + rh) * kP * N + lm_row(rp, N) + n0 * 32;
 #pragma unroll
             for (int i = 0; i < NH; i += 4) {
-                const float4 v = *reinterpret_cast<const float4*>(Hin + i);
+                const float4 v = *reinterpret_cast<const float4*>(Hin + i * 32);
                 Hs[i] = v.x * sc0;
                 Hs[i + 1] = v.y * sc0;
                 Hs[i + 2] = v.z * sc0;
@@ -1685,19 +1687,20 @@ __global__ void __launch_bounds__(kDxThreads, 1)
                 // after it (both states from the fp32 scans)
                 wait_or_abort(&fac_full[0], 0, abort_flag, a.hdr);
                 const float sc = expf(-frec(0, rh)[FAC_HALF]);
-                const float* Gin = a.adj + (((long long)seg * a.H + h0 + rh) * kP + rp) * N + n0;
+                const float* Gin =
+                    a.adj + ((long long)seg * a.H + h0 + rh) * kP * N + lm_row(rp, N) + n0 * 32;
                 const bool more = !(si.flags & SEG_LAST);
                 const float* Hend =
-                    a.A + (((long long)(seg + 1) * a.H + h0 + rh) * kP + rp) * N + n0;
+                    a.A + ((long long)(seg + 1) * a.H + h0 + rh) * kP * N + lm_row(rp, N) + n0 * 32;
                 float kp = 0.f;
 #pragma unroll
                 for (int c0 = 0; c0 < NH; c0 += 16) {
                     float h[16];
 #pragma unroll
                     for (int i = 0; i < 16; i += 4) {
-                        const float4 v = *reinterpret_cast<const float4*>(Gin + c0 + i);
+                        const float4 v = *reinterpret_cast<const float4*>(Gin + (c0 + i) * 32);
                         if (more) {
-                            const float4 w = *reinterpret_cast<const float4*>(Hend + c0 + i);
+                            const float4 w = *reinterpret_cast<const float4*>(Hend + (c0 + i) * 32);
                             kp += v.x * w.x + v.y * w.y + v.z * w.z + v.w * w.w;
                         }
                         h[i] = v.x * sc;
