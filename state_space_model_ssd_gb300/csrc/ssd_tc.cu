@@ -36,7 +36,7 @@ namespace {
 
 // ================================================================ segment aggregates
 // Warps: 0 = TMA producer, 1 = MMA issuer (and TMEM owner), 2..9 = compute.
-constexpr int kStateStages = 3;
+constexpr int kStateStages = 2;  // with three CTAs per SM (shared memory and TMEM allow it)
 constexpr int kStateThreads = 320;  // TMA warp, MMA warp, 8 compute warps
 constexpr int kMaxSeg = 1024;  // segment length bound for the per-token weights
 
@@ -53,7 +53,7 @@ constexpr int kWPad = kMaxSeg + kMaxSeg / 16;  // per-head weight row, padded ag
 __device__ __forceinline__ int widx(int t) { return t + (t >> 4); }
 
 template <int N, int MODE>
-__global__ void __launch_bounds__(kStateThreads, 2)
+__global__ void __launch_bounds__(kStateThreads, 3)
     tc_seg_state_kernel(const __grid_constant__ CUtensorMap map_x,
                         const __grid_constant__ CUtensorMap map_b, Args a) {
     const int seg = blockIdx.x;
@@ -1803,6 +1803,8 @@ constexpr int state_smem_bytes(int N) {
     return kStateStages * StateSmem::stage_bytes(N) + 2 * kWPad * 4 + 32 * 4 + 3 * kStateStages * 8 +
            8 + 16 + 1024;
 }
+// three CTAs of the aggregate kernel per SM (1 KB per CTA reserved by the system)
+static_assert(3 * (state_smem_bytes(128) + 1024) <= 233472, "aggregate kernel occupancy");
 
 // SMs of the current device (persistent grids take one CTA per SM).
 int sm_count() {
