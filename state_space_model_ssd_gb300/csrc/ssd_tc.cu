@@ -1507,23 +1507,26 @@ __global__ void __launch_bounds__(kDxThreads, 1)
                     mma_bf16(tmem + T_DX, kdesc(bs, k, 8192), kdesc(gb, k, 16384), id_dx2, 1u);
                 mma_commit(dx_full);
                 mma_commit(l0_free);
-                // dB = sum_h P2m_h C + xg_h Gs_h
-                if (!wait_or_abort(e_ready, it & 1, abort_flag, a.hdr)) break;
+                // dB = sum_h xg_h Gs_h + P2m_h C: the first half needs no masks and is the
+                // last reader of the Gs operand
                 if (it >= 1 && !wait_or_abort(db_free, (it - 1) & 1, abort_flag, a.hdr)) break;
                 tc_fence_after();
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-#pragma unroll
-                    for (int k = 0; k < 4; ++k)
-                        mma_bf16(tmem + T_DB, kdesc(p2m + h * 8192, k, 0), mdesc(cs, k, 8192),
-                                 id_db, (h > 0 || k > 0) ? 1u : 0u);
+                for (int h = 0; h < 2; ++h)
 #pragma unroll
                     for (int k = 0; k < 4; ++k)
                         mma_bf16(tmem + T_DB, kdesc(xs + h * 8192, k, 0),
-                                 mdesc(gb + h * 8192, k, 16384), id_db, 1u);
-                }
-                mma_commit(db_full);
+                                 mdesc(gb + h * 8192, k, 16384), id_db, (h > 0 || k > 0) ? 1u : 0u);
                 mma_commit(g_free);
+                if (!wait_or_abort(e_ready, it & 1, abort_flag, a.hdr)) break;
+                tc_fence_after();
+#pragma unroll
+                for (int h = 0; h < 2; ++h)
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        mma_bf16(tmem + T_DB, kdesc(p2m + h * 8192, k, 0), mdesc(cs, k, 8192),
+                                 id_db, 1u);
+                mma_commit(db_full);
                 mma_commit(p2m_free);
                 mma_commit(&empty[s]);
             }
@@ -1619,6 +1622,10 @@ __global__ void __launch_bounds__(kDxThreads, 1)
                                 qv = fmaf(xf.y, __uint_as_float(v[e + 2 * i + 1]), qv);
                             }
                         }
+                    }
+                    // this warpgroup is done with the stage's xg rows
+                    if (j == 32) mbar_arrive(&empty[s]);
+                    if (ok) {
                         if (tt < vc) {
 #pragma unroll
                             for (int e = 0; e < 32; e += 8)
@@ -1630,7 +1637,6 @@ __global__ void __launch_bounds__(kDxThreads, 1)
                         }
                     }
                 }
-                mbar_arrive(&empty[s]);  // this warpgroup is done with the stage's xg rows
                 // d_raw = sigmoid(z) (q / delta - sum_{u >= t in the segment} (r - q) - kseg):
                 // suffix sums over the chunk's rows u >= t (16 rows per warp and head, then
                 // the later warps' totals), plus the later chunks' carry
