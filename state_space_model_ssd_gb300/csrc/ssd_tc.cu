@@ -825,12 +825,14 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
 // Both backward kernels walk a segment chunk by chunk for one pair of heads,
 // with the same warp roles as the forward walk (0 = TMA, 1 = MMA, 2..9 =
 // compute).  Per chunk: f(t) = exp(s_t - m), g(t) = delta_t exp(m - s_t) as in
-// the forward; dyf = f dy and xg = g x are scaled in place in the stage.
+// the forward; xg = g x (both walks) and dyf = f dy (dx/dB walk) are scaled in place
+// in the stage.
 //
 // tc_bwd_dc (chunks in order, state Hs_c = exp(m_c) H_c as in the forward walk):
-//   P1_h[t, s] = dyf_t . xg_s                                  (M=64, N=64, K=P)
+//   P1_h[t, s] = dy_t . xg_s                                   (M=64, N=64, K=P)
 //   W_h        = P1_h masked to s <= t                           (epilogue, bf16)
-//   dC_h[t, .] = W_h B + dyf_h Hs_h   = H_t^T dy_t for head h    (M=64, N=N, K=64 + 64)
+//   E_h[t, .]  = W_h B + dy_h Hs_h                               (M=64, N=N, K=64 + 64)
+//   dC_h[t, .] = f(t) E_h[t, .]       = H_t^T dy_t for head h    (epilogue)
 //   r_t,h      = C_t . dC_h[t, .]     = dy_t . y_t
 //   dC         = sum over the pair, added into the fp32 accumulator
 // tc_bwd_dxdb (chunks in reverse, adjoint Gs_c = exp(s_end - m) G_c where G_c
@@ -911,18 +913,13 @@ __device__ __forceinline__ void bwd_factors(const ChunkFactors& F, const FacVals
     named_sync(1, kCT);
 }
 
-// x -> g x and dy -> f dy in place (the 4 bf16 tiles at the start of a stage).
-__device__ __forceinline__ void bwd_scale_stage(unsigned char* st, const float* gv,
-                                                const float* fv, int ct) {
+// x -> g x in place (the 2 x tiles at the start of a stage).
+__device__ __forceinline__ void bwd_scale_x(unsigned char* st, const float* gv, int ct) {
     uint4* xs = reinterpret_cast<uint4*>(st);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const int idx = ct + kCT * i;  // 0..2047: [x h0 | x h1 | dy h0 | dy h1] 16-byte chunks
-        const int tile = idx >> 9;
-        const int hh = tile & 1;
-        const int row = (idx >> 3) & 63;
-        const float sc = (tile < 2) ? gv[hh * 64 + row] : fv[hh * 64 + row];
-        xs[idx] = scale_chunk(xs[idx], sc);
+    for (int i = 0; i < 4; ++i) {
+        const int idx = ct + kCT * i;  // 0..1023: [x h0 | x h1] 16-byte chunks
+        xs[idx] = scale_chunk(xs[idx], gv[(idx >> 9) * 64 + ((idx >> 3) & 63)]);
     }
 }
 
@@ -1146,12 +1143,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         fence_proxy_async();
         mbar_arrive(&h_ready[0]);
         int pending_empty = -1;  // thread 0: stage whose reduce-add may still read shared memory
-        // x -> g x and dy -> f dy of chunk cc in its stage (factors in buffer cc & 1)
+        // x -> g x of chunk cc in its stage (factors in buffer cc & 1); dy stays unscaled:
+        // f(t) multiplies whole rows t of P1 and of dyf Hs, so the epilogue applies it to
+        // the rows of dC and r instead
         auto scale_chunk_stage = [&](int cc) {
             const int sc = cc & 1;
             if (wait_or_abort(&full[sc], (cc >> 1) & 1, abort_flag, a.hdr))
-                bwd_scale_stage(sm + Lay::OFF_STAGE + sc * Lay::STAGE, F.gbuf + sc * 128,
-                                F.fbuf + sc * 128, ct);
+                bwd_scale_x(sm + Lay::OFF_STAGE + sc * Lay::STAGE, F.gbuf + sc * 128, ct);
             fence_proxy_async();
             mbar_arrive(xg_ready);
         };
@@ -1215,6 +1213,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 const bool ok = wait_or_abort(dc_full, pc, abort_flag, a.hdr);
                 tc_fence_after();
                 const unsigned char* cst = st + 32768 + N * 128;
+                const float f0 = F.fbuf[s * 128 + t], f1 = F.fbuf[s * 128 + 64 + t];
                 float rp0 = 0.f, rp1 = 0.f;
                 // the partial dC tiles go into this stage's x / dy tiles, which every MMA of
                 // the chunk has finished reading
@@ -1254,13 +1253,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                         float sum[16];
 #pragma unroll
                         for (int u = 0; u < 16; ++u)
-                            sum[u] = (ok && t < vc) ? __uint_as_float(v0[u]) + __uint_as_float(v1[u])
+                            sum[u] = (ok && t < vc) ? fmaf(f0, __uint_as_float(v0[u]),
+                                                           f1 * __uint_as_float(v1[u]))
                                                     : 0.f;
                         stage_row16(rtiles, t, n, sum);
                     }
                 }
-                rp0 += __shfl_xor_sync(0xffffffffu, rp0, 16);
-                rp1 += __shfl_xor_sync(0xffffffffu, rp1, 16);
+                rp0 = f0 * (rp0 + __shfl_xor_sync(0xffffffffu, rp0, 16));
+                rp1 = f1 * (rp1 + __shfl_xor_sync(0xffffffffu, rp1, 16));
                 tc_fence_before();
                 mbar_arrive(dc_free);
                 fence_proxy_async();
