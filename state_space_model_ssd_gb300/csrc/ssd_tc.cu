@@ -1547,7 +1547,10 @@ __global__ void __launch_bounds__(kDxThreads, 1)
                 ok = wait_or_abort(&full[s], (j >> 1) & 1, abort_flag, a.hdr) && ok;
                 if (ok) {
                     uint4* xs = reinterpret_cast<uint4*>(sm + Lay::OFF_STAGE + s * Lay::STAGE);
-#pragma unroll 4
+                    // two chunks in flight per thread: a deeper unroll makes this warpgroup
+                    // crowd the shared-memory pipe that the masks and epilogues wait on (measured
+                    // slower at 4 and 16)
+#pragma unroll 2
                     for (int i = 0; i < 16; ++i) {
                         const int idx = ct + 128 * i;  // [x h0 | x h1 | dy h0 | dy h1] 16-byte chunks
                         const int tile = idx >> 9, row = (idx >> 3) & 63;
