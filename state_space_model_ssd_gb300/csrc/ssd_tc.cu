@@ -698,6 +698,7 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
                     mbar_arrive(&fac_empty[sl]);
                     uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.y) +
                                                           ((tok0 + tt) * a.H + I.h0 + hf) * kP);
+                    const bool wide = (reinterpret_cast<uintptr_t>(a.y) & 31) == 0;
 #pragma unroll
                     for (int j = 0; j < 64; j += 32) {
                         uint32_t v[32];
@@ -709,13 +710,8 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
                             mbar_arrive(&y_free[s]);
                         }
                         if (ok && tt < vc) {
-#pragma unroll
-                            for (int e = 0; e < 32; e += 8)
-                                dst[(j + e) >> 3] = make_uint4(
-                                    pack_bf16(fv * __uint_as_float(v[e]), fv * __uint_as_float(v[e + 1])),
-                                    pack_bf16(fv * __uint_as_float(v[e + 2]), fv * __uint_as_float(v[e + 3])),
-                                    pack_bf16(fv * __uint_as_float(v[e + 4]), fv * __uint_as_float(v[e + 5])),
-                                    pack_bf16(fv * __uint_as_float(v[e + 6]), fv * __uint_as_float(v[e + 7])));
+                            store_bf16x16(dst + (j >> 3), v, fv, wide);
+                            store_bf16x16(dst + ((j + 16) >> 3), v + 16, fv, wide);
                         }
                     }
                 }

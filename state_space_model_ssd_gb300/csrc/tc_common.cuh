@@ -95,6 +95,25 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
     return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// s * (16 fp32 values) as 16 bf16 (32 bytes) at p: one 256-bit store when wide (p 32-byte
+// aligned), else two 128-bit stores.  A warp whose lanes write different rows then fills
+// whole 32-byte sectors with each store.
+__device__ __forceinline__ void store_bf16x16(void* p, const uint32_t* v, float s, bool wide) {
+    uint32_t w[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+        w[i] = pack_bf16(s * __uint_as_float(v[2 * i]), s * __uint_as_float(v[2 * i + 1]));
+    if (wide) {
+        asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p),
+                     "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]),
+                     "r"(w[7])
+                     : "memory");
+    } else {
+        reinterpret_cast<uint4*>(p)[0] = make_uint4(w[0], w[1], w[2], w[3]);
+        reinterpret_cast<uint4*>(p)[1] = make_uint4(w[4], w[5], w[6], w[7]);
+    }
+}
+
 // Multiplies the 8 bf16 values of a 16-byte chunk by s.
 __device__ __forceinline__ uint4 scale_chunk(uint4 v, float s) {
     uint32_t w[4] = {v.x, v.y, v.z, v.w};

@@ -207,6 +207,21 @@ def test_deterministic_forward(ssd):
     assert bool((y1 == y2).all()) and bool((f1 == f2).all())
 
 
+def test_output_base_16_byte_aligned(ssd):
+    """y written through a base that is 16- but not 32-byte aligned (the walk then stores
+    each 32-byte piece of a row as two 16-byte stores) equals y written to an aligned
+    buffer, bit for bit."""
+    import torch
+    d = _draw(13, 1, 1000, 4, 64, 128, dtype="bf16")
+    t = to_device(d, "bf16")
+    y1, _ = ssd.forward(t["x"], t["raw_dt"], t["B"], t["C"], delta_init=-4.6)
+    buf = torch.empty(t["x"].numel() + 8, dtype=torch.bfloat16, device="cuda")
+    y2 = buf[8:].view(t["x"].shape)
+    assert y2.data_ptr() % 32 == 16
+    ssd.forward(t["x"], t["raw_dt"], t["B"], t["C"], delta_init=-4.6, out=y2)
+    assert bool((y1 == y2).all())
+
+
 def test_bad_cu_seqlens_reports_device_status(ssd):
     """A non-monotone cu_seqlens is caught on the device; the call returns, no hang."""
     import torch
