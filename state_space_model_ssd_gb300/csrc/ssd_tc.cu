@@ -1001,7 +1001,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     float* rpart = reinterpret_cast<float*>(sm + Lay::OFF_RQ);  // [2 wg][2 head][64]
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + Lay::OFF_BAR);
     uint64_t* full = bars + 0;      // [2]
-    uint64_t* empty = bars + 2;     // [2] (compute threads arrive after the chunk's epilogue)
+    // [2] the chunk's partial dC tiles are in its stage, which the compute threads no
+    // longer read (the producer adds them into the accumulator, then reloads the stage)
+    uint64_t* staged = bars + 2;
     uint64_t* xg_ready = bars + 4;
     uint64_t* s_full = bars + 5;
     uint64_t* s_free = bars + 6;
@@ -1018,7 +1020,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     if (tid == 0) {
         for (int i = 0; i < 2; ++i) {
             mbar_init(&full[i], 1);
-            mbar_init(&empty[i], kCT);
+            mbar_init(&staged[i], kCT);
         }
         mbar_init(xg_ready, kCT);
         mbar_init(s_full, 1);
@@ -1043,10 +1045,26 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
     if (warp == 0) {
         if (lane == 0) {
-            for (int c = 0; c < nchunks; ++c) {
+            // partial dC tiles of chunk cc (in its stage) -> reduce-add into the accumulator
+            auto add_partial = [&](int cc) -> bool {
+                const int sc = cc & 1;
+                if (!wait_or_abort(&staged[sc], (cc >> 1) & 1, abort_flag, a.hdr)) return false;
+                unsigned char* rt = sm + Lay::OFF_STAGE + sc * Lay::STAGE;
+                const int tok = (int)(si.start + (long long)cc * kQ);
+                for (int j = 0; j < N / 32; ++j)
+                    tma_reduce_add_3d(&map_acc, rt + j * 8192, j * 32, g, tok);
+                tma_store_commit();
+                return true;
+            };
+            bool run = true;
+            for (int c = 0; c < nchunks && run; ++c) {
                 const int s = c & 1;
-                if (c >= 2 && !wait_or_abort(&empty[s], ((c >> 1) - 1) & 1, abort_flag, a.hdr))
-                    break;
+                if (c >= 2) {
+                    // the stage of chunk c - 2 is reloaded once its partial tiles are read
+                    run = add_partial(c - 2);
+                    tma_store_wait_read<0>();
+                    if (!run) break;
+                }
                 unsigned char* st = sm + Lay::OFF_STAGE + s * Lay::STAGE;
                 const int tok = (int)(si.start + (long long)c * kQ);
                 mbar_expect_tx(&full[s], Lay::STAGE);
@@ -1060,6 +1078,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                                 tok);
                 }
             }
+            for (int cc = nchunks >= 2 ? nchunks - 2 : 0; cc < nchunks && run; ++cc)
+                run = add_partial(cc);
+            tma_store_wait_all<0>();
         }
     } else if (warp == 1) {
         if (lane == 0) {
@@ -1138,7 +1159,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         write_state<NH>(sm + Lay::OFF_S, Hs, r, n0);
         fence_proxy_async();
         mbar_arrive(&h_ready[0]);
-        int pending_empty = -1;  // thread 0: stage whose reduce-add may still read shared memory
         // x -> g x of chunk cc in its stage (factors in buffer cc & 1); dy stays unscaled:
         // f(t) multiplies whole rows t of P1 and of dyf Hs, so the epilogue applies it to
         // the rows of dC and r instead
@@ -1153,13 +1173,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
         for (int c = 0; c < nchunks; ++c) {
             const int s = c & 1, ph = (c >> 1) & 1, pc = c & 1;
-            // release the previous chunk's stage once its dC reduce-add has read it (the
-            // next chunk's copy into it is waited for before this iteration's epilogue)
-            if (ct == 0 && pending_empty >= 0) {
-                tma_store_wait_read<0>();
-                mbar_arrive(&empty[pending_empty]);
-                pending_empty = -1;
-            }
             const bool last = (c == nchunks - 1);
             const int vc = min(kQ, si.len - c * kQ);
             const long long tok0 = si.start + (long long)c * kQ;
@@ -1260,13 +1273,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 tc_fence_before();
                 mbar_arrive(dc_free);
                 fence_proxy_async();
-                named_sync(1, kCT);
-                if (ct == 0) {
-                    for (int j = 0; j < N / 32; ++j)
-                        tma_reduce_add_3d(&map_acc, rtiles + j * 8192, j * 32, g, (int)tok0);
-                    tma_store_commit();
-                    pending_empty = s;  // released once the reduce-add has read the tiles
-                }
+                mbar_arrive(&staged[s]);
                 if (hf == 0) {
                     rpart[(wg * 2 + 0) * 64 + t] = rp0;
                     rpart[(wg * 2 + 1) * 64 + t] = rp1;
@@ -1276,11 +1283,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     a.rtok[(tok0 + t) * a.H + h0] = rpart[0 * 64 + t] + rpart[2 * 64 + t];
                     a.rtok[(tok0 + t) * a.H + h0 + 1] = rpart[1 * 64 + t] + rpart[3 * 64 + t];
                 }
-                if (ct != 0) mbar_arrive(&empty[s]);
             }
             named_sync(1, kCT);  // rpart reuse
         }
-        if (ct == 0) tma_store_wait_all<0>();
     }
     tc_fence_before();
     __syncthreads();
