@@ -10,6 +10,10 @@ than L2, so no flush is needed between steps.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 
+The "e2e" figure times the same step through ssd_step_host on pinned host buffers:
+each step copies its inputs in and its results out inside the timed region, two steps
+in flight on two streams.
+
 --impl reference times the fp64 CPU oracle on the host cores (a bounded
 sample of the same workload per step).  Under torchrun every rank runs its
 own replica (weak scaling); only the barrier and the max-over-ranks timing
@@ -317,72 +321,39 @@ def gpu_arm(args, w, rank, world, dist):
     tokens_per_step = w.total_tokens
     value = world * tokens_per_step / (ms_max * 1e-3)
 
-    # ---- end to end through the public API: pinned host in, host out.  Every step
-    # copies its own inputs in and its results out inside the timed region; the copies
-    # run on their own streams, double-buffered, so that step i + 1's inputs and step
-    # i - 1's results move while step i computes (a data loader's pipelining).
-    out_keys = ["y"] + (["dx", "d_raw_dt", "dB", "dC"] if w.backward else [])
-    dev_in = [dv, {k: torch.empty_like(v) for k, v in dv.items()}]
-    dev_out = [{"y": y, **(grads or {})},
-               {"y": torch.empty_like(y), **({k: torch.empty_like(v) for k, v in grads.items()}
-                                             if grads else {})}]
-    host_out = [{k: torch.empty(dev_out[0][k].shape, dtype=dev_out[0][k].dtype).pin_memory()
-                 for k in out_keys} for _ in range(2)]
+    # ---- end to end through the C ABI on host buffers: every step is one ssd_step_host
+    # call, which copies the step's inputs in from pinned host memory, runs the forward
+    # (and backward) and copies the results back out.  Two device buffers and two streams
+    # alternate, so that one step's copies move while the other step's kernels run (a data
+    # loader's pipelining).
+    host_cu = None if d["cu_seqlens"] is None else torch.from_numpy(
+        np.ascontiguousarray(d["cu_seqlens"], dtype=np.int32))
+    nseq = prob.nseq if prob.nseq > 0 else prob.batch
+
+    def pinned_like(t):
+        return torch.empty(t.shape, dtype=t.dtype).pin_memory()
+
+    host_out = []
+    for _ in range(2):
+        o = {"y": pinned_like(host["x"]),
+             "final_state": torch.empty((nseq, prob.nheads, prob.headdim, prob.dstate),
+                                        dtype=torch.float32).pin_memory()}
+        if w.backward:
+            o.update({"dx": pinned_like(host["x"]), "d_raw_dt": pinned_like(host["raw_dt"]),
+                      "dB": pinned_like(host["B"]), "dC": pinned_like(host["C"])})
+        host_out.append(o)
     h2d = sum(v.numel() * v.element_size() for v in host.values())
+    h2d += 0 if host_cu is None else host_cu.numel() * host_cu.element_size()
     d2h = sum(v.numel() * v.element_size() for v in host_out[0].values())
-    # NS streams per direction; tensors above 64 MB are copied in token halves, and the
-    # pieces are dealt out to the streams largest first
-    NS = 4
-
-    def pieces(names, size_of):
-        out = []
-        for k in sorted(names, key=lambda k: -size_of(k)):
-            out += [(k, 0, 2), (k, 1, 2)] if size_of(k) > (64 << 20) else [(k, 0, 1)]
-        return out
-
-    def part(t, i, n):
-        L = t.shape[1]
-        return t[:, i * L // n:(i + 1) * L // n]
-
-    in_pieces = pieces(list(host), lambda k: host[k].numel() * host[k].element_size())
-    out_pieces = pieces(out_keys, lambda k: dev_out[0][k].numel() * dev_out[0][k].element_size())
-    s_in = [torch.cuda.Stream() for _ in range(NS)]
-    s_out = [torch.cuda.Stream() for _ in range(NS)]
-    in_free = [torch.cuda.Event(), torch.cuda.Event()]    # compute done with an input set
-    out_free = [[torch.cuda.Event() for _ in range(NS)] for _ in range(2)]  # results copied out
-    for b in range(2):
-        in_free[b].record(stream)
-        for j in range(NS):
-            out_free[b][j].record(stream)
+    nbytes = ssd.step_host_size(prob)
+    dev_buf = [torch.empty(nbytes, dtype=torch.uint8, device=dev) for _ in range(2)]
+    s_step = [torch.cuda.Stream(), torch.cuda.Stream()]
 
     def e2e_step(i):
         b = i & 1
-        din, dout = dev_in[b], dev_out[b]
-        ready = [torch.cuda.Event() for _ in range(NS)]
-        for j in range(NS):
-            with torch.cuda.stream(s_in[j]):
-                s_in[j].wait_event(in_free[b])
-                for k, i, n in in_pieces[j::NS]:
-                    part(din[k], i, n).copy_(part(host[k], i, n), non_blocking=True)
-                ready[j].record(s_in[j])
-        for j in range(NS):
-            stream.wait_event(ready[j])
-            stream.wait_event(out_free[b][j])
-        ssd.forward(din["x"], din["raw_dt"], din["B"], din["C"], w.delta_init, w.chunk_size, cu,
-                    final_state=True, out=dout["y"], workspace=ws)
-        if w.backward:
-            ssd.backward(din["x"], din["raw_dt"], din["B"], din["C"], din["dy"], w.delta_init,
-                         w.chunk_size, cu, out={k: dout[k] for k in out_keys[1:]}, workspace=ws,
-                         after_forward=True)
-        done = torch.cuda.Event()
-        done.record(stream)
-        in_free[b].record(stream)
-        for j in range(NS):
-            with torch.cuda.stream(s_out[j]):
-                s_out[j].wait_event(done)
-                for k, i, n in out_pieces[j::NS]:
-                    part(host_out[b][k], i, n).copy_(part(dout[k], i, n), non_blocking=True)
-                out_free[b][j].record(s_out[j])
+        ssd.step_host(host["x"], host["raw_dt"], host["B"], host["C"], host.get("dy"),
+                      w.delta_init, w.chunk_size, host_cu, out=host_out[b],
+                      device_buffer=dev_buf[b], stream=s_step[b])
 
     for i in range(max(1, args.warmup)):
         e2e_step(i)
@@ -390,13 +361,14 @@ def gpu_arm(args, w, rank, world, dist):
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for j in range(NS):
-        s_in[j].wait_event(e0)
+    for s_ in s_step:
+        s_.wait_event(e0)
     for i in range(args.steps):
         e2e_step(i)
-    for b in range(2):
-        for j in range(NS):
-            stream.wait_event(out_free[b][j])
+    for s_ in s_step:
+        done = torch.cuda.Event()
+        done.record(s_)
+        stream.wait_event(done)
     e1.record(stream)
     barrier()
     e2e_ms = e0.elapsed_time(e1) / args.steps

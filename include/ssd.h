@@ -17,8 +17,9 @@
  *
  * General rules for every entry point:
  *  - All tensor arguments are DEVICE pointers on the current CUDA device,
- *    contiguous, row-major, 16-byte aligned.  The caller owns every buffer;
- *    the library allocates nothing and keeps no pointer after a call returns.
+ *    contiguous, row-major, 16-byte aligned (ssd_step_host alone takes host
+ *    buffers).  The caller owns every buffer; the library allocates nothing on
+ *    the device and keeps no pointer after a call returns.
  *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy
  *    default stream).  No call synchronises except ssd_device_status().
  *  - Host-side argument checks run before any launch; on failure nothing is
@@ -126,6 +127,37 @@ ssd_status_t ssd_backward_after_forward(const ssd_problem_t* prob, const void* x
                                         const int32_t* cu_seqlens, const void* dy, void* dx,
                                         float* d_raw_dt, void* dB, void* dC, void* workspace,
                                         size_t workspace_bytes, void* stream);
+
+/* Device bytes that ssd_step_host needs for `prob`: the backward workspace followed by
+ * device copies of the step's inputs and results.  Pure host function. */
+ssd_status_t ssd_step_host_size(const ssd_problem_t* prob, size_t* bytes);
+
+/* One forward + backward step on HOST buffers (the layouts above, in host memory):
+ * x, raw_dt, B, C, cu_seqlens (a host array; NULL for a dense batch) and dy are read from
+ * host memory; y, final_state (NULL: not written), dx, d_raw_dt, dB and dC are written to
+ * host memory.  With dy = NULL the step is the forward alone (dx, d_raw_dt, dB and dC
+ * are then not used and may be NULL).  The call copies the inputs into `device` (>= ssd_step_host_size bytes of
+ * device memory owned by the caller, 256-byte aligned), runs ssd_forward and
+ * ssd_backward_after_forward there, and copies the results back.  Asynchronous on
+ * `stream` like every other call: the host outputs are complete once the stream has
+ * passed the call (e.g. after cudaStreamSynchronize), and every host buffer must stay
+ * valid until then.  Page-locked host memory lets the copies run asynchronously
+ * (pageable memory is staged synchronously by the CUDA runtime).  Inside a call, dy is
+ * copied in while the forward runs and y and final_state out while the backward runs,
+ * on copy streams the library creates once per device; each call is ordered after the
+ * caller's earlier work on `stream` and the caller's later work after all of it.  Two
+ * calls on different streams with different `device` buffers overlap one step's copies
+ * with the other's kernels.  The workspace is the first region of `device`, so
+ * ssd_device_status(device, ...) reads the step's device status.  Errors: those of
+ * ssd_forward and ssd_backward; SSD_ERR_WORKSPACE if `device` is NULL or smaller than
+ * ssd_step_host_size(); SSD_ERR_ALIGNMENT if it is not 256-byte aligned; SSD_ERR_CUDA if
+ * a copy or an event could not be enqueued.  One host thread at a time enqueues a step
+ * (calls from several threads are serialised). */
+ssd_status_t ssd_step_host(const ssd_problem_t* prob, const void* x, const float* raw_dt,
+                           const void* B, const void* C, const int32_t* cu_seqlens,
+                           const void* dy, void* y, float* final_state, void* dx,
+                           float* d_raw_dt, void* dB, void* dC, void* device,
+                           size_t device_bytes, void* stream);
 
 /* Size of the device scratch array that ssd_forward_noalloc works in. */
 #define SSD_NOALLOC_SCRATCH_BYTES (64u << 20)

@@ -21,8 +21,8 @@ from typing import Optional
 from . import _lib
 from ._lib import SSDError, check
 
-__all__ = ["forward", "backward", "workspace_size", "dispatch_path", "make_problem",
-           "last_launch_count", "profiler", "SSDError"]
+__all__ = ["forward", "backward", "step_host", "step_host_size", "workspace_size",
+           "dispatch_path", "make_problem", "last_launch_count", "profiler", "SSDError"]
 
 
 def _torch():
@@ -154,6 +154,55 @@ def backward(x, raw_dt, B, C, dy, delta_init: float, chunk_size: int = 64, cu_se
                                        _ptr(out["d_raw_dt"]), _ptr(out["dB"]), _ptr(out["dC"]),
                                        _ptr(ws), ws.numel(), _stream(stream))
     check(st, name)
+    return out
+
+
+def step_host_size(problem: _lib.Problem) -> int:
+    n = ctypes.c_size_t(0)
+    check(_lib.lib().ssd_step_host_size(ctypes.byref(problem), ctypes.byref(n)),
+          "ssd_step_host_size")
+    return int(n.value)
+
+
+def step_host(x, raw_dt, B, C, dy, delta_init: float, chunk_size: int = 64, cu_seqlens=None,
+              final_state: bool = True, out=None, device_buffer=None, stream=None):
+    """Runs ssd_step_host on CPU tensors (pin them for asynchronous copies): returns a dict
+    ``y, final_state (or None), dx, d_raw_dt, dB, dC`` of CPU tensors (``dy=None``: the
+    forward alone, no gradients), complete once ``stream`` (default: the current stream)
+    has passed the call.  ``device_buffer`` is a CUDA uint8 tensor of at least
+    ``step_host_size`` bytes; the current device is used."""
+    torch = _torch()
+    for t, name in ((x, "x"), (raw_dt, "raw_dt"), (B, "B"), (C, "C"), (dy, "dy")):
+        if t is None and name == "dy":
+            continue
+        if t.is_cuda or not t.is_contiguous():
+            raise ValueError("%s must be a contiguous CPU tensor" % name)
+    if raw_dt.dtype != torch.float32:
+        raise TypeError("raw_dt must be float32")
+    if cu_seqlens is not None and (cu_seqlens.is_cuda or cu_seqlens.dtype != torch.int32):
+        raise ValueError("cu_seqlens must be an int32 CPU tensor")
+    prob = make_problem(x, B, delta_init, chunk_size, cu_seqlens)
+    nseq = prob.nseq if prob.nseq > 0 else prob.batch
+    if out is None:
+        pin = x.is_pinned()
+        def like(t):
+            return torch.empty(t.shape, dtype=t.dtype, pin_memory=pin)
+        grads = dy is not None
+        out = {"y": like(x), "dx": like(x) if grads else None,
+               "d_raw_dt": like(raw_dt) if grads else None,
+               "dB": like(B) if grads else None, "dC": like(C) if grads else None,
+               "final_state": torch.empty((nseq, prob.nheads, prob.headdim, prob.dstate),
+                                          dtype=torch.float32, pin_memory=pin)
+               if final_state else None}
+    dev = torch.device("cuda", torch.cuda.current_device())
+    buf = _workspace(step_host_size(prob), dev, device_buffer)
+    st = _lib.lib().ssd_step_host(ctypes.byref(prob), _ptr(x), _ptr(raw_dt), _ptr(B), _ptr(C),
+                                  _ptr(cu_seqlens), _ptr(dy), _ptr(out["y"]),
+                                  _ptr(out.get("final_state")), _ptr(out.get("dx")),
+                                  _ptr(out.get("d_raw_dt")), _ptr(out.get("dB")),
+                                  _ptr(out.get("dC")),
+                                  _ptr(buf), buf.numel(), _stream(stream))
+    check(st, "ssd_step_host")
     return out
 
 

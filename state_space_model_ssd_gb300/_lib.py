@@ -55,6 +55,9 @@ _SIGS = {
     "ssd_backward_after_forward": (ctypes.c_int, [_PP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP,
                                                   _VP, _VP, _VP, _SZ, _VP]),
     "ssd_forward_noalloc": (ctypes.c_int, [_PP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP]),
+    "ssd_step_host_size": (ctypes.c_int, [_PP, ctypes.POINTER(_SZ)]),
+    "ssd_step_host": (ctypes.c_int, [_PP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP,
+                                     _VP, _VP, _VP, _SZ, _VP]),
     "ssd_device_status": (ctypes.c_int, [_VP, _VP, ctypes.POINTER(ctypes.c_int32)]),
     "ssd_dispatch_path": (ctypes.c_char_p, [_PP, ctypes.c_int]),
     "ssd_last_launch_count": (ctypes.c_int, []),

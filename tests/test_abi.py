@@ -104,3 +104,29 @@ def test_python_binding_refuses_cpu_tensors(lib):
     with pytest.raises(ValueError):
         ssd.forward(x, torch.zeros(1, 8, 2), torch.zeros(1, 8, 1, 16), torch.zeros(1, 8, 1, 16),
                     delta_init=-4.6)
+
+
+def test_step_host_checks_arguments_before_any_cuda_call(lib):
+    """ssd_step_host sizes its device region on the host and refuses a missing, small or
+    misaligned region, or a cu_seqlens that does not match the problem, before it makes
+    any CUDA call (none can succeed here)."""
+    p = _prob()
+    n = ctypes.c_size_t()
+    assert lib.ssd_step_host_size(ctypes.byref(p), ctypes.byref(n)) == 0
+    ws = ctypes.c_size_t()
+    assert lib.ssd_workspace_size(ctypes.byref(p), 1, ctypes.byref(ws)) == 0
+    T, H, P, N = 256, 2, 16, 16
+    inputs = 4 * (2 * T * H * P + T * H + 2 * T * N)      # x, dy, raw_dt, B, C (f32)
+    outputs = 4 * (2 * T * H * P + T * H + 2 * T * N + H * P * N)
+    assert n.value >= ws.value + inputs + outputs and n.value % 256 == 0
+    h = ctypes.c_void_p(0x10000)
+    dev = ctypes.c_void_p(0x40000)
+
+    def call(device, nbytes, cu=None, prob=p):
+        return lib.ssd_step_host(ctypes.byref(prob), h, h, h, h, cu, h, h, None, h, h, h, h,
+                                 device, nbytes, None)
+    assert call(None, n.value) == 4                       # no device region
+    assert call(dev, n.value - 256) == 4                  # too small
+    assert call(ctypes.c_void_p(0x40010), n.value) == 3   # not 256-byte aligned
+    assert call(dev, n.value, cu=h) == 1                  # cu_seqlens for a dense batch
+    assert call(dev, n.value, prob=_prob(headdim=12)) == 2
