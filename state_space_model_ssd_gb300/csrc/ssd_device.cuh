@@ -16,6 +16,15 @@ __device__ __forceinline__ void st_out(float* p, long long i, float v) { p[i] = 
 __device__ __forceinline__ void st_out(__nv_bfloat16* p, long long i, float v) {
     p[i] = __float2bfloat16_rn(v);
 }
+// Elements 4 i .. 4 i + 3 of p (16-byte aligned base).
+__device__ __forceinline__ void st_out4(float* p, long long i, float4 v) {
+    reinterpret_cast<float4*>(p)[i] = v;
+}
+__device__ __forceinline__ void st_out4(__nv_bfloat16* p, long long i, float4 v) {
+    __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y), hi = __floats2bfloat162_rn(v.z, v.w);
+    reinterpret_cast<uint2*>(p)[i] =
+        make_uint2(*reinterpret_cast<uint32_t*>(&lo), *reinterpret_cast<uint32_t*>(&hi));
+}
 
 // delta = softplus(raw + delta_init): log(1 + e^z) written without overflow.
 __device__ __forceinline__ float softplus_f(float z) {

@@ -125,7 +125,7 @@ __global__ void forward_match_kernel(Args a) {
 }
 
 constexpr int kScanThreads = 128;
-constexpr int kScanUnroll = 8;
+constexpr int kScanUnroll = 4;  // segments per batch; the next batch loads while this one is stored
 
 // Forward scan over segments, per head and per state element (4 per thread; the
 // scan is the same for either storage order of the states).
@@ -146,20 +146,24 @@ __global__ void __launch_bounds__(kScanThreads) state_scan_kernel(Args a, int wr
         fe4 = (blk * 32 + (j & 31)) * N4 + (j >> 5);
     }
     float4 carry = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int s0 = 0; s0 < nseg; s0 += kScanUnroll) {
-        float4 agg[kScanUnroll];
-        float dec[kScanUnroll];
-        int flags[kScanUnroll], seq[kScanUnroll];
+    float4 agg[kScanUnroll], nagg[kScanUnroll];
+    float dec[kScanUnroll], ndec[kScanUnroll];
+    int flags[kScanUnroll], seq[kScanUnroll], nflags[kScanUnroll], nseqi[kScanUnroll];
+    auto load = [&](int s0, float4* g, float* dc, int* fl, int* sq) {
 #pragma unroll
         for (int u = 0; u < kScanUnroll; ++u) {
             const int s = s0 + u;
             if (s < nseg) {
-                agg[u] = A4[((long long)s * a.H + h) * PN4 + e4];
-                dec[u] = expf(a.lam[(long long)s * a.H + h]);
-                flags[u] = a.segtab[s].flags;
-                seq[u] = a.segtab[s].seq;
+                g[u] = A4[((long long)s * a.H + h) * PN4 + e4];
+                dc[u] = expf(a.lam[(long long)s * a.H + h]);
+                fl[u] = a.segtab[s].flags;
+                sq[u] = a.segtab[s].seq;
             }
         }
+    };
+    load(0, agg, dec, flags, seq);
+    for (int s0 = 0; s0 < nseg; s0 += kScanUnroll) {
+        if (s0 + kScanUnroll < nseg) load(s0 + kScanUnroll, nagg, ndec, nflags, nseqi);
 #pragma unroll
         for (int u = 0; u < kScanUnroll; ++u) {
             const int s = s0 + u;
@@ -173,6 +177,13 @@ __global__ void __launch_bounds__(kScanThreads) state_scan_kernel(Args a, int wr
             if (write_final && (flags[u] & SEG_LAST))
                 reinterpret_cast<float4*>(a.final_state)[((long long)seq[u] * a.H + h) * PN4 + fe4] =
                     carry;
+        }
+#pragma unroll
+        for (int u = 0; u < kScanUnroll; ++u) {
+            agg[u] = nagg[u];
+            dec[u] = ndec[u];
+            flags[u] = nflags[u];
+            seq[u] = nseqi[u];
         }
     }
 }
@@ -188,19 +199,23 @@ __global__ void __launch_bounds__(kScanThreads) adjoint_scan_kernel(Args a) {
     const int nseg = a.hdr->nseg;
     float4* G4 = reinterpret_cast<float4*>(a.adj);
     float4 carry = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int s0 = nseg - 1; s0 >= 0; s0 -= kScanUnroll) {
-        float4 agg[kScanUnroll];
-        float dec[kScanUnroll];
-        int flags[kScanUnroll];
+    float4 agg[kScanUnroll], nagg[kScanUnroll];
+    float dec[kScanUnroll], ndec[kScanUnroll];
+    int flags[kScanUnroll], nflags[kScanUnroll];
+    auto load = [&](int s0, float4* g, float* dc, int* fl) {
 #pragma unroll
         for (int u = 0; u < kScanUnroll; ++u) {
             const int s = s0 - u;
             if (s >= 0) {
-                agg[u] = G4[((long long)s * a.H + h) * PN4 + e4];
-                dec[u] = expf(a.lam[(long long)s * a.H + h]);
-                flags[u] = a.segtab[s].flags;
+                g[u] = G4[((long long)s * a.H + h) * PN4 + e4];
+                dc[u] = expf(a.lam[(long long)s * a.H + h]);
+                fl[u] = a.segtab[s].flags;
             }
         }
+    };
+    load(nseg - 1, agg, dec, flags);
+    for (int s0 = nseg - 1; s0 >= 0; s0 -= kScanUnroll) {
+        if (s0 - kScanUnroll >= 0) load(s0 - kScanUnroll, nagg, ndec, nflags);
 #pragma unroll
         for (int u = 0; u < kScanUnroll; ++u) {
             const int s = s0 - u;
@@ -211,6 +226,12 @@ __global__ void __launch_bounds__(kScanThreads) adjoint_scan_kernel(Args a) {
             carry.y = fmaf(dec[u], carry.y, agg[u].y);
             carry.z = fmaf(dec[u], carry.z, agg[u].z);
             carry.w = fmaf(dec[u], carry.w, agg[u].w);
+        }
+#pragma unroll
+        for (int u = 0; u < kScanUnroll; ++u) {
+            agg[u] = nagg[u];
+            dec[u] = ndec[u];
+            flags[u] = nflags[u];
         }
     }
 }
@@ -244,15 +265,20 @@ __global__ void ddt_finalize_kernel(Args a) {
     }
 }
 
+// fp32 dB / dC accumulators -> outputs, four elements per thread and step (N is a
+// multiple of 8, so T G N is a multiple of 4).
 template <typename TO>
 __global__ void dbc_convert_kernel(Args a) {
-    const long long n = a.T * a.G * a.N;
+    const long long n4 = a.T * a.G * a.N / 4;
     TO* dB = static_cast<TO*>(a.dB);
     TO* dC = static_cast<TO*>(a.dC);
-    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
+    const float4* b4 = reinterpret_cast<const float4*>(a.dbacc);
+    const float4* c4 = reinterpret_cast<const float4*>(a.dcacc);
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n4;
          i += (long long)gridDim.x * blockDim.x) {
-        st_out(dB, i, a.dbacc[i]);
-        st_out(dC, i, a.dcacc[i]);
+        const float4 vb = b4[i], vc = c4[i];
+        st_out4(dB, i, vb);
+        st_out4(dC, i, vc);
     }
 }
 
@@ -301,7 +327,7 @@ cudaError_t launch_bwd_epilogue(const Prob& pb, const Args& a, Launch& L) {
 }
 
 cudaError_t launch_dbc_convert(const Prob& pb, const Args& a, Launch& L) {
-    const long long n = pb.T * pb.G * pb.N;
+    const long long n = pb.T * pb.G * pb.N / 4;
     long long blocks = (n + 255) / 256;
     if (blocks > 152 * 16) blocks = 152 * 16;
     if (blocks < 1) blocks = 1;

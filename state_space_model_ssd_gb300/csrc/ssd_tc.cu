@@ -358,8 +358,11 @@ constexpr int l0_smem_bytes() {
 // m = s_end / 2, and f(t) = exp(s_t - m) (zero past the chunk's tokens), g(t) = delta_t
 // exp(m - s_t), half = -m.  With them exp(s_t - s_s) = f(t) g(s) / delta_s keeps every
 // exponent within |s_end| / 2.  The walks of both passes copy these records instead of
-// recomputing them.  One CTA per chunk slot and pair of heads.
-constexpr int kFacThreads = 128;
+// recomputing them.  One CTA per chunk slot and group of kFacHeads heads: the raw_dt
+// tile (64 tokens x kFacHeads heads) is read with coalesced loads into shared memory,
+// then one warp scans one head's 64 tokens, two per lane.
+constexpr int kFacThreads = 256;
+constexpr int kFacHeads = 16;
 
 __global__ void __launch_bounds__(kFacThreads) tc_factors_kernel(Args a) {
     const int cps = a.Ls / kQ;
@@ -367,25 +370,38 @@ __global__ void __launch_bounds__(kFacThreads) tc_factors_kernel(Args a) {
     if (seg >= a.hdr->nseg) return;
     const SegInfo si = a.segtab[seg];
     if (c >= (si.len + kQ - 1) / kQ) return;
-    __shared__ float red[4];
-    const int ct = threadIdx.x, lane = ct & 31, head = ct >> 6, t = ct & 63;
-    const int hw = (ct >> 5) & 1;
-    const int h = blockIdx.y * 2 + head;  // the head count is even on this path
+    __shared__ float zt[kFacHeads][kQ + 1];  // raw_dt + delta_init, [head][token]
+    const int ct = threadIdx.x, lane = ct & 31, warp = ct >> 5;
+    const int hb = blockIdx.y * kFacHeads;
     const int vc = min(kQ, si.len - c * kQ);
-    float d = 0.f;
-    if (t < vc) d = softplus_f(a.raw[(si.start + (long long)c * kQ + t) * a.H + h] + a.delta_init);
-    float inc = warp_scan(d, lane);
-    if (lane == 31) red[head * 2 + hw] = inc;
+    const long long tok0 = si.start + (long long)c * kQ;
+#pragma unroll
+    for (int k = 0; k < kQ * kFacHeads / kFacThreads; ++k) {
+        const int idx = ct + kFacThreads * k, t = idx / kFacHeads, hh = idx % kFacHeads;
+        float z = 0.f;
+        if (t < vc && hb + hh < a.H) z = a.raw[(tok0 + t) * a.H + hb + hh] + a.delta_init;
+        zt[hh][t] = z;
+    }
     __syncthreads();
-    if (hw) inc += red[head * 2];
-    const float send = red[head * 2] + red[head * 2 + 1];  // sum of delta over the chunk
-    const float half = 0.5f * send;
-    float* rec = a.fac + ((long long)(seg * cps + c) * a.H + h) * kFacRec;
-    rec[FAC_F + t] = (t < vc) ? expf(half - inc) : 0.f;
-    rec[FAC_G + t] = d * expf(inc - half);
-    rec[FAC_D + t] = d;
-    if (t < 4) rec[FAC_HALF + t] = (t == 0) ? half : 0.f;
-    if (t == 0 && send > kMaxChunkDecay) set_status(a.hdr, SSD_ERR_DEVICE);
+    for (int hh = warp; hh < kFacHeads && hb + hh < a.H; hh += kFacThreads / 32) {
+        const int h = hb + hh, t0 = 2 * lane;
+        const float d0 = (t0 < vc) ? softplus_f(zt[hh][t0]) : 0.f;
+        const float d1 = (t0 + 1 < vc) ? softplus_f(zt[hh][t0 + 1]) : 0.f;
+        const float incl = warp_scan(d0 + d1, lane);
+        float excl = __shfl_up_sync(0xffffffffu, incl, 1);
+        if (lane == 0) excl = 0.f;
+        const float send = __shfl_sync(0xffffffffu, incl, 31);  // sum of delta over the chunk
+        const float half = 0.5f * send;
+        const float s0 = excl + d0, s1 = s0 + d1;  // inclusive sums at tokens t0, t0 + 1
+        float* rec = a.fac + ((long long)(seg * cps + c) * a.H + h) * kFacRec;
+        *reinterpret_cast<float2*>(rec + FAC_F + t0) =
+            make_float2((t0 < vc) ? expf(half - s0) : 0.f, (t0 + 1 < vc) ? expf(half - s1) : 0.f);
+        *reinterpret_cast<float2*>(rec + FAC_G + t0) =
+            make_float2(d0 * expf(s0 - half), d1 * expf(s1 - half));
+        *reinterpret_cast<float2*>(rec + FAC_D + t0) = make_float2(d0, d1);
+        if (lane < 4) rec[FAC_HALF + lane] = (lane == 0) ? half : 0.f;
+        if (lane == 0 && send > kMaxChunkDecay) set_status(a.hdr, SSD_ERR_DEVICE);
+    }
 }
 
 // ================================================================ chunk walk
@@ -1094,7 +1110,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 if (c >= 1 && !wait_or_abort(s_free, pc ^ 1, abort_flag, a.hdr)) break;
                 tc_fence_after();
                 const uint32_t xs = smem_u32(sm + Lay::OFF_STAGE + s * Lay::STAGE);
-                const uint32_t ys = xs + 16384, bs = xs + 32768, cs = bs + N * 128;
+                const uint32_t ys = xs + 16384, bs = xs + 32768;
                 if (c < nchunks - 1) {  // chunk state, needed only for later chunks
 #pragma unroll
                     for (int k = 0; k < 4; ++k)
@@ -1172,7 +1188,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         scale_chunk_stage(0);
 
         for (int c = 0; c < nchunks; ++c) {
-            const int s = c & 1, ph = (c >> 1) & 1, pc = c & 1;
+            const int s = c & 1, pc = c & 1;
             const bool last = (c == nchunks - 1);
             const int vc = min(kQ, si.len - c * kQ);
             const long long tok0 = si.start + (long long)c * kQ;
@@ -1843,7 +1859,7 @@ cudaError_t launch_l0(const Prob& pb, const Args& a, Launch& L, const CUtensorMa
 }
 
 cudaError_t launch_factors(const Prob& pb, const Args& a, Launch& L) {
-    const dim3 grid((unsigned)(pb.nseg_max * (pb.Ls / kQ)), pb.H / 2);
+    const dim3 grid((unsigned)(pb.nseg_max * (pb.Ls / kQ)), (pb.H + kFacHeads - 1) / kFacHeads);
     L.begin("tc_factors");
     tc_factors_kernel<<<grid, kFacThreads, 0, L.stream>>>(a);
     return L.end();
