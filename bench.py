@@ -240,6 +240,34 @@ def reference_arm(args, w, rank, world):
     print(json.dumps(line), flush=True)
 
 
+def bind_to_gpu_node(dev_index: int):
+    """Restricts this process to the CPUs that the GPU's PCI device reports as local, so
+    that the pinned host buffers of the end-to-end steps are allocated in the memory
+    attached to the GPU's host link.  Returns (description, previous affinity), or
+    (None, None) where the topology cannot be read."""
+    import torch
+    try:
+        p = torch.cuda.get_device_properties(dev_index)
+        base = "/sys/bus/pci/devices/%04x:%02x:%02x.0" % (p.pci_domain_id, p.pci_bus_id,
+                                                          p.pci_device_id)
+        cpus = set()
+        for part in open(base + "/local_cpulist").read().strip().split(","):
+            if "-" in part:
+                lo, hi = part.split("-")
+                cpus.update(range(int(lo), int(hi) + 1))
+            elif part:
+                cpus.add(int(part))
+        node = open(base + "/numa_node").read().strip()
+        before = os.sched_getaffinity(0)
+        cpus &= before
+        if not cpus or cpus == before:
+            return ("numa node %s, all %d cpus local" % (node, len(before)), None)
+        os.sched_setaffinity(0, cpus)
+        return ("numa node %s, %d of %d cpus" % (node, len(cpus), len(before)), before)
+    except (OSError, ValueError, AttributeError):
+        return (None, None)
+
+
 def gpu_arm(args, w, rank, world, dist):
     import torch
 
@@ -248,6 +276,7 @@ def gpu_arm(args, w, rank, world, dist):
 
     local = int(os.environ.get("LOCAL_RANK", "0"))
     torch.cuda.set_device(local)
+    host_node, prev_affinity = bind_to_gpu_node(local)
     dev = torch.device("cuda", local)
     ssd_build.build()
     d = make_inputs(w, seed=rank)
@@ -376,6 +405,8 @@ def gpu_arm(args, w, rank, world, dist):
         t = torch.tensor([e2e_ms], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         e2e_ms = float(t.item())
+    if prev_affinity is not None:  # the oracle baseline below runs on all the cores again
+        os.sched_setaffinity(0, prev_affinity)
 
     if rank != 0:
         return
@@ -438,7 +469,8 @@ def gpu_arm(args, w, rank, world, dist):
         "kernels": kernels,
         "cpu_baseline": cpu,
         "e2e": {"value": world * tokens_per_step / (e2e_ms * 1e-3), "unit": "tokens/s",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+                "host_buffers": host_node},
         "gpu_launches": launches,
         "clocks": clocks,
     }
