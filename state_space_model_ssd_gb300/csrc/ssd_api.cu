@@ -308,11 +308,8 @@ ssd_status_t ssd_forward(const ssd_problem_t* prob, const void* x, const float* 
     a.cu = cu_seqlens;
     a.y = y;
     a.final_state = final_state;
-    if (cudaMemsetAsync(a.hdr, 0, sizeof(WsHeader), s) != cudaSuccess) return SSD_ERR_CUDA;
-    if (final_state &&
-        cudaMemsetAsync(final_state, 0, sizeof(float) * (size_t)b.nseq * b.H * b.P * b.N, s) !=
-            cudaSuccess)
-        return SSD_ERR_CUDA;
+    // the segment-table kernel resets the header and zeroes the final states that no
+    // segment writes
     Launch L;
     L.stream = s;
     cudaError_t e = b.tc ? tc_forward(b, a, L) : simt_forward(b, a, L);
@@ -355,12 +352,12 @@ ssd_status_t backward_impl(const ssd_problem_t* prob, const void* x, const float
     a.dC = dC;
     // the tensor-core path can take the forward's segment table, tiles, factors and
     // segment states from the workspace (its header is then kept, status included)
+    // (the segment-table kernel resets the header; the tensor-core path's adjoint
+    // aggregate kernel zeroes the dB / dC accumulators)
     const bool reuse = after_forward && b.tc;
-    if (!reuse && cudaMemsetAsync(a.hdr, 0, sizeof(WsHeader), s) != cudaSuccess)
-        return SSD_ERR_CUDA;
     const size_t nbc = sizeof(float) * (size_t)b.T * b.G * b.N;
-    if (cudaMemsetAsync(a.dbacc, 0, nbc, s) != cudaSuccess ||
-        cudaMemsetAsync(a.dcacc, 0, nbc, s) != cudaSuccess)
+    if (!b.tc && (cudaMemsetAsync(a.dbacc, 0, nbc, s) != cudaSuccess ||
+                  cudaMemsetAsync(a.dcacc, 0, nbc, s) != cudaSuccess))
         return SSD_ERR_CUDA;
     Launch L;
     L.stream = s;

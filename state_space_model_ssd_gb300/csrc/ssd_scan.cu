@@ -25,6 +25,9 @@ __global__ void __launch_bounds__(kTableThreads) seg_table_kernel(Args a) {
     __shared__ int bad;
     const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
     if (tid == 0) {
+        // the pass starts here: no error yet, no table yet
+        a.hdr->status = 0;
+        a.hdr->sig_valid = 0;
         base_s = 0;
         bad = 0;
         if (a.cu && (a.cu[0] != 0 || (long long)a.cu[a.nseq] != a.T)) bad = 1;
@@ -34,6 +37,16 @@ __global__ void __launch_bounds__(kTableThreads) seg_table_kernel(Args a) {
         for (int s = tid; s < a.nseq; s += blockDim.x)
             if (a.cu[s + 1] < a.cu[s]) bad = 1;
     __syncthreads();
+    // final states that no segment writes: every row when the boundaries are malformed,
+    // else the rows of empty packed sequences
+    const long long row4 = (long long)a.H * a.P * a.N / 4;
+    if (a.final_state && (bad || a.cu)) {
+        float4* fs4 = reinterpret_cast<float4*>(a.final_state);
+        for (int s = 0; s < a.nseq; ++s)
+            if (bad || a.cu[s + 1] == a.cu[s])
+                for (long long i = tid; i < row4; i += blockDim.x)
+                    fs4[(long long)s * row4 + i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
     if (bad) {
         if (tid == 0) {
             set_status(a.hdr, SSD_ERR_DEVICE);

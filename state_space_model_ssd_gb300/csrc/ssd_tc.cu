@@ -56,6 +56,21 @@ template <int N, int MODE>
 __global__ void __launch_bounds__(kStateThreads, 3)
     tc_seg_state_kernel(const __grid_constant__ CUtensorMap map_x,
                         const __grid_constant__ CUtensorMap map_b, Args a) {
+    if (MODE == 1) {
+        // this CTA's share of the fp32 dB / dC accumulators, which the backward walks that
+        // follow add into, set to zero
+        const long long n4 = a.T * a.G * a.N / 4;
+        const long long nb = (long long)gridDim.x * gridDim.y;
+        const long long per = (n4 + nb - 1) / nb;
+        const long long lo = ((long long)blockIdx.y * gridDim.x + blockIdx.x) * per;
+        const long long hi = lo + per < n4 ? lo + per : n4;
+        float4* db4 = reinterpret_cast<float4*>(a.dbacc);
+        float4* dc4 = reinterpret_cast<float4*>(a.dcacc);
+        for (long long i = lo + threadIdx.x; i < hi; i += blockDim.x) {
+            db4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+            dc4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+    }
     const int seg = blockIdx.x;
     const int h0 = blockIdx.y * 2;
     if (seg >= a.hdr->nseg) return;
