@@ -205,6 +205,11 @@ int ssd_last_launch_count(void);
  * them and reports, per kernel name, the launch count and total device time.
  * Not thread-safe; meant for benchmarks. */
 ssd_status_t ssd_profiler_enable(int on);
+/* Restricts the timing to launches of the kernel called `name` (as reported by
+ * ssd_profiler_entry); NULL times every kernel again.  Each pair of events holds the
+ * launch that follows it back until the kernel before it has finished, so timing
+ * only the kernel of interest leaves the other kernel boundaries of a pass alone. */
+ssd_status_t ssd_profiler_only(const char* name);
 void ssd_profiler_reset(void);
 int ssd_profiler_count(void);
 ssd_status_t ssd_profiler_entry(int index, const char** name, int64_t* launches,

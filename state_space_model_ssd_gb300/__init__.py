@@ -221,6 +221,11 @@ class profiler:
         _lib.lib().ssd_profiler_enable(int(on))
 
     @staticmethod
+    def only(name=None) -> None:
+        """Times only the launches of kernel ``name`` (None: every kernel)."""
+        _lib.lib().ssd_profiler_only(None if name is None else name.encode())
+
+    @staticmethod
     def reset() -> None:
         _lib.lib().ssd_profiler_reset()
 

@@ -62,6 +62,7 @@ _SIGS = {
     "ssd_dispatch_path": (ctypes.c_char_p, [_PP, ctypes.c_int]),
     "ssd_last_launch_count": (ctypes.c_int, []),
     "ssd_profiler_enable": (ctypes.c_int, [ctypes.c_int]),
+    "ssd_profiler_only": (ctypes.c_int, [ctypes.c_char_p]),
     "ssd_profiler_reset": (None, []),
     "ssd_profiler_count": (ctypes.c_int, []),
     "ssd_profiler_entry": (ctypes.c_int, [ctypes.c_int, ctypes.POINTER(ctypes.c_char_p),

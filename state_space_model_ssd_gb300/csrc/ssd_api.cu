@@ -26,6 +26,7 @@ struct ProfTotal {
     double ms;
 };
 bool g_prof_on = false;
+std::string g_prof_only;  // when not empty, only launches of this kernel are timed
 std::vector<ProfRecord> g_prof_pending;
 std::vector<ProfTotal> g_prof_totals;
 std::vector<cudaEvent_t> g_event_pool;
@@ -218,7 +219,7 @@ ssd_status_t check_common(const ssd_problem_t* prob, const int32_t* cu, void* ws
 
 void Launch::begin(const char* name) {
     ++count;
-    if (g_prof_on) {
+    if (g_prof_on && (g_prof_only.empty() || g_prof_only == name)) {
         g_prof_name = name;
         g_prof_start = take_event();
         if (g_prof_start) cudaEventRecord(g_prof_start, stream);
@@ -401,6 +402,11 @@ ssd_status_t ssd_device_status(const void* workspace, void* stream, int32_t* dev
 ssd_status_t ssd_profiler_enable(int on) {
     if (!on && g_prof_on) prof_flush();
     g_prof_on = on != 0;
+    return SSD_OK;
+}
+
+ssd_status_t ssd_profiler_only(const char* name) {
+    g_prof_only = name ? name : "";
     return SSD_OK;
 }
 
