@@ -130,3 +130,9 @@ def test_step_host_checks_arguments_before_any_cuda_call(lib):
     assert call(ctypes.c_void_p(0x40010), n.value) == 3   # not 256-byte aligned
     assert call(dev, n.value, cu=h) == 1                  # cu_seqlens for a dense batch
     assert call(dev, n.value, prob=_prob(headdim=12)) == 2
+
+
+def test_profiler_filter_is_host_only(lib):
+    """Setting or clearing the profiler's kernel filter touches no GPU state."""
+    assert lib.ssd_profiler_only(b"tc_bwd_dxdb") == 0
+    assert lib.ssd_profiler_only(None) == 0

@@ -250,3 +250,28 @@ def test_launch_count_and_profiler(ssd):
     assert n >= 3
     assert sum(v[0] for v in prof.values()) == n
     assert all(v[1] > 0 for v in prof.values())
+
+
+def test_profiler_only_times_the_named_kernel(ssd):
+    """With a kernel name set, the profiler times that kernel's launches alone; with None
+    it times every launch again."""
+    d = _draw(11, 1, 500, 2, 64, 128, dtype="bf16")
+    t = to_device(d, "bf16")
+    try:
+        ssd.profiler.only("tc_fwd_walk")
+        ssd.profiler.reset()
+        ssd.profiler.enable(True)
+        for _ in range(2):
+            ssd.forward(t["x"], t["raw_dt"], t["B"], t["C"], delta_init=-4.6)
+        ssd.profiler.enable(False)
+        prof = ssd.profiler.read()
+        assert list(prof) == ["tc_fwd_walk"] and prof["tc_fwd_walk"][0] == 2
+    finally:
+        ssd.profiler.enable(False)
+        ssd.profiler.only(None)
+    ssd.profiler.reset()
+    ssd.profiler.enable(True)
+    ssd.forward(t["x"], t["raw_dt"], t["B"], t["C"], delta_init=-4.6)
+    n = ssd.last_launch_count()
+    ssd.profiler.enable(False)
+    assert sum(v[0] for v in ssd.profiler.read().values()) == n
