@@ -47,6 +47,22 @@ SM_COUNT = 152
 FP32_LANES_PER_SM = 128
 
 
+def max_over_ranks(x: float, dist, device) -> float:
+    """The largest x over all ranks (x itself without a process group): the job's time
+    is its slowest replica's."""
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(world: int, tokens_per_step: int, ms_per_step: float) -> float:
+    """Whole-job throughput of `world` replicas, each doing tokens_per_step per step."""
+    return world * tokens_per_step / (ms_per_step * 1e-3)
+
+
 def describe(w) -> str:
     kind = "fwd+bwd" if w.backward else "fwd"
     return ("%s %s: batch %d, L=%d, %d heads x P=%d, N=%d, chunk %d, %s x/B/C%s, fp32 raw_dt, "
@@ -359,13 +375,9 @@ def gpu_arm(args, w, rank, world, dist):
     clocks = sampler.stop()
     ms = ev0.elapsed_time(ev1) / args.steps
     prof_dom = ssd.profiler.read()
-    ms_max = ms
-    if dist is not None:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_max = float(t.item())
+    ms_max = max_over_ranks(ms, dist, dev)
     tokens_per_step = w.total_tokens
-    value = world * tokens_per_step / (ms_max * 1e-3)
+    value = job_tokens_per_s(world, tokens_per_step, ms_max)
 
     # ---- end to end through the C ABI on host buffers: every step is one ssd_step_host
     # call, which copies the step's inputs in from pinned host memory, runs the forward
@@ -418,10 +430,7 @@ def gpu_arm(args, w, rank, world, dist):
     e1.record(stream)
     barrier()
     e2e_ms = e0.elapsed_time(e1) / args.steps
-    if dist is not None:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e2e_ms, dist, dev)
     if prev_affinity is not None:  # the oracle baseline below runs on all the cores again
         os.sched_setaffinity(0, prev_affinity)
 
@@ -487,7 +496,7 @@ def gpu_arm(args, w, rank, world, dist):
         "kernels_source": "%d steps after the warm-up, outside the timed region, every launch "
                           "timed; the timed region times only %s" % (nprof, dom),
         "cpu_baseline": cpu,
-        "e2e": {"value": world * tokens_per_step / (e2e_ms * 1e-3), "unit": "tokens/s",
+        "e2e": {"value": job_tokens_per_s(world, tokens_per_step, e2e_ms), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                 "host_buffers": host_node},
         "gpu_launches": launches,
