@@ -123,10 +123,10 @@ def kernel_model(name, w):
 
 
 def measured_traffic(name, w):
-    """DRAM bytes per launch of `name` at workload `w`, from the committed ncu
-    summary profiles/traffic.txt, or None when there is none or the kernel source
-    changed since it was taken (the summary records the source file's sha256)."""
-    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    """DRAM bytes per launch of `name` at workload `w`, from the committed ncu summary
+    profiles/dram_traffic_walks_mamba2.8b_16k.txt, or None when there is none or the
+    kernel source changed since it was taken (the summary records the source's sha256)."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic_walks_mamba2.8b_16k.txt")
     if not os.path.exists(path):
         return None
     import hashlib
