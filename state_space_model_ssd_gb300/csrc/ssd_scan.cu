@@ -42,10 +42,18 @@ __global__ void __launch_bounds__(kTableThreads) seg_table_kernel(Args a) {
     const long long row4 = (long long)a.H * a.P * a.N / 4;
     if (a.final_state && (bad || a.cu)) {
         float4* fs4 = reinterpret_cast<float4*>(a.final_state);
-        for (int s = 0; s < a.nseq; ++s)
-            if (bad || a.cu[s + 1] == a.cu[s])
-                for (long long i = tid; i < row4; i += blockDim.x)
-                    fs4[(long long)s * row4 + i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        // one sequence per thread and pass; the block zeroes the rows of the empty ones
+        for (int s0 = 0; s0 < a.nseq; s0 += blockDim.x) {
+            const int s = s0 + tid;
+            const bool empty = s < a.nseq && (bad || a.cu[s + 1] == a.cu[s]);
+            if (!__syncthreads_or(empty)) continue;
+            for (int k = 0; k < (int)blockDim.x && s0 + k < a.nseq; ++k) {
+                const int sk = s0 + k;
+                if (bad || a.cu[sk + 1] == a.cu[sk])
+                    for (long long i = tid; i < row4; i += blockDim.x)
+                        fs4[(long long)sk * row4 + i] = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+        }
     }
     if (bad) {
         if (tid == 0) {

@@ -275,3 +275,23 @@ def test_profiler_only_times_the_named_kernel(ssd):
     n = ssd.last_launch_count()
     ssd.profiler.enable(False)
     assert sum(v[0] for v in ssd.profiler.read().values()) == n
+
+
+@pytest.mark.parametrize("dtype,P,N", [("f32", 16, 16), ("bf16", 64, 64)])
+def test_many_short_sequences_with_empty_ones(ssd, oracle_mod, dtype, P, N):
+    """1500 packed sequences of 0..4 tokens: every empty sequence's final state is zero
+    (no segment writes it) and the rest match the oracle."""
+    rng = np.random.default_rng(21)
+    lens = rng.integers(0, 5, size=1500)
+    lens[::5] = 0
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    d = _draw(22, 1, int(cu[-1]), 2, P, N, dtype=dtype, cu=cu)
+    t = to_device(d, dtype)
+    y, fs = ssd.forward(t["x"], t["raw_dt"], t["B"], t["C"], delta_init=-4.6,
+                        cu_seqlens=t["cu_seqlens"])
+    yr, fr = oracle_mod.forward(d["x"], d["raw_dt"], d["B"], d["C"], -4.6,
+                                cu_seqlens=d["cu_seqlens"])
+    assert rel_err(to_np(y), yr) <= TOL[dtype]
+    got = to_np(fs)
+    assert np.all(got[lens == 0] == 0.0)
+    assert rel_err(got, fr) <= TOL[dtype]
