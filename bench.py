@@ -42,6 +42,7 @@ from state_space_model_ssd_gb300.inputs import WORKLOADS, make_inputs  # noqa: E
 
 METRIC = "SSD scan tokens/s (fwd, fwd+bwd) on 1 GB300; % of HBM/tensor roofline"
 DEFAULT_WORKLOAD = "mamba2.8b_32k"
+LONG_WORKLOAD = "genomics_2m"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 SM_COUNT = 152
 FP32_LANES_PER_SM = 128
@@ -284,6 +285,126 @@ def bind_to_gpu_node(dev_index: int):
         return (None, None)
 
 
+def roofline_record(dom, prof_dom, w, peaks, peak_kind, clocks):
+    """The dominant kernel's achieved rate against its bound: algorithmic amount per
+    launch (kernel_model) over its average launch duration in the timed region."""
+    if dom is None or dom not in prof_dom:
+        return None
+    bound, amount, unit = kernel_model(dom, w)
+    n_dom, t_dom = prof_dom[dom]
+    avg_s = t_dom / max(n_dom, 1) * 1e-3
+    if bound == "hbm":
+        ach = amount / avg_s / 1e9
+        peak = peaks["hbm_gbs"]
+        return {"kernel": dom, "bound": "hbm", "achieved": ach, "peak": peak, "unit": "GB/s",
+                "frac": ach / peak, "traffic": measured_traffic(dom, w),
+                "algorithmic_bytes": amount, "avg_launch_ms": avg_s * 1e3,
+                "peak_source": "%s hbm_gbs (copy)" % peak_kind}
+    if bound == "alu":
+        clk = (clocks.get("sm_max_mhz") or peaks.get("sm_max_mhz") or 2070.0) * 1e6
+        peak = SM_COUNT * FP32_LANES_PER_SM * 2 * clk / 1e12
+        ach = amount / avg_s / 1e12
+        return {"kernel": dom, "bound": "alu", "achieved": ach, "peak": peak,
+                "unit": "TFLOP/s", "frac": ach / peak, "traffic": None,
+                "avg_launch_ms": avg_s * 1e3,
+                "peak_source": "fp32 FMA: 152 SMs x 128 lanes x 2 flops x max SM clock"}
+    return None
+
+
+def timed_loop(ssd, torch, stream, run, steps, warmup, barrier, profile=True):
+    """Warm-up, a per-kernel breakdown from profiled runs outside the timed region, then
+    `steps` runs between two device events on `stream`; only the dominant kernel's
+    launches are bracketed by the library's events inside the timed region.
+    Returns (ms per run, launches in the timed region, breakdown, dominant kernel,
+    dominant kernel's (launches, total ms) in the timed region)."""
+    for _ in range(warmup):
+        run()
+    prof, dom = {}, None
+    if profile:
+        ssd.profiler.only(None)
+        ssd.profiler.reset()
+        ssd.profiler.enable(True)
+        for _ in range(max(1, min(steps, 10))):
+            run()
+        torch.cuda.synchronize()
+        ssd.profiler.enable(False)
+        prof = ssd.profiler.read()
+        dom = max(prof.items(), key=lambda kv: kv[1][1])[0] if prof else None
+        ssd.profiler.only(dom)
+        ssd.profiler.reset()
+        ssd.profiler.enable(True)
+    barrier()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    launches = 0
+    ev0.record(stream)
+    for _ in range(steps):
+        launches += run()
+    ev1.record(stream)
+    barrier()
+    prof_dom = {}
+    if profile:
+        ssd.profiler.enable(False)
+        ssd.profiler.only(None)
+        prof_dom = ssd.profiler.read()
+    return ev0.elapsed_time(ev1) / steps, launches, prof, dom, prof_dom
+
+
+def breakdown(prof):
+    tot = max(sum(v[1] for v in prof.values()), 1e-12)
+    return {k: {"launches": n, "total_ms": t, "avg_ms": t / max(n, 1), "share": t / tot}
+            for k, (n, t) in prof.items()}
+
+
+def long_seq_record(args, ssd, torch, dev, stream, barrier, peaks, peak_kind, clocks_ref,
+                    rank):
+    """The long-sequence forward (genomics row: 2,097,152 tokens, 16 heads, P = N = 64,
+    delta_init -5.0) timed in this process: tokens/s, its dominant kernel's roofline, the
+    whole pass against the binding roofline, and the oracle on a bounded sample."""
+    w = WORKLOADS[LONG_WORKLOAD]
+    d = make_inputs(w, seed=rank)
+    tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    dv = {k: torch.from_numpy(d[k]).to(dev, tdt) for k in ("x", "B", "C")}
+    dv["raw_dt"] = torch.from_numpy(d["raw_dt"]).to(dev)
+    prob = ssd.make_problem(dv["x"], dv["B"], w.delta_init, w.chunk_size)
+    ws = torch.empty(ssd.workspace_size(prob, False), dtype=torch.uint8, device=dev)
+    y = torch.empty_like(dv["x"])
+    fs = torch.empty((w.batch, w.nheads, w.headdim, w.dstate), dtype=torch.float32, device=dev)
+
+    def run():
+        ssd.forward(dv["x"], dv["raw_dt"], dv["B"], dv["C"], w.delta_init, w.chunk_size,
+                    None, final_state=False, out=y, workspace=ws, final_state_out=fs)
+        return ssd.last_launch_count()
+
+    steps = max(3, min(args.steps, 20))
+    ms, launches, prof, dom, prof_dom = timed_loop(ssd, torch, stream, run, steps,
+                                                  max(3, args.warmup), barrier)
+    fwd_b, _, fwd_f, _ = algorithmic(w)
+    t_bind = max(fwd_b / (peaks["hbm_gbs"] * 1e9), fwd_f / (peaks["bf16_tflops"] * 1e12))
+    rec = {"workload": describe(w), "path": ssd.dispatch_path(prob),
+           "value": w.total_tokens / (ms * 1e-3), "unit": "tokens/s", "ms_per_step": ms,
+           "steps": steps, "gpu_launches": launches,
+           "l2": "inputs larger than L2 (x alone %.0f MB), no flush" % (
+               dv["x"].numel() * dv["x"].element_size() / 1e6),
+           "roofline": roofline_record(dom, prof_dom, w, peaks, peak_kind, clocks_ref),
+           "path_roofline": {"bytes": fwd_b, "flops": fwd_f, "binding_ms": t_bind * 1e3,
+                             "frac": t_bind * 1e3 / ms,
+                             "target_tokens_per_s": 0.6 * w.total_tokens / t_bind},
+           "kernels": breakdown(prof)}
+    del dv, ws, y, fs
+    torch.cuda.empty_cache()
+    if not args.no_cpu_baseline:
+        import oracle
+        oracle.build()
+        tokens = 1 << 18
+        dt, tok = oracle_sample(w, d, w.nheads, tokens, os.cpu_count() or 1)
+        rec["cpu_baseline"] = {
+            "value": tok / dt, "unit": "tokens/s", "cores": oracle.max_threads(),
+            "kind": "oracle",
+            "sample": "all %d heads x first %d tokens, fwd, %.1f s" % (w.nheads, tokens, dt)}
+    return rec
+
+
 def gpu_arm(args, w, rank, world, dist):
     import torch
 
@@ -310,18 +431,22 @@ def gpu_arm(args, w, rank, world, dist):
     ws = torch.empty(max(ssd.workspace_size(prob, False), ssd.workspace_size(prob, True)),
                      dtype=torch.uint8, device=dev)
     y = torch.empty_like(dv["x"])
+    nseq = prob.nseq if prob.nseq > 0 else prob.batch
+    fs = torch.empty((nseq, prob.nheads, prob.headdim, prob.dstate), dtype=torch.float32,
+                     device=dev)
     grads = None
     if w.backward:
         grads = {"dx": torch.empty_like(dv["x"]), "d_raw_dt": torch.empty_like(dv["raw_dt"]),
                  "dB": torch.empty_like(dv["B"]), "dC": torch.empty_like(dv["C"])}
     stream = torch.cuda.current_stream()
 
-    def step(mid=None):
-        _, fs = ssd.forward(dv["x"], dv["raw_dt"], dv["B"], dv["C"], w.delta_init,
-                            w.chunk_size, cu, final_state=True, out=y, workspace=ws)
-        n = ssd.last_launch_count()
-        if mid is not None:
-            mid.record(stream)
+    def forward():
+        ssd.forward(dv["x"], dv["raw_dt"], dv["B"], dv["C"], w.delta_init, w.chunk_size, cu,
+                    final_state=False, out=y, workspace=ws, final_state_out=fs)
+        return ssd.last_launch_count()
+
+    def step():
+        n = forward()
         if w.backward:
             ssd.backward(dv["x"], dv["raw_dt"], dv["B"], dv["C"], dv["dy"], w.delta_init,
                          w.chunk_size, cu, out=grads, workspace=ws, after_forward=True)
@@ -333,48 +458,20 @@ def gpu_arm(args, w, rank, world, dist):
             dist.barrier()
         torch.cuda.synchronize()
 
-    # clocks are sampled from the warm-up on, through the timed region
+    # clocks are sampled from the warm-up on, through every timed region
     sampler = ClockSampler(local)
     sampler.start()
-    for _ in range(args.warmup):
-        step()
-    # ---- per-kernel breakdown and the forward part, from steps outside the timed region
-    # with every launch bracketed by events (each pair holds the next launch back until
-    # the kernel before it has finished, about 4 us per kernel boundary)
-    nprof = max(1, min(args.steps, 10))
-    ssd.profiler.only(None)
-    ssd.profiler.reset()
-    ssd.profiler.enable(True)
-    marks = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-             for _ in range(nprof)]
-    for i in range(nprof):
-        marks[i][0].record(stream)
-        step(marks[i][1])
-    torch.cuda.synchronize()
-    ssd.profiler.enable(False)
-    prof = ssd.profiler.read()
-    ms_fwd = float(np.mean([a.elapsed_time(b) for a, b in marks]))
-    dom = max(prof.items(), key=lambda kv: kv[1][1])[0] if prof else None
-    # ---- timed region: whole steps, device events on the launch stream; the library
-    # brackets only the dominant kernel's launches with events (its duration for the
-    # roofline), so that the other kernel boundaries run as they do unprofiled
-    ssd.profiler.only(dom)
-    ssd.profiler.reset()
-    ssd.profiler.enable(True)
-    barrier()
-    ev0 = torch.cuda.Event(enable_timing=True)
-    ev1 = torch.cuda.Event(enable_timing=True)
-    launches = 0
-    ev0.record(stream)
-    for i in range(args.steps):
-        launches += step()
-    ev1.record(stream)
-    barrier()
-    ssd.profiler.enable(False)
-    ssd.profiler.only(None)
-    clocks = sampler.stop()
-    ms = ev0.elapsed_time(ev1) / args.steps
-    prof_dom = ssd.profiler.read()
+    # ---- the step: forward + backward on resident inputs (per-kernel breakdown from
+    # profiled steps outside the timed region; the timed region brackets only the
+    # dominant kernel's launches with the library's events)
+    ms, launches, prof, dom, prof_dom = timed_loop(ssd, torch, stream, step, args.steps,
+                                                  args.warmup, barrier)
+    # ---- the forward alone, its own timed region (no profiling events at all)
+    ms_fwd = None
+    if w.backward:
+        ms_fwd, _, _, _, _ = timed_loop(ssd, torch, stream, forward, args.steps, args.warmup,
+                                        barrier, profile=False)
+        ms_fwd = max_over_ranks(ms_fwd, dist, dev)
     ms_max = max_over_ranks(ms, dist, dev)
     tokens_per_step = w.total_tokens
     value = job_tokens_per_s(world, tokens_per_step, ms_max)
@@ -386,7 +483,6 @@ def gpu_arm(args, w, rank, world, dist):
     # loader's pipelining).
     host_cu = None if d["cu_seqlens"] is None else torch.from_numpy(
         np.ascontiguousarray(d["cu_seqlens"], dtype=np.int32))
-    nseq = prob.nseq if prob.nseq > 0 else prob.batch
 
     def pinned_like(t):
         return torch.empty(t.shape, dtype=t.dtype).pin_memory()
@@ -431,35 +527,25 @@ def gpu_arm(args, w, rank, world, dist):
     barrier()
     e2e_ms = e0.elapsed_time(e1) / args.steps
     e2e_ms = max_over_ranks(e2e_ms, dist, dev)
+    del dev_buf, host_out
+    torch.cuda.empty_cache()
+
+    peaks, peak_kind = load_peaks()
+    # ---- the long-sequence forward, in the same process (rank 0 only at N > 1)
+    long_seq = None
+    if not args.no_long_seq and rank == 0 and args.workload == DEFAULT_WORKLOAD:
+        del dv, ws, y, grads
+        torch.cuda.empty_cache()
+        long_seq = long_seq_record(args, ssd, torch, dev, stream, barrier, peaks, peak_kind,
+                                   {"sm_max_mhz": None}, rank)
+    clocks = sampler.stop()
     if prev_affinity is not None:  # the oracle baseline below runs on all the cores again
         os.sched_setaffinity(0, prev_affinity)
 
     if rank != 0:
         return
-    peaks, peak_kind = load_peaks()
     fwd_b, bwd_b, fwd_f, bwd_f = algorithmic(w)
-    kernels = {k: {"launches": n, "total_ms": t, "avg_ms": t / max(n, 1),
-                   "share": t / max(sum(v[1] for v in prof.values()), 1e-12)}
-               for k, (n, t) in prof.items()}
-    roof = None
-    if dom is not None and dom in prof_dom:
-        bound, amount, unit = kernel_model(dom, w)
-        n_dom, t_dom = prof_dom[dom]
-        avg_s = t_dom / max(n_dom, 1) * 1e-3  # measured in the timed region
-        if bound == "hbm":
-            ach = amount / avg_s / 1e9
-            peak = peaks["hbm_gbs"]
-            roof = {"kernel": dom, "bound": "hbm", "achieved": ach, "peak": peak, "unit": "GB/s",
-                    "frac": ach / peak, "traffic": measured_traffic(dom, w),
-                    "algorithmic_bytes": amount,
-                    "peak_source": "%s hbm_gbs (copy)" % peak_kind}
-        elif bound == "alu":
-            clk = (clocks.get("sm_max_mhz") or peaks.get("sm_max_mhz") or 2070.0) * 1e6
-            peak = SM_COUNT * FP32_LANES_PER_SM * 2 * clk / 1e12
-            ach = amount / avg_s / 1e12
-            roof = {"kernel": dom, "bound": "alu", "achieved": ach, "peak": peak,
-                    "unit": "TFLOP/s", "frac": ach / peak, "traffic": None,
-                    "peak_source": "fp32 FMA: 152 SMs x 128 lanes x 2 flops x max SM clock"}
+    roof = roofline_record(dom, prof_dom, w, peaks, peak_kind, clocks)
     step_bytes = fwd_b + (bwd_b if w.backward else 0)
     step_flops = fwd_f + (bwd_f if w.backward else 0)
     t_bind = max(step_bytes / (peaks["hbm_gbs"] * 1e9), step_flops / (peaks["bf16_tflops"] * 1e12))
@@ -474,6 +560,12 @@ def gpu_arm(args, w, rank, world, dist):
                "kind": "oracle",
                "sample": "the whole workload once (all %d heads x %d tokens), fwd%s, %.1f s" % (
                    w.nheads, w.seqlen, "+bwd" if w.backward else "", dt)}
+    fwd_rec = None
+    if ms_fwd is not None:
+        t_bind_f = max(fwd_b / (peaks["hbm_gbs"] * 1e9), fwd_f / (peaks["bf16_tflops"] * 1e12))
+        fwd_rec = {"ms": ms_fwd, "tokens_per_s": job_tokens_per_s(world, tokens_per_step, ms_fwd),
+                   "binding_ms": t_bind_f * 1e3, "frac": t_bind_f * 1e3 / ms_fwd,
+                   "source": "its own timed region of %d forward-only steps" % args.steps}
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,
@@ -482,23 +574,25 @@ def gpu_arm(args, w, rank, world, dist):
         "data": "synthetic",
         "config": {"workload": describe(w), "path": path,
                    "l2": "inputs larger than L2 (x alone %.0f MB), no flush" % (
-                       dv["x"].numel() * dv["x"].element_size() / 1e6),
+                       w.total_tokens * w.nheads * w.headdim * (2 if w.dtype == "bf16" else 4)
+                       / 1e6),
                    "parallelism": "replicas" if world > 1 else "single GPU",
                    "global_batch": w.batch * world, "seq_len": w.seqlen},
-        "fwd": {"ms": ms_fwd, "tokens_per_s": tokens_per_step / (ms_fwd * 1e-3)
-                if ms_fwd > 0 else None},
+        "fwd": fwd_rec,
         "path_roofline": {"bytes": step_bytes, "flops": step_flops,
                           "binding_ms": t_bind * 1e3, "frac": t_bind * 1e3 / ms_max,
                           "peaks": "%s hbm %.1f GB/s, bf16 %.1f TFLOP/s" % (
                               peak_kind, peaks["hbm_gbs"], peaks["bf16_tflops"])},
         "roofline": roof,
-        "kernels": kernels,
+        "kernels": breakdown(prof),
         "kernels_source": "%d steps after the warm-up, outside the timed region, every launch "
-                          "timed; the timed region times only %s" % (nprof, dom),
+                          "timed; the timed region times only %s" % (
+                              max(1, min(args.steps, 10)), dom),
         "cpu_baseline": cpu,
         "e2e": {"value": job_tokens_per_s(world, tokens_per_step, e2e_ms), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                 "host_buffers": host_node},
+        "long_seq": long_seq,
         "gpu_launches": launches,
         "clocks": clocks,
     }
@@ -513,6 +607,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-long-seq", action="store_true",
+                    help="skip the long-sequence forward record")
     ap.add_argument("--tokens", type=int, default=0,
                     help="run the workload at this row length instead (profiling a smaller case)")
     args = ap.parse_args()

@@ -78,8 +78,9 @@ typedef struct {
 
 /* Supported shapes: P in {8,16,32,64,128}; N in {8,16,32,64,128};
  * chunk_size in {16,32,64,128,256}; T <= 2^31 - 1; G divides H.
- * bf16 problems with P = 64, N in {64,128}, chunk_size = 64 run on the
- * tensor-core path; every other supported problem runs on the SIMT path. */
+ * bf16 problems with P = 64, N in {64,128}, chunk_size = 64, an even number of heads
+ * per group and at least chunk_size tokens in all run on the tensor-core path; every
+ * other supported problem runs on the SIMT path. */
 
 /* Bytes of device workspace that ssd_forward (for_backward = 0) or
  * ssd_backward (for_backward = 1) needs for `prob`.  Pure host function.
@@ -182,10 +183,19 @@ ssd_status_t ssd_step_host(const ssd_problem_t* prob, const void* x, const float
  *    call's contents (the call clears what it needs cleared); calls that may
  *    overlap on the GPU, from any stream or thread, race and must be ordered
  *    by the caller.
- *  - Allocates nothing: no cudaMalloc, cudaFree or allocating library call. */
+ *  - Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
+ *  - Errors that only the device sees (a malformed cu_seqlens, a wait that timed out)
+ *    go to the status word inside the array; ssd_forward_noalloc_status() reads it.
+ *  - The array's address is kept per device for the life of the process: calling
+ *    cudaDeviceReset() after the first call on a device is not supported. */
 ssd_status_t ssd_forward_noalloc(const ssd_problem_t* prob, const void* x, const float* raw_dt,
                                  const void* B, const void* C, const int32_t* cu_seqlens,
                                  void* y, float* final_state, void* stream);
+
+/* The device status word that the last ssd_forward_noalloc call on the current device
+ * left (SSD_OK, SSD_ERR_DEVICE, SSD_ERR_TIMEOUT), read like ssd_device_status():
+ * synchronises `stream` first.  Returns SSD_ERR_CUDA if that failed. */
+ssd_status_t ssd_forward_noalloc_status(void* stream, int32_t* device_status);
 
 /* Synchronises `stream` and returns in *device_status the status word that
  * the last call using `workspace` left (SSD_OK, SSD_ERR_DEVICE, SSD_ERR_TIMEOUT).

@@ -100,8 +100,10 @@ def _stream(stream):
 
 
 def forward(x, raw_dt, B, C, delta_init: float, chunk_size: int = 64, cu_seqlens=None,
-            final_state: bool = True, out=None, workspace=None, stream=None):
-    """Runs ssd_forward.  Returns ``(y, final_state or None)``."""
+            final_state: bool = True, out=None, workspace=None, stream=None,
+            final_state_out=None):
+    """Runs ssd_forward.  Returns ``(y, final_state or None)``; ``final_state_out`` (a
+    float32 ``[nseq, H, P, N]`` CUDA tensor) receives the final states when given."""
     torch = _torch()
     dev = x.device
     _check_tensor(x, "x")
@@ -114,7 +116,12 @@ def forward(x, raw_dt, B, C, delta_init: float, chunk_size: int = 64, cu_seqlens
     nseq = prob.nseq if prob.nseq > 0 else prob.batch
     y = torch.empty_like(x) if out is None else out
     fs = None
-    if final_state:
+    if final_state_out is not None:
+        _check_tensor(final_state_out, "final_state_out", torch.float32, dev)
+        if tuple(final_state_out.shape) != (nseq, prob.nheads, prob.headdim, prob.dstate):
+            raise ValueError("final_state_out must be [nseq, H, P, N]")
+        fs = final_state_out
+    elif final_state:
         fs = torch.empty((nseq, prob.nheads, prob.headdim, prob.dstate), dtype=torch.float32,
                          device=dev)
     ws = _workspace(workspace_size(prob, False), dev, workspace)

@@ -55,6 +55,7 @@ _SIGS = {
     "ssd_backward_after_forward": (ctypes.c_int, [_PP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP,
                                                   _VP, _VP, _VP, _SZ, _VP]),
     "ssd_forward_noalloc": (ctypes.c_int, [_PP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP]),
+    "ssd_forward_noalloc_status": (ctypes.c_int, [_VP, ctypes.POINTER(ctypes.c_int32)]),
     "ssd_step_host_size": (ctypes.c_int, [_PP, ctypes.POINTER(_SZ)]),
     "ssd_step_host": (ctypes.c_int, [_PP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP,
                                      _VP, _VP, _VP, _SZ, _VP]),

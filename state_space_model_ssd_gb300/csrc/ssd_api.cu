@@ -116,7 +116,11 @@ ssd_status_t make_prob(const ssd_problem_t* p, Prob* out) {
     b.Q = p->chunk_size;
     b.delta_init = p->delta_init;
     b.dtype = p->dtype;
-    b.tc = tc_supported(p->dtype, p->headdim, p->dstate, p->chunk_size, p->nheads, p->ngroups);
+    // Fewer tokens than one chunk: the tensor-core tiles would be mostly padding, and the
+    // SIMT path's fp32 products keep a lone token's head-summed dB / dC exact where the
+    // heads' terms cancel (bf16 operands would leave their rounding in the small sum).
+    b.tc = T >= p->chunk_size &&
+           tc_supported(p->dtype, p->headdim, p->dstate, p->chunk_size, p->nheads, p->ngroups);
     b.Ls = choose_segment_length(T, b.nseq, b.H, b.Q);
     // every sequence (dense row) may end in a partial segment
     b.nseg_max = (T + b.Ls - 1) / b.Ls + b.nseq;
@@ -139,15 +143,18 @@ Layout make_layout(const Prob& b, bool bwd) {
     off = align_up(off + sizeof(float) * (size_t)b.nseg_max * b.H);
     // regions both passes use come first, so that a forward's workspace is a prefix of
     // the backward's (ssd_backward_after_forward reuses it)
-    l.l0 = l.fac = 0;
+    l.l0 = l.fac = l.fb = 0;
     if (b.tc) {  // one 64 x 64 bf16 tile per chunk slot of every segment and group
         l.l0 = off;
         off = align_up(off + (size_t)8192 * b.nseg_max * (b.Ls / b.Q) * b.G);
         // one factor record per chunk slot and head
         l.fac = off;
         off = align_up(off + sizeof(float) * kFacRec * b.nseg_max * (b.Ls / b.Q) * b.H);
+        // one fallback flag per (segment, head pair)
+        l.fb = off;
+        off = align_up(off + sizeof(int) * b.nseg_max * (b.H / 2));
     }
-    l.adj = l.rq = l.rqsuf = l.dbacc = l.dcacc = l.rtok = 0;
+    l.adj = l.rq = l.rqsuf = l.dbacc = l.dcacc = l.rtok = l.cb32 = 0;
     if (bwd) {
         l.adj = off;
         off = align_up(off + sizeof(float) * (size_t)b.nseg_max * b.H * PN);
@@ -161,6 +168,10 @@ Layout make_layout(const Prob& b, bool bwd) {
         off = align_up(off + sizeof(float) * (size_t)b.T * b.G * b.N);
         l.rtok = off;
         off = align_up(off + sizeof(float) * (size_t)b.T * b.H);
+        if (b.tc) {  // fp32 C B^T lower triangle per chunk slot of every segment and group
+            l.cb32 = off;
+            off = align_up(off + sizeof(float) * kCbTri * b.nseg_max * (b.Ls / b.Q) * b.G);
+        }
     }
     l.total = off;
     return l;
@@ -186,6 +197,8 @@ Args make_args(const Prob& b, const Layout& l, void* ws) {
     }
     if (l.l0) a.l0 = reinterpret_cast<unsigned char*>(base + l.l0);
     if (l.fac) a.fac = reinterpret_cast<float*>(base + l.fac);
+    if (l.fb) a.fb = reinterpret_cast<int*>(base + l.fb);
+    if (l.cb32) a.cb32 = reinterpret_cast<float*>(base + l.cb32);
     a.T = b.T;
     a.rowlen = b.rowlen;
     a.nseg_max = b.nseg_max;

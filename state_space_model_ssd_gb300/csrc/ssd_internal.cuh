@@ -53,7 +53,7 @@ struct Prob {
 
 // Byte offsets of the workspace regions.
 struct Layout {
-    size_t header, segtab, A, lam, adj, rq, rqsuf, dbacc, dcacc, rtok, l0, fac, total;
+    size_t header, segtab, A, lam, adj, rq, rqsuf, dbacc, dcacc, rtok, l0, fac, fb, cb32, total;
 };
 
 // Everything a kernel needs; passed by value.
@@ -79,9 +79,15 @@ struct Args {
     float* rqsuf;   // [nseg_max][H]
     float* dbacc;   // [T][G][N] fp32
     float* dcacc;   // [T][G][N] fp32
-    float* rtok;    // [T][H] fp32: dy_t . y_t per token and head (tensor-core backward)
+    float* rtok;    // [T][H] fp32 (tensor-core backward): the part of dy_t . y_t that comes from
+                    // tokens before t's chunk
     unsigned char* l0;  // tensor-core path: [nseg_max][Ls / Q][G] 8 KB tiles, masked C B^T per chunk
     float* fac;         // tensor-core path: [nseg_max][Ls / Q][H] chunk factor records (kFacRec floats)
+    int* fb;            // tensor-core path: [nseg_max][H / 2] 1 where a chunk of the (segment,
+                        // head pair) has a delta sum beyond kMaxChunkDecay: that work item
+                        // runs the SIMT evaluation instead
+    float* cb32;        // tensor-core backward: [nseg_max][Ls / Q][G] lower triangles of the
+                        // 64 x 64 fp32 C_t . B_s (s <= t), kCbTri floats each (cb_tri_row)
     long long T, rowlen;
     long long nseg_max;
     int nseq, H, P, N, G, Q, Ls;
@@ -99,6 +105,10 @@ struct Args {
 __host__ __device__ __forceinline__ long long lm_row(int p, int N) {
     return (long long)(p & ~31) * N + (p & 31) * 4;
 }
+
+// Packed lower triangle of a 64 x 64 tile: row t holds columns 0..t from float t (t + 1) / 2.
+constexpr int kCbTri = 64 * 65 / 2;
+__host__ __device__ __forceinline__ int cb_tri_row(int t) { return t * (t + 1) / 2; }
 
 // Chunk factor record of one chunk and head (tensor-core path, chunk length 64):
 // f[64], g[64], delta[64], half, then padding to a multiple of 16 bytes.

@@ -49,3 +49,12 @@ extern "C" ssd_status_t ssd_forward_noalloc(const ssd_problem_t* prob, const voi
     return ssd_forward(prob, x, raw_dt, B, C, cu_seqlens, y, final_state, scratch,
                        (size_t)SSD_NOALLOC_SCRATCH_BYTES, stream);
 }
+
+// The status word sits at the start of the scratch array, where every workspace keeps it.
+extern "C" ssd_status_t ssd_forward_noalloc_status(void* stream, int32_t* device_status) {
+    if (!device_status) return SSD_ERR_INVALID_ARG;
+    void* scratch = nullptr;
+    ssd_status_t st = noalloc_scratch(&scratch);
+    if (st != SSD_OK) return st;
+    return ssd_device_status(scratch, stream, device_status);
+}

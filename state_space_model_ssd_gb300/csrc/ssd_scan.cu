@@ -19,10 +19,32 @@ constexpr int kTableThreads = 1024;
 // Builds the segment table from cu_seqlens (or the dense row length): every
 // sequence is cut into segments of Ls tokens from its own start.  Checks the
 // boundaries on the device and records SSD_ERR_DEVICE if they are malformed.
+__device__ __forceinline__ void write_segment(const Args& a, long long base, int k, int cnt,
+                                              long long start, int len, int s) {
+    const long long idx = base + k;
+    if (idx < a.nseg_max) {
+        SegInfo e;
+        e.start = start + (long long)k * a.Ls;
+        e.len = min(a.Ls, len - k * a.Ls);
+        e.seq = s;
+        e.flags = (k == 0 ? SEG_FIRST : 0) | (k == cnt - 1 ? SEG_LAST : 0);
+        e.pad[0] = e.pad[1] = e.pad[2] = 0;
+        a.segtab[idx] = e;
+    } else {
+        set_status(a.hdr, SSD_ERR_DEVICE);
+    }
+}
+
+// Sequences with more segments than this are written by the whole block.
+constexpr int kOwnSegments = 8;
+
 __global__ void __launch_bounds__(kTableThreads) seg_table_kernel(Args a) {
     __shared__ int warp_sums[32];
     __shared__ long long base_s;
     __shared__ int bad;
+    __shared__ int nlong;
+    __shared__ int long_seq[kTableThreads];
+    __shared__ long long long_base[kTableThreads];
     const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
     if (tid == 0) {
         // the pass starts here: no error yet, no table yet
@@ -62,6 +84,10 @@ __global__ void __launch_bounds__(kTableThreads) seg_table_kernel(Args a) {
         }
         return;
     }
+    // tensor-core path: no work item falls back to the SIMT evaluation until the chunk
+    // factors say so
+    if (a.fb)
+        for (long long i = tid; i < a.nseg_max * (a.H / 2); i += blockDim.x) a.fb[i] = 0;
     for (int s0 = 0; s0 < a.nseq; s0 += blockDim.x) {
         const int s = s0 + tid;
         long long start = 0;
@@ -91,19 +117,24 @@ __global__ void __launch_bounds__(kTableThreads) seg_table_kernel(Args a) {
         __syncthreads();
         const int excl = v - cnt + (w > 0 ? warp_sums[w - 1] : 0);
         const long long base = base_s + excl;
-        for (int k = 0; k < cnt; ++k) {
-            const long long idx = base + k;
-            if (idx < a.nseg_max) {
-                SegInfo e;
-                e.start = start + (long long)k * a.Ls;
-                e.len = min(a.Ls, len - k * a.Ls);
-                e.seq = s;
-                e.flags = (k == 0 ? SEG_FIRST : 0) | (k == cnt - 1 ? SEG_LAST : 0);
-                e.pad[0] = e.pad[1] = e.pad[2] = 0;
-                a.segtab[idx] = e;
-            } else {
-                set_status(a.hdr, SSD_ERR_DEVICE);
-            }
+        if (tid == 0) nlong = 0;
+        __syncthreads();
+        if (cnt <= kOwnSegments) {
+            for (int k = 0; k < cnt; ++k) write_segment(a, base, k, cnt, start, len, s);
+        } else {
+            const int i = atomicAdd(&nlong, 1);
+            long_seq[i] = s;
+            long_base[i] = base;
+        }
+        __syncthreads();
+        // the long sequences of this batch, one at a time, a segment per thread
+        for (int i = 0; i < nlong; ++i) {
+            const int sl = long_seq[i];
+            const long long st = a.cu ? (long long)a.cu[sl] : (long long)sl * a.rowlen;
+            const int ln = a.cu ? a.cu[sl + 1] - a.cu[sl] : (int)a.rowlen;
+            const int cn = (ln + a.Ls - 1) / a.Ls;
+            for (int k = tid; k < cn; k += blockDim.x)
+                write_segment(a, long_base[i], k, cn, st, ln, sl);
         }
         __syncthreads();
         if (tid == (int)blockDim.x - 1) base_s += excl + cnt;

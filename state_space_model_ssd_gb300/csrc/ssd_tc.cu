@@ -25,6 +25,7 @@
 // entering it.
 #include <mutex>
 
+#include "simt_body.cuh"
 #include "tc_common.cuh"
 
 namespace ssd {
@@ -33,6 +34,38 @@ using namespace tc;
 using namespace tcc;
 
 namespace {
+
+// ================================================================ SIMT fallback
+// Work items (segment, pair of heads) with a chunk whose delta sum exceeds kMaxChunkDecay
+// run the SIMT recurrence on the first simt::kSimtThreads threads of the CTA.
+template <int N>
+__device__ __forceinline__ void fallback_seg_state(const Args& a, int seg, int h0, float* sm,
+                                                int bar, int mode) {
+    const simt::Ctx cx{(int)threadIdx.x, bar};
+    for (int hh = 0; hh < 2; ++hh) {
+        if (mode == 0)
+            simt::seg_state_body<__nv_bfloat16, kP / 8, N / 32>(a, seg, h0 + hh, sm, cx);
+        else
+            simt::adj_state_body<__nv_bfloat16, kP / 8, N / 32>(a, seg, h0 + hh, sm, cx);
+        cx.sync();
+    }
+}
+template <int N>
+__device__ __forceinline__ void fallback_walk(const Args& a, int seg, int h0, float* sm, int bar) {
+    const simt::Ctx cx{(int)threadIdx.x, bar};
+    for (int hh = 0; hh < 2; ++hh) {
+        simt::seg_walk_body<__nv_bfloat16, kP / 8, N / 32>(a, seg, h0 + hh, sm, cx);
+        cx.sync();
+    }
+}
+template <int N>
+__device__ __forceinline__ void fallback_bwd(const Args& a, int seg, int h0, float* sm, int bar) {
+    const simt::Ctx cx{(int)threadIdx.x, bar};
+    for (int hh = 0; hh < 2; ++hh) {
+        simt::bwd_walk_body<__nv_bfloat16, kP / 8, N / 32>(a, seg, h0 + hh, sm, cx, true);
+        cx.sync();
+    }
+}
 
 // ================================================================ segment aggregates
 // Warps: 0 = TMA producer, 1 = MMA issuer (and TMEM owner), 2..9 = compute.
@@ -74,6 +107,12 @@ __global__ void __launch_bounds__(kStateThreads, 3)
     const int seg = blockIdx.x;
     const int h0 = blockIdx.y * 2;
     if (seg >= a.hdr->nseg) return;
+    if (a.fb[(long long)seg * (a.H / 2) + blockIdx.y]) {
+        // a chunk decay beyond the factorisation's range: the SIMT recurrence, both heads
+        extern __shared__ float fsm[];
+        if (threadIdx.x < simt::kSimtThreads) fallback_seg_state<N>(a, seg, h0, fsm, 3, MODE);
+        return;
+    }
     const SegInfo si = a.segtab[seg];
     const int g = h0 / (a.H / a.G);
     const int nchunks = (si.len + kQ - 1) / kQ;
@@ -244,13 +283,17 @@ __global__ void __launch_bounds__(kStateThreads, 3)
 // dx/dB walk reads the same bytes as the MN-major A operand of L0^T (rows u, K = t).
 // Warps: 0 = TMA producer, 1 = MMA issuer, 2..5 = masking epilogue.  Each CTA takes
 // kL0Chunks consecutive chunks of one segment.
+// When a.cb32 is set (the backward), the lower triangle of the same products is also
+// written in fp32 (kCbTri floats per chunk and group, row t from cb_tri_row(t)): the dC
+// walk needs C_t . B_s at the precision its tensor-core products carry it.  write_tile =
+// 0 writes only those.
 constexpr int kL0Threads = 192;
 constexpr int kL0Chunks = 4;
 
 template <int N>
 __global__ void __launch_bounds__(kL0Threads)
     tc_l0_kernel(const __grid_constant__ CUtensorMap map_b,
-                 const __grid_constant__ CUtensorMap map_c, Args a) {
+                 const __grid_constant__ CUtensorMap map_c, Args a, int write_tile) {
     const int cps = a.Ls / kQ;                       // chunk slots per segment
     const int parts = (cps + kL0Chunks - 1) / kL0Chunks;
     const int seg = blockIdx.x / parts;
@@ -343,17 +386,24 @@ __global__ void __launch_bounds__(kL0Threads)
             tc_fence_before();
             mbar_arrive(&tfree[s]);
             if (!ok) continue;
-            unsigned char* tile =
-                a.l0 + (((long long)seg * cps + c0 + j) * a.G + g) * 8192 + tt * 128;
+            const long long slot = ((long long)seg * cps + c0 + j) * a.G + g;
+            unsigned char* tile = a.l0 + slot * 8192 + tt * 128;
+            float* crow = a.cb32 ? a.cb32 + slot * kCbTri + cb_tri_row(tt) + 32 * hf : nullptr;
 #pragma unroll
             for (int e0 = 0; e0 < 32; e0 += 8) {
                 const int e = 32 * hf + e0;
                 float f[8];
 #pragma unroll
                 for (int u = 0; u < 8; ++u) f[u] = (e + u <= tt) ? __uint_as_float(v[e0 + u]) : 0.f;
-                *reinterpret_cast<uint4*>(tile + ((((e >> 3) ^ tt) & 7) << 4)) =
-                    make_uint4(pack_bf16(f[0], f[1]), pack_bf16(f[2], f[3]), pack_bf16(f[4], f[5]),
-                               pack_bf16(f[6], f[7]));
+                if (write_tile)
+                    *reinterpret_cast<uint4*>(tile + ((((e >> 3) ^ tt) & 7) << 4)) =
+                        make_uint4(pack_bf16(f[0], f[1]), pack_bf16(f[2], f[3]),
+                                   pack_bf16(f[4], f[5]), pack_bf16(f[6], f[7]));
+                if (crow) {
+#pragma unroll
+                    for (int u = 0; u < 8; ++u)
+                        if (e + u <= tt) crow[e0 + u] = f[u];
+                }
             }
         }
     }
@@ -415,7 +465,9 @@ __global__ void __launch_bounds__(kFacThreads) tc_factors_kernel(Args a) {
             make_float2(d0 * expf(s0 - half), d1 * expf(s1 - half));
         *reinterpret_cast<float2*>(rec + FAC_D + t0) = make_float2(d0, d1);
         if (lane < 4) rec[FAC_HALF + lane] = (lane == 0) ? half : 0.f;
-        if (lane == 0 && send > kMaxChunkDecay) set_status(a.hdr, SSD_ERR_DEVICE);
+        // beyond this decay the factors would leave fp32 range: the (segment, head pair)
+        // is evaluated by the SIMT recurrence instead (every writer stores the same 1)
+        if (lane == 0 && !(send <= kMaxChunkDecay)) a.fb[(long long)seg * (a.H / 2) + h / 2] = 1;
     }
 }
 
@@ -552,6 +604,7 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
             int gc = 0;
             bool stop = false;
             for (int it = blockIdx.x; it < nitems && !stop; it += gridDim.x) {
+                if (a.fb[it]) continue;  // the SIMT recurrence takes it, below
                 const Item I = item_of(it);
                 for (int c = 0; c < I.nchunks; ++c, ++gc) {
                     const int tok = (int)(I.si.start + (long long)c * kQ);
@@ -602,6 +655,7 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
             int gc = 0;
             bool stop = false;
             for (int it = blockIdx.x; it < nitems && !stop; it += gridDim.x) {
+                if (a.fb[it]) continue;  // the SIMT recurrence takes it, below
                 const Item I = item_of(it);
                 for (int c = 0; c < I.nchunks; ++c, ++gc) {
                     const int s = gc & 1, ph = (gc >> 1) & 1;
@@ -639,6 +693,7 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
             int gc = 0;
             bool stop = false;
             for (int it = blockIdx.x; it < nitems && !stop; it += gridDim.x) {
+                if (a.fb[it]) continue;  // the SIMT recurrence takes it, below
                 const Item I = item_of(it);
                 for (int c = 0; c < I.nchunks; ++c, ++gc) {
                     const int s = gc & 1, ph = (gc >> 1) & 1;
@@ -689,6 +744,7 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
             // ------------------------------------------------ x -> g x
             int gc = 0;
             for (int it = blockIdx.x; it < nitems; it += gridDim.x) {
+                if (a.fb[it]) continue;
                 const Item I = item_of(it);
                 for (int c = 0; c < I.nchunks; ++c, ++gc) {
                     const int xsl = gc % kXS, xph = (gc / kXS) & 1, fs = gc % kFS;
@@ -716,6 +772,7 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
             const int hf = lane >> 4;             // M=64 column half of this lane
             int gc = 0;
             for (int it = blockIdx.x; it < nitems; it += gridDim.x) {
+                if (a.fb[it]) continue;
                 const Item I = item_of(it);
                 for (int c = 0; c < I.nchunks; ++c, ++gc) {
                     // y of the chunk: lane half hf holds head hf, p = 0..63 of token tt
@@ -775,6 +832,7 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
             };
             int gc = 0;
             for (int it = blockIdx.x; it < nitems; it += gridDim.x) {
+                if (a.fb[it]) continue;
                 const Item I = item_of(it);
                 {
                     // the item's first chunk: state entering the segment; its G3 operand
@@ -848,6 +906,18 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
     if (warp == 1) tmem_dealloc(tmem, 512);
 }
 
+// The forward walk of the items (segment, pair of heads) whose chunk decays leave the
+// factorisation's range (tc_fwd_walk skips them): the SIMT recurrence, a persistent grid
+// over the items; it exits at once when there are none.
+template <int N>
+__global__ void __launch_bounds__(simt::kSimtThreads) tc_fallback_walk_kernel(Args a) {
+    extern __shared__ float fsm[];
+    const int npairs = a.H / 2;
+    const int nitems = a.hdr->nseg * npairs;
+    for (int it = blockIdx.x; it < nitems; it += gridDim.x)
+        if (a.fb[it]) fallback_walk<N>(a, it / npairs, (it % npairs) * 2, fsm, 1);
+}
+
 // ================================================================ backward walks
 // Both backward kernels walk a segment chunk by chunk for one pair of heads,
 // with the same warp roles as the forward walk (0 = TMA, 1 = MMA, 2..9 =
@@ -856,10 +926,9 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
 // in the stage.
 //
 // tc_bwd_dc (chunks in order, state Hs_c = exp(m_c) H_c as in the forward walk):
-//   P1_h[t, s] = dy_t . xg_s                                   (M=64, N=64, K=P)
+//   P1_h[t, s] = dyf_t . xg_s                                  (M=64, N=64, K=P)
 //   W_h        = P1_h masked to s <= t                           (epilogue, bf16)
-//   E_h[t, .]  = W_h B + dy_h Hs_h                               (M=64, N=N, K=64 + 64)
-//   dC_h[t, .] = f(t) E_h[t, .]       = H_t^T dy_t for head h    (epilogue)
+//   dC_h[t, .] = W_h B + dyf_h Hs_h   = H_t^T dy_t for head h    (M=64, N=N, K=64 + 64)
 //   r_t,h      = C_t . dC_h[t, .]     = dy_t . y_t
 //   dC         = sum over the pair, added into the fp32 accumulator
 // tc_bwd_dxdb (chunks in reverse, adjoint Gs_c = exp(s_end - m) G_c where G_c
@@ -878,14 +947,15 @@ struct BwdLayout {
     static constexpr int STAGE = 32768 + 2 * N * 128;      // x h0|h1, dy h0|h1, B, C
     static constexpr int OFF_STAGE = 0;
     static constexpr int OFF_T0 = 2 * STAGE;               // two 8K operand tiles (W / P2m)
-    static constexpr int OFF_T1 = OFF_T0 + 16384;          // 8K (L0T)
-    static constexpr int OFF_S = OFF_T1 + 8192;            // state operand, 2 x (N/64) x 16K
+    static constexpr int OFF_S = OFF_T0 + 16384;           // state operand, 2 x (N/64) x 16K
     static constexpr int SBUF = (N / 64) * 16384;
-    static constexpr int OFF_F = OFF_S + 2 * SBUF;         // f, g, delta: [2 buf][2 head][64] each
+    static constexpr int OFF_CB = OFF_S + 2 * SBUF;        // fp32 C B^T triangle of a chunk
+    static constexpr int OFF_F = OFF_CB + kCbTri * 4;      // f, g, delta: [2 buf][2 head][64] each
     static constexpr int OFF_SC = OFF_F + 3 * 2 * 2 * 64 * 4;  // half: [2 buf][2 head][4]
     static constexpr int OFF_RQ = OFF_SC + 2 * 2 * 4 * 4;      // [2 wg][2 head][64]
     static constexpr int OFF_RED = OFF_RQ + 2 * 2 * 64 * 4;    // [16]
-    static constexpr int OFF_BAR = OFF_RED + 64;
+    static constexpr int OFF_RI = OFF_RED + 64;                // [2 head][64]
+    static constexpr int OFF_BAR = OFF_RI + 2 * 64 * 4;
     static constexpr int NBAR = 16;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr int TOTAL = OFF_MISC + 16 + 1024;
@@ -940,13 +1010,16 @@ __device__ __forceinline__ void bwd_factors(const ChunkFactors& F, const FacVals
     named_sync(1, kCT);
 }
 
-// x -> g x in place (the 2 x tiles at the start of a stage).
-__device__ __forceinline__ void bwd_scale_x(unsigned char* st, const float* gv, int ct) {
+// x -> g x and dy -> f dy in place (the 2 x tiles and the 2 dy tiles at the start of a
+// stage), with the rounding the dx/dB walk's scaling applies to the same values.
+__device__ __forceinline__ void bwd_scale_xdy(unsigned char* st, const float* gv, const float* fv,
+                                              int ct) {
     uint4* xs = reinterpret_cast<uint4*>(st);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const int idx = ct + kCT * i;  // 0..1023: [x h0 | x h1] 16-byte chunks
-        xs[idx] = scale_chunk(xs[idx], gv[(idx >> 9) * 64 + ((idx >> 3) & 63)]);
+    for (int i = 0; i < 8; ++i) {
+        const int idx = ct + kCT * i;  // 0..2047: [x h0 | x h1 | dy h0 | dy h1] 16-byte chunks
+        const int k = ((idx >> 9) & 1) * 64 + ((idx >> 3) & 63);
+        xs[idx] = scale_chunk(xs[idx], (idx < 1024) ? gv[k] : fv[k]);
     }
 }
 
@@ -975,6 +1048,44 @@ __device__ __forceinline__ void masked_tile(uint32_t taddr_row, unsigned char* t
             make_uint4(pack_bf16(f[0], f[1]), pack_bf16(f[2], f[3]), pack_bf16(f[4], f[5]),
                        pack_bf16(f[6], f[7]));
     }
+}
+
+// masked_tile for the lower mask (u <= t) that also returns two sums over this thread's
+// columns u <= t, with cb[u] = C_t . B_u in fp32 (zero past t):
+//   .x = sum bf16(P[t, u]) cb[u]         (the tile as its MMA sees it, with exact C B^T),
+//   .y = sum P[t, u] bf16(cb[u])         (fp32 P with the bf16 C B^T tile's values).
+__device__ __forceinline__ float2 masked_tile_lower_dots(uint32_t taddr_row, unsigned char* tile,
+                                                         int t, int hf, bool active,
+                                                         const float* cb) {
+    uint32_t v[32];
+    tmem_ld16x2<32>(taddr_row + 0, &v[0]);
+    tmem_ld16x2<32>(taddr_row + 16, &v[16]);
+    tmem_wait_ld_regs<32>(v);
+    if (!active) return make_float2(0.f, 0.f);
+    unsigned char* row = tile + t * 128;
+    float dr = 0.f, dc = 0.f;
+#pragma unroll
+    for (int e0 = 0; e0 < 32; e0 += 8) {
+        const int e = 32 * hf + e0;
+        float f[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) f[u] = (e + u <= t) ? __uint_as_float(v[e0 + u]) : 0.f;
+        uint32_t w[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) w[i] = pack_bf16(f[2 * i], f[2 * i + 1]);
+        *reinterpret_cast<uint4*>(row + ((((e >> 3) ^ t) & 7) << 4)) =
+            make_uint4(w[0], w[1], w[2], w[3]);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float2 r = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[i]));
+            const float2 l = __bfloat1622float2(__floats2bfloat162_rn(cb[e0 + 2 * i], cb[e0 + 2 * i + 1]));
+            dr = fmaf(r.x, cb[e0 + 2 * i], dr);
+            dr = fmaf(r.y, cb[e0 + 2 * i + 1], dr);
+            dc = fmaf(f[2 * i], l.x, dc);
+            dc = fmaf(f[2 * i + 1], l.y, dc);
+        }
+    }
+    return make_float2(dr, dc);
 }
 
 // bf16(S) of this thread's row (h,p) and column half into the state operand buffer.
@@ -1016,6 +1127,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const int seg = blockIdx.x;
     const int h0 = blockIdx.y * 2;
     if (seg >= a.hdr->nseg) return;
+    // an item beyond the factorisation's range: the dx/dB walk's SIMT evaluation adds dC
+    if (a.fb[(long long)seg * (a.H / 2) + blockIdx.y]) return;
     const SegInfo si = a.segtab[seg];
     const int g = h0 / (a.H / a.G);
     const int nchunks = (si.len + kQ - 1) / kQ;
@@ -1030,6 +1143,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     F.scal = reinterpret_cast<float*>(sm + Lay::OFF_SC);
     F.red = reinterpret_cast<float*>(sm + Lay::OFF_RED);
     float* rpart = reinterpret_cast<float*>(sm + Lay::OFF_RQ);  // [2 wg][2 head][64]
+    // [2 head][64]: ri_t - cs_t of the in-chunk sums below
+    float* rint = reinterpret_cast<float*>(sm + Lay::OFF_RI);
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + Lay::OFF_BAR);
     uint64_t* full = bars + 0;      // [2]
     // [2] the chunk's partial dC tiles are in its stage, which the compute threads no
@@ -1043,6 +1158,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     uint64_t* dc_full = bars + 10;
     uint64_t* dc_free = bars + 11;
     uint64_t* h_ready = bars + 12;  // [2], one per state operand buffer
+    uint64_t* cb_full = bars + 14;  // the chunk's C B^T triangle landed
+    uint64_t* cb_free = bars + 15;  // ... and was read by both compute warpgroups
+    const float* cbt = reinterpret_cast<const float*>(sm + Lay::OFF_CB);
     uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + Lay::OFF_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tslot + 1);
     const uint32_t T_S = 0, T_P1 = 128, T_DC = 256;  // TMEM columns
@@ -1062,6 +1180,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         mbar_init(&h_ready[1], kCT);
         mbar_init(dc_full, 1);
         mbar_init(dc_free, kCT);
+        mbar_init(cb_full, 1);
+        mbar_init(cb_free, kCT);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -1108,6 +1228,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     tma_load_3d(st + 32768 + N * 128 + nb * 8192, &map_c, &full[s], nb * 64, g,
                                 tok);
                 }
+                // the chunk's fp32 C B^T triangle, once the previous one has been read
+                if (c >= 1 && !wait_or_abort(cb_free, (c - 1) & 1, abort_flag, a.hdr)) break;
+                mbar_expect_tx(cb_full, kCbTri * 4);
+                bulk_load(sm + Lay::OFF_CB,
+                          a.cb32 + (((long long)seg * (a.Ls / kQ) + c) * a.G + g) * kCbTri,
+                          kCbTri * 4, cb_full);
             }
             for (int cc = nchunks >= 2 ? nchunks - 2 : 0; cc < nchunks && run; ++cc)
                 run = add_partial(cc);
@@ -1190,13 +1316,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         write_state<NH>(sm + Lay::OFF_S, Hs, r, n0);
         fence_proxy_async();
         mbar_arrive(&h_ready[0]);
-        // x -> g x of chunk cc in its stage (factors in buffer cc & 1); dy stays unscaled:
-        // f(t) multiplies whole rows t of P1 and of dyf Hs, so the epilogue applies it to
-        // the rows of dC and r instead
+        // x -> g x and dy -> f dy of chunk cc in its stage (factors in buffer cc & 1): the
+        // dx/dB walk forms q from the same bf16 f dy, which the in-chunk sums below need
         auto scale_chunk_stage = [&](int cc) {
             const int sc = cc & 1;
             if (wait_or_abort(&full[sc], (cc >> 1) & 1, abort_flag, a.hdr))
-                bwd_scale_x(sm + Lay::OFF_STAGE + sc * Lay::STAGE, F.gbuf + sc * 128, ct);
+                bwd_scale_xdy(sm + Lay::OFF_STAGE + sc * Lay::STAGE, F.gbuf + sc * 128,
+                              F.fbuf + sc * 128, ct);
             fence_proxy_async();
             mbar_arrive(xg_ready);
         };
@@ -1209,13 +1335,34 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             const long long tok0 = si.start + (long long)c * kQ;
             unsigned char* st = sm + Lay::OFF_STAGE + s * Lay::STAGE;
             const FacVals fac_next = load_fac_vals(a, seg, h0, c + 1, nchunks, ct);
-            // B: W_h = P1_h masked to s <= t (warpgroup h handles head h)
+            // B: W_h = P1_h masked to s <= t (warpgroup h handles head h), and two in-chunk
+            // sums of row t for the delta gradient:
+            //   ri_t = sum_s W_h[t, s] C_t . B_s, the part of r_t from the chunk's own tokens
+            //          as the dC MMA gives it (bf16 W_h, exact products), and
+            //   cs_t = sum_s P1_h[t, s] L0[t, s], the same pairs as the dx/dB walk's DX MMA
+            //          gives them (fp32 products of the bf16 f dy, g x and L0 values).
+            // r_t - ri_t + cs_t is stored: summed over u >= t it leaves, up to fp32 rounding,
+            // the in-chunk pairs s < t <= u that the delta gradient needs, instead of the
+            // difference of two differently rounded sums of every in-chunk pair.
             {
-                const bool ok = wait_or_abort(p1_full, pc, abort_flag, a.hdr);
+                bool ok = wait_or_abort(cb_full, pc, abort_flag, a.hdr);
+                // row t of the triangle, columns 32 hf .. 32 hf + 31 (those past t are
+                // masked; the index stays inside the triangle for every t)
+                float cbv[32];
+                const float* crow = cbt + cb_tri_row(t) + 32 * hf;
+#pragma unroll
+                for (int j = 0; j < 32; ++j) cbv[j] = (32 * hf + j <= t) ? crow[j] : 0.f;
+                mbar_arrive(cb_free);
+                ok = wait_or_abort(p1_full, pc, abort_flag, a.hdr) && ok;
                 tc_fence_after();
-                masked_tile(tq + T_P1 + wg * 64, sm + Lay::OFF_T0 + wg * 8192, t, hf, ok, true);
+                const float2 dots = masked_tile_lower_dots(tq + T_P1 + wg * 64,
+                                                           sm + Lay::OFF_T0 + wg * 8192, t, hf,
+                                                           ok, cbv);
                 fence_proxy_async();
                 mbar_arrive(w_ready);
+                const float dd = dots.x - dots.y;
+                const float dsum = dd + __shfl_xor_sync(0xffffffffu, dd, 16);  // whole warp
+                if (hf == 0) rint[wg * 64 + t] = dsum;
             }
             // C: chunk state -> Hs for the next chunk (kept in registers until dC is done)
             if (!last) {
@@ -1253,7 +1400,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 const bool ok = wait_or_abort(dc_full, pc, abort_flag, a.hdr);
                 tc_fence_after();
                 const unsigned char* cst = st + 32768 + N * 128;
-                const float f0 = F.fbuf[s * 128 + t], f1 = F.fbuf[s * 128 + 64 + t];
                 float rp0 = 0.f, rp1 = 0.f;
                 // the partial dC tiles go into this stage's x / dy tiles, which every MMA of
                 // the chunk has finished reading
@@ -1293,14 +1439,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                         float sum[16];
 #pragma unroll
                         for (int u = 0; u < 16; ++u)
-                            sum[u] = (ok && t < vc) ? fmaf(f0, __uint_as_float(v0[u]),
-                                                           f1 * __uint_as_float(v1[u]))
+                            sum[u] = (ok && t < vc) ? __uint_as_float(v0[u]) + __uint_as_float(v1[u])
                                                     : 0.f;
                         stage_row16(rtiles, t, n, sum);
                     }
                 }
-                rp0 = f0 * (rp0 + __shfl_xor_sync(0xffffffffu, rp0, 16));
-                rp1 = f1 * (rp1 + __shfl_xor_sync(0xffffffffu, rp1, 16));
+                rp0 += __shfl_xor_sync(0xffffffffu, rp0, 16);
+                rp1 += __shfl_xor_sync(0xffffffffu, rp1, 16);
                 tc_fence_before();
                 mbar_arrive(dc_free);
                 fence_proxy_async();
@@ -1311,8 +1456,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 }
                 named_sync(1, kCT);
                 if (wg == 0 && hf == 0 && t < vc && ok) {
-                    a.rtok[(tok0 + t) * a.H + h0] = rpart[0 * 64 + t] + rpart[2 * 64 + t];
-                    a.rtok[(tok0 + t) * a.H + h0 + 1] = rpart[1 * 64 + t] + rpart[3 * 64 + t];
+                    a.rtok[(tok0 + t) * a.H + h0] =
+                        (rpart[0 * 64 + t] + rpart[2 * 64 + t]) - rint[t];
+                    a.rtok[(tok0 + t) * a.H + h0 + 1] =
+                        (rpart[1 * 64 + t] + rpart[3 * 64 + t]) - rint[64 + t];
                 }
             }
             named_sync(1, kCT);  // rpart reuse
@@ -1363,6 +1510,13 @@ __global__ void __launch_bounds__(kDxThreads, 1)
     const int seg = blockIdx.x;
     const int h0 = blockIdx.y * 2;
     if (seg >= a.hdr->nseg) return;
+    if (a.fb[(long long)seg * (a.H / 2) + blockIdx.y]) {
+        // a chunk decay beyond the factorisation's range: the SIMT recurrence for both heads
+        // (dx, dB and dC added into the accumulators, the finished d_raw_dt)
+        extern __shared__ float fsm[];
+        if (threadIdx.x < simt::kSimtThreads) fallback_bwd<N>(a, seg, h0, fsm, 10);
+        return;
+    }
     const SegInfo si = a.segtab[seg];
     const int g = h0 / (a.H / a.G);
     const int nchunks = (si.len + kQ - 1) / kQ;
@@ -1863,13 +2017,14 @@ cudaError_t set_smem(K kernel, int bytes) {
 
 template <int N>
 cudaError_t launch_l0(const Prob& pb, const Args& a, Launch& L, const CUtensorMap& mb,
-                      const CUtensorMap& mc) {
+                      const CUtensorMap& mc, bool write_tile = true) {
     const int cps = pb.Ls / kQ;
     const dim3 grid((unsigned)(pb.nseg_max * ((cps + kL0Chunks - 1) / kL0Chunks)), pb.G);
     cudaError_t e = set_smem(tc_l0_kernel<N>, l0_smem_bytes<N>());
     if (e != cudaSuccess) return e;
     L.begin("tc_l0");
-    tc_l0_kernel<N><<<grid, kL0Threads, l0_smem_bytes<N>(), L.stream>>>(mb, mc, a);
+    tc_l0_kernel<N><<<grid, kL0Threads, l0_smem_bytes<N>(), L.stream>>>(mb, mc, a,
+                                                                        write_tile ? 1 : 0);
     return L.end();
 }
 
@@ -1906,6 +2061,10 @@ cudaError_t forward_n(const Prob& pb, const Args& a, Launch& L) {
     const dim3 pgrid((unsigned)(items < sm_count() ? items : sm_count()));
     L.begin("tc_fwd_walk");
     tc_fwd_walk_kernel<N><<<pgrid, kWalkThreads, WalkLayout<N>::TOTAL, L.stream>>>(mx, mb, mc, a);
+    if ((e = L.end()) != cudaSuccess) return e;
+    constexpr int fsmem = sizeof(float) * simt::walk_smem_floats(kP, N);
+    L.begin("tc_fallback_walk");
+    tc_fallback_walk_kernel<N><<<(unsigned)(2 * sm_count()), simt::kSimtThreads, fsmem, L.stream>>>(a);
     return L.end();
 }
 
@@ -1920,8 +2079,10 @@ cudaError_t backward_n(const Prob& pb, const Args& a, Launch& L, bool reuse_forw
     cudaError_t e;
     if (reuse_forward) {
         // the forward's segment table, tiles, factors and segment states are in the
-        // workspace; only check that they were made for these inputs
+        // workspace; only check that they were made for these inputs, and add the fp32
+        // C B^T tiles the forward does not make
         if ((e = launch_forward_match(pb, a, L)) != cudaSuccess) return e;
+        if ((e = launch_l0<N>(pb, a, L, mb, mc, false)) != cudaSuccess) return e;
     } else {
         if ((e = launch_seg_table(pb, a, L)) != cudaSuccess) return e;
         if ((e = launch_l0<N>(pb, a, L, mb, mc)) != cudaSuccess) return e;

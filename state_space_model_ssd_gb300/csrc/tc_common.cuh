@@ -14,7 +14,9 @@ using namespace tc;
 
 constexpr int kQ = 64;                 // chunk length
 constexpr int kP = 64;                 // head dimension
-constexpr float kMaxChunkDecay = 160.f;
+// Largest delta sum over a chunk that the factorisation exp(s_t - s_s) = f(t) g(s) / delta_s
+// carries: factors stay within exp(+-64).  Chunks beyond it run the SIMT evaluation.
+constexpr float kMaxChunkDecay = 128.f;
 constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr uint32_t kSleepHintNs = 20000;  // longest suspension per check of a wait
 

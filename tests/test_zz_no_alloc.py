@@ -9,6 +9,8 @@ failure has already run every other test.
 """
 
 import ctypes
+import os
+import re
 
 import numpy as np
 import pytest
@@ -17,7 +19,18 @@ from helpers import TOL, rel_err, to_device, to_np
 
 pytestmark = pytest.mark.gpu
 
-SCRATCH_BYTES = 64 << 20  # SSD_NOALLOC_SCRATCH_BYTES in include/ssd.h
+
+
+def _scratch_bytes() -> int:
+    """SSD_NOALLOC_SCRATCH_BYTES as include/ssd.h defines it."""
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    text = open(os.path.join(root, "include", "ssd.h")).read()
+    m = re.search(r"#define\s+SSD_NOALLOC_SCRATCH_BYTES\s+\((\d+)u\s*<<\s*(\d+)\)", text)
+    assert m, "SSD_NOALLOC_SCRATCH_BYTES not found in ssd.h"
+    return int(m.group(1)) << int(m.group(2))
+
+
+SCRATCH_BYTES = _scratch_bytes()
 
 
 @pytest.fixture(scope="module")
@@ -87,12 +100,38 @@ def test_noalloc_matches_forward_on_consecutive_calls(ssd, dtype, shape):
 
 def test_noalloc_rejects_problems_beyond_its_scratch(ssd):
     import torch
-    x = torch.zeros(1, 1 << 18, 16, 64, dtype=torch.bfloat16, device="cuda")
-    B = torch.zeros(1, 1 << 18, 1, 128, dtype=torch.bfloat16, device="cuda")
-    prob = ssd.make_problem(x, B, -4.6)
-    assert ssd.workspace_size(prob, False) > SCRATCH_BYTES
-    raw = torch.zeros(1, 1 << 18, 16, device="cuda")
+    # the shortest power-of-two length whose forward workspace exceeds the scratch
+    L = 1 << 10
+    while True:
+        x = torch.empty(1, L, 16, 64, dtype=torch.bfloat16, device="meta")
+        B = torch.empty(1, L, 1, 128, dtype=torch.bfloat16, device="meta")
+        if ssd.workspace_size(ssd.make_problem(x, B, -4.6), False) > SCRATCH_BYTES:
+            break
+        L *= 2
+    x = torch.zeros(1, L, 16, 64, dtype=torch.bfloat16, device="cuda")
+    B = torch.zeros(1, L, 1, 128, dtype=torch.bfloat16, device="cuda")
+    raw = torch.zeros(1, L, 16, device="cuda")
     t = {"x": x, "B": B, "C": B, "raw_dt": raw, "cu_seqlens": None}
     st, y, _ = _noalloc(ssd, t, -4.6)
     assert st == 4  # SSD_ERR_WORKSPACE, nothing launched
     assert bool(torch.isnan(y[0, :4]).all())
+
+
+def test_noalloc_reports_device_status(ssd):
+    """A non-monotone cu_seqlens is caught on the device; the no-alloc path's status query
+    reports it, and a following good call clears it."""
+    import torch
+    from state_space_model_ssd_gb300 import _lib
+    d = _draw(23, 1, 100, 2, 16, 16, "f32", cu=[0, 60, 40, 100])
+    t = to_device(d, "f32")
+    st, _, _ = _noalloc(ssd, t, -4.6)
+    assert st == 0
+    v = ctypes.c_int32(-1)
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    assert _lib.lib().ssd_forward_noalloc_status(stream, ctypes.byref(v)) == 0
+    assert v.value == 7  # SSD_ERR_DEVICE
+    t["cu_seqlens"] = torch.tensor([0, 40, 60, 100], dtype=torch.int32, device="cuda")
+    st, _, _ = _noalloc(ssd, t, -4.6)
+    assert st == 0
+    assert _lib.lib().ssd_forward_noalloc_status(stream, ctypes.byref(v)) == 0
+    assert v.value == 0
