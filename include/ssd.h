@@ -98,6 +98,17 @@ ssd_status_t ssd_forward(const ssd_problem_t* prob, const void* x, const float* 
                          float* final_state, void* workspace, size_t workspace_bytes,
                          void* stream);
 
+/* ssd_forward from a given state per sequence: H = initial_state[seq] before the first
+ * token of every sequence (dense row) instead of zero -- the carried-over state of page
+ * "Mamba-2架构与LaCT并行计算技术解析" §1.1 (the note on initialising H from the previous
+ * frame's final state).  initial_state: [nseq or batch][H][P][N] float32 device memory,
+ * 16-byte aligned, or NULL for zero (then this is ssd_forward).  The final state of an
+ * empty packed sequence is its initial state. */
+ssd_status_t ssd_forward_state(const ssd_problem_t* prob, const void* x, const float* raw_dt,
+                               const void* B, const void* C, const int32_t* cu_seqlens,
+                               const float* initial_state, void* y, float* final_state,
+                               void* workspace, size_t workspace_bytes, void* stream);
+
 /* Backward of ssd_forward for an upstream gradient dy of y (the gradient of
  * final_state is taken as zero).  Writes dx [T][H][P], d_raw_dt [T][H]
  * (float32, includes the softplus derivative), dB and dC [T][G][N] (summed
@@ -117,7 +128,8 @@ ssd_status_t ssd_backward(const ssd_problem_t* prob, const void* x, const float*
  * forward's segment table, masked C B^T tiles, chunk factors and segment states from the
  * workspace instead of recomputing them (activations saved by the forward, in the
  * sense of page "Mamba-2架构与LaCT并行计算技术解析" §4.1); the results are those of
- * ssd_backward.  The forward records its problem and input pointers in the workspace;
+ * ssd_backward.  The forward records its problem and input pointers (initial_state
+ * included) in the workspace;
  * if they differ from this call's, the device status becomes SSD_ERR_WORKSPACE and no
  * gradient is computed (ssd_device_status reports it).  Buffer contents are not
  * compared: changing them between the two calls gives the gradient at the old inputs.
@@ -128,6 +140,24 @@ ssd_status_t ssd_backward_after_forward(const ssd_problem_t* prob, const void* x
                                         const int32_t* cu_seqlens, const void* dy, void* dx,
                                         float* d_raw_dt, void* dB, void* dC, void* workspace,
                                         size_t workspace_bytes, void* stream);
+
+/* Backward of ssd_forward_state: the gradient of
+ *     L = sum_t dy_t . y_t + sum_seq <d_final_state[seq], final_state[seq]>
+ * with respect to x, raw_dt, B, C (written as by ssd_backward) and, when d_initial_state is
+ * not NULL, to initial_state: d_initial_state[seq] = dL / dH before the sequence's first
+ * token ([nseq or batch][H][P][N] float32; an empty sequence's is its d_final_state).
+ * initial_state (NULL: zero) must be the one the forward used; d_final_state ([nseq or
+ * batch][H][P][N] float32, NULL: zero) is the upstream gradient of final_state.  Reverse
+ * mode of the recurrence of page "Mamba-2架构与LaCT并行计算技术解析" §1.1.
+ * after_forward != 0: as ssd_backward_after_forward (the preceding ssd_forward_state on the
+ * same workspace, inputs and initial_state); 0: as ssd_backward.  workspace: >=
+ * ssd_workspace_size(prob, 1) bytes. */
+ssd_status_t ssd_backward_state(const ssd_problem_t* prob, const void* x, const float* raw_dt,
+                                const void* B, const void* C, const int32_t* cu_seqlens,
+                                const float* initial_state, const void* dy,
+                                const float* d_final_state, void* dx, float* d_raw_dt, void* dB,
+                                void* dC, float* d_initial_state, int after_forward,
+                                void* workspace, size_t workspace_bytes, void* stream);
 
 /* Device bytes that ssd_step_host needs for `prob`: the backward workspace followed by
  * device copies of the step's inputs and results.  Pure host function. */

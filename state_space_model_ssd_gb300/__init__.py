@@ -101,9 +101,10 @@ def _stream(stream):
 
 def forward(x, raw_dt, B, C, delta_init: float, chunk_size: int = 64, cu_seqlens=None,
             final_state: bool = True, out=None, workspace=None, stream=None,
-            final_state_out=None):
-    """Runs ssd_forward.  Returns ``(y, final_state or None)``; ``final_state_out`` (a
-    float32 ``[nseq, H, P, N]`` CUDA tensor) receives the final states when given."""
+            final_state_out=None, initial_state=None):
+    """Runs ssd_forward (ssd_forward_state with ``initial_state``, a float32
+    ``[nseq, H, P, N]`` CUDA tensor).  Returns ``(y, final_state or None)``;
+    ``final_state_out`` (float32 ``[nseq, H, P, N]``) receives the final states when given."""
     torch = _torch()
     dev = x.device
     _check_tensor(x, "x")
@@ -124,20 +125,28 @@ def forward(x, raw_dt, B, C, delta_init: float, chunk_size: int = 64, cu_seqlens
     elif final_state:
         fs = torch.empty((nseq, prob.nheads, prob.headdim, prob.dstate), dtype=torch.float32,
                          device=dev)
+    if initial_state is not None:
+        _check_tensor(initial_state, "initial_state", torch.float32, dev)
+        if tuple(initial_state.shape) != (nseq, prob.nheads, prob.headdim, prob.dstate):
+            raise ValueError("initial_state must be [nseq, H, P, N]")
     ws = _workspace(workspace_size(prob, False), dev, workspace)
     with torch.cuda.device(dev):
-        st = _lib.lib().ssd_forward(ctypes.byref(prob), _ptr(x), _ptr(raw_dt), _ptr(B), _ptr(C),
-                                    _ptr(cu_seqlens), _ptr(y), _ptr(fs), _ptr(ws),
-                                    ws.numel(), _stream(stream))
-    check(st, "ssd_forward")
+        st = _lib.lib().ssd_forward_state(ctypes.byref(prob), _ptr(x), _ptr(raw_dt), _ptr(B),
+                                          _ptr(C), _ptr(cu_seqlens), _ptr(initial_state),
+                                          _ptr(y), _ptr(fs), _ptr(ws), ws.numel(),
+                                          _stream(stream))
+    check(st, "ssd_forward_state")
     return y, fs
 
 
 def backward(x, raw_dt, B, C, dy, delta_init: float, chunk_size: int = 64, cu_seqlens=None,
-             out=None, workspace=None, stream=None, after_forward: bool = False):
-    """Runs ssd_backward, or ssd_backward_after_forward when ``after_forward`` is set
-    (``workspace`` must then be the one the preceding forward on these inputs used).
-    Returns a dict ``dx, d_raw_dt, dB, dC``."""
+             out=None, workspace=None, stream=None, after_forward: bool = False,
+             initial_state=None, d_final_state=None, d_initial_state: bool = False):
+    """Runs ssd_backward_state (ssd_backward with no initial state and a zero final-state
+    gradient).  ``after_forward``: the workspace holds the preceding forward on these
+    inputs.  ``initial_state`` / ``d_final_state``: float32 ``[nseq, H, P, N]`` CUDA tensors
+    or None.  Returns a dict ``dx, d_raw_dt, dB, dC`` and, with ``d_initial_state``,
+    ``d_initial_state``."""
     torch = _torch()
     dev = x.device
     _check_tensor(x, "x")
@@ -153,14 +162,24 @@ def backward(x, raw_dt, B, C, dy, delta_init: float, chunk_size: int = 64, cu_se
                "dB": torch.empty_like(B), "dC": torch.empty_like(C)}
     if after_forward and workspace is None:
         raise ValueError("after_forward needs the forward's workspace")
+    nseq = prob.nseq if prob.nseq > 0 else prob.batch
+    shape = (nseq, prob.nheads, prob.headdim, prob.dstate)
+    for t, name in ((initial_state, "initial_state"), (d_final_state, "d_final_state")):
+        if t is not None:
+            _check_tensor(t, name, torch.float32, dev)
+            if tuple(t.shape) != shape:
+                raise ValueError("%s must be [nseq, H, P, N]" % name)
+    if d_initial_state and "d_initial_state" not in out:
+        out["d_initial_state"] = torch.empty(shape, dtype=torch.float32, device=dev)
     ws = _workspace(workspace_size(prob, True), dev, workspace)
-    name = "ssd_backward_after_forward" if after_forward else "ssd_backward"
     with torch.cuda.device(dev):
-        st = getattr(_lib.lib(), name)(ctypes.byref(prob), _ptr(x), _ptr(raw_dt), _ptr(B),
-                                       _ptr(C), _ptr(cu_seqlens), _ptr(dy), _ptr(out["dx"]),
-                                       _ptr(out["d_raw_dt"]), _ptr(out["dB"]), _ptr(out["dC"]),
-                                       _ptr(ws), ws.numel(), _stream(stream))
-    check(st, name)
+        st = _lib.lib().ssd_backward_state(
+            ctypes.byref(prob), _ptr(x), _ptr(raw_dt), _ptr(B), _ptr(C), _ptr(cu_seqlens),
+            _ptr(initial_state), _ptr(dy), _ptr(d_final_state), _ptr(out["dx"]),
+            _ptr(out["d_raw_dt"]), _ptr(out["dB"]), _ptr(out["dC"]),
+            _ptr(out.get("d_initial_state") if d_initial_state else None), int(after_forward),
+            _ptr(ws), ws.numel(), _stream(stream))
+    check(st, "ssd_backward_state")
     return out
 
 

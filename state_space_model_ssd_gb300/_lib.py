@@ -54,6 +54,10 @@ _SIGS = {
                                     _VP, _SZ, _VP]),
     "ssd_backward_after_forward": (ctypes.c_int, [_PP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP,
                                                   _VP, _VP, _VP, _SZ, _VP]),
+    "ssd_forward_state": (ctypes.c_int, [_PP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _SZ,
+                                         _VP]),
+    "ssd_backward_state": (ctypes.c_int, [_PP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP,
+                                          _VP, _VP, _VP, ctypes.c_int, _VP, _SZ, _VP]),
     "ssd_forward_noalloc": (ctypes.c_int, [_PP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP]),
     "ssd_forward_noalloc_status": (ctypes.c_int, [_VP, ctypes.POINTER(ctypes.c_int32)]),
     "ssd_step_host_size": (ctypes.c_int, [_PP, ctypes.POINTER(_SZ)]),

@@ -240,7 +240,7 @@ __device__ void adj_state_body(const Args& a, int seg, int h, float* sm, const C
 // finish = false leaves x.(G B) - sum_{u >= t in the segment} (r_u - q_u) in d_raw and
 // the segment's sum of (r - q) in rq (ssd_scan.cu completes them); finish = true writes
 // the finished d_raw_dt from the fp32 boundary term <G_seg, H_end> read from the scans'
-// states.
+// states.  Either way a sequence's last segment includes <d final_state, final state>.
 template <typename TI, int RP, int CP>
 __device__ void bwd_walk_body(const Args& a, int seg, int h, float* sm, const Ctx& cx,
                               bool finish) {
@@ -333,7 +333,11 @@ __device__ void bwd_walk_body(const Args& a, int seg, int h, float* sm, const Ct
     {
         const float* Gin = a.adj + ((long long)seg * a.H + h) * P * N;
         const float* Hend = a.A + ((long long)(seg + 1) * a.H + h) * P * N;
-        const bool more = finish && !(si.flags & SEG_LAST);
+        const bool last = (si.flags & SEG_LAST) != 0;
+        const bool more = finish && !last;
+        // a sequence's last segment with an upstream final-state gradient: the pairs beyond
+        // its end are <d final_state, final state>, and S holds the final state now
+        const bool tail = last && a.dhT != nullptr;
         float kp = 0.f;
 #pragma unroll
         for (int r = 0; r < RP; ++r)
@@ -342,8 +346,9 @@ __device__ void bwd_walk_body(const Args& a, int seg, int h, float* sm, const Ct
                 const int n = lane + 32 * c;
                 Gs[r][c] = (n < N) ? Gin[st_idx(a, warp + 8 * r, n)] : 0.f;
                 if (more && n < N) kp = fmaf(Gs[r][c], Hend[st_idx(a, warp + 8 * r, n)], kp);
+                if (tail && n < N) kp = fmaf(Gs[r][c], S[r][c], kp);
             }
-        if (finish) {
+        if (finish || tail) {
             kp = warp_sum(kp);
             if (lane == 0) wred[warp] = kp;
             cx.sync();
@@ -415,7 +420,7 @@ __device__ void bwd_walk_body(const Args& a, int seg, int h, float* sm, const Ct
                     if (finish)
                         a.draw[o] = (v - racc - kseg) * sigmoid_f(a.raw[o] + a.delta_init);
                     else
-                        a.draw[o] = v - racc;
+                        a.draw[o] = v - racc - kseg;
                 }
             }
 #pragma unroll
@@ -425,7 +430,9 @@ __device__ void bwd_walk_body(const Args& a, int seg, int h, float* sm, const Ct
         }
         cx.sync();
     }
-    if (!finish && cx.tid == 0) a.rq[(long long)seg * a.H + h] = racc;
+    // the sum of (r - q) over the segment, and a last segment's final-state term, for the
+    // earlier segments of the sequence
+    if (!finish && cx.tid == 0) a.rq[(long long)seg * a.H + h] = racc + kseg;
 }
 
 }  // namespace simt

@@ -154,8 +154,10 @@ Layout make_layout(const Prob& b, bool bwd) {
         l.fb = off;
         off = align_up(off + sizeof(int) * b.nseg_max * (b.H / 2));
     }
-    l.adj = l.rq = l.rqsuf = l.dbacc = l.dcacc = l.rtok = l.cb32 = 0;
+    l.adj = l.rq = l.rqsuf = l.dbacc = l.dcacc = l.rtok = l.kfin = l.cb32 = 0;
     if (bwd) {
+        l.kfin = off;
+        off = align_up(off + sizeof(float) * (size_t)b.nseg_max * b.H);
         l.adj = off;
         off = align_up(off + sizeof(float) * (size_t)b.nseg_max * b.H * PN);
         l.rq = off;
@@ -194,6 +196,7 @@ Args make_args(const Prob& b, const Layout& l, void* ws) {
         a.dbacc = reinterpret_cast<float*>(base + l.dbacc);
         a.dcacc = reinterpret_cast<float*>(base + l.dcacc);
         a.rtok = reinterpret_cast<float*>(base + l.rtok);
+        a.kfin = reinterpret_cast<float*>(base + l.kfin);
     }
     if (l.l0) a.l0 = reinterpret_cast<unsigned char*>(base + l.l0);
     if (l.fac) a.fac = reinterpret_cast<float*>(base + l.fac);
@@ -293,21 +296,26 @@ const char* ssd_dispatch_path(const ssd_problem_t* prob, int for_backward) {
 
 int ssd_last_launch_count(void) { return g_last_launches; }
 
-ssd_status_t ssd_forward(const ssd_problem_t* prob, const void* x, const float* raw_dt,
-                         const void* B, const void* C, const int32_t* cu_seqlens, void* y,
-                         float* final_state, void* workspace, size_t workspace_bytes,
-                         void* stream) {
+ssd_status_t ssd_forward_state(const ssd_problem_t* prob, const void* x, const float* raw_dt,
+                               const void* B, const void* C, const int32_t* cu_seqlens,
+                               const float* initial_state, void* y, float* final_state,
+                               void* workspace, size_t workspace_bytes, void* stream) {
     g_last_launches = 0;
     Prob b;
     Layout l;
     ssd_status_t st = check_common(prob, cu_seqlens, workspace, workspace_bytes, false, &b, &l);
     if (st != SSD_OK) return st;
+    if (initial_state && !aligned16(initial_state)) return SSD_ERR_ALIGNMENT;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (b.T == 0) {  // nothing to read: only the (zero) final states are written
-        if (final_state &&
-            cudaMemsetAsync(final_state, 0, sizeof(float) * (size_t)b.nseq * b.H * b.P * b.N,
-                            s) != cudaSuccess)
-            return SSD_ERR_CUDA;
+    const size_t sbytes = sizeof(float) * (size_t)b.nseq * b.H * b.P * b.N;
+    if (b.T == 0) {  // nothing to read: the final states are the initial ones (or zero)
+        if (final_state) {
+            const cudaError_t e =
+                initial_state ? cudaMemcpyAsync(final_state, initial_state, sbytes,
+                                                cudaMemcpyDeviceToDevice, s)
+                              : cudaMemsetAsync(final_state, 0, sbytes, s);
+            if (e != cudaSuccess) return SSD_ERR_CUDA;
+        }
         return SSD_OK;
     }
     if (!x || !raw_dt || !B || !C || !y) return SSD_ERR_INVALID_ARG;
@@ -322,7 +330,8 @@ ssd_status_t ssd_forward(const ssd_problem_t* prob, const void* x, const float* 
     a.cu = cu_seqlens;
     a.y = y;
     a.final_state = final_state;
-    // the segment-table kernel resets the header and zeroes the final states that no
+    a.h0 = initial_state;
+    // the segment-table kernel resets the header and writes the final states that no
     // segment writes
     Launch L;
     L.stream = s;
@@ -331,39 +340,60 @@ ssd_status_t ssd_forward(const ssd_problem_t* prob, const void* x, const float* 
     return e == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
 }
 
+ssd_status_t ssd_forward(const ssd_problem_t* prob, const void* x, const float* raw_dt,
+                         const void* B, const void* C, const int32_t* cu_seqlens, void* y,
+                         float* final_state, void* workspace, size_t workspace_bytes,
+                         void* stream) {
+    return ssd_forward_state(prob, x, raw_dt, B, C, cu_seqlens, nullptr, y, final_state,
+                             workspace, workspace_bytes, stream);
+}
+
 }  // extern "C"
 
 namespace {
 
 ssd_status_t backward_impl(const ssd_problem_t* prob, const void* x, const float* raw_dt,
                            const void* B, const void* C, const int32_t* cu_seqlens,
-                           const void* dy, void* dx, float* d_raw_dt, void* dB, void* dC,
-                           void* workspace, size_t workspace_bytes, void* stream,
-                           bool after_forward) {
+                           const float* h0, const void* dy, const float* dhT, void* dx,
+                           float* d_raw_dt, void* dB, void* dC, float* dh0, void* workspace,
+                           size_t workspace_bytes, void* stream, bool after_forward) {
     g_last_launches = 0;
     Prob b;
     Layout l;
     ssd_status_t st = check_common(prob, cu_seqlens, workspace, workspace_bytes, true, &b, &l);
     if (st != SSD_OK) return st;
-    if (b.T == 0) return SSD_OK;  // no tokens: every gradient is empty
+    if ((h0 && !aligned16(h0)) || (dhT && !aligned16(dhT)) || (dh0 && !aligned16(dh0)))
+        return SSD_ERR_ALIGNMENT;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (b.T == 0) {  // no tokens: the initial state's gradient is the final state's
+        if (dh0) {
+            const size_t sbytes = sizeof(float) * (size_t)b.nseq * b.H * b.P * b.N;
+            const cudaError_t e = dhT ? cudaMemcpyAsync(dh0, dhT, sbytes, cudaMemcpyDeviceToDevice, s)
+                                      : cudaMemsetAsync(dh0, 0, sbytes, s);
+            if (e != cudaSuccess) return SSD_ERR_CUDA;
+        }
+        return SSD_OK;
+    }
     if (!x || !raw_dt || !B || !C || !dy || !dx || !d_raw_dt || !dB || !dC)
         return SSD_ERR_INVALID_ARG;
     if (!aligned16(x) || !aligned16(raw_dt) || !aligned16(B) || !aligned16(C) ||
         !aligned16(dy) || !aligned16(dx) || !aligned16(d_raw_dt) || !aligned16(dB) ||
         !aligned16(dC))
         return SSD_ERR_ALIGNMENT;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
     Args a = make_args(b, l, workspace);
     a.x = x;
     a.raw = raw_dt;
     a.B = B;
     a.C = C;
     a.cu = cu_seqlens;
+    a.h0 = h0;
     a.dy = dy;
+    a.dhT = dhT;
     a.dx = dx;
     a.draw = d_raw_dt;
     a.dB = dB;
     a.dC = dC;
+    a.dh0 = dh0;
     // the tensor-core path can take the forward's segment table, tiles, factors and
     // segment states from the workspace (its header is then kept, status included)
     // (the segment-table kernel resets the header; the tensor-core path's adjoint
@@ -376,6 +406,7 @@ ssd_status_t backward_impl(const ssd_problem_t* prob, const void* x, const float
     Launch L;
     L.stream = s;
     cudaError_t e = b.tc ? tc_backward(b, a, L, reuse) : simt_backward(b, a, L);
+    if (e == cudaSuccess && dh0 && b.varlen) e = launch_empty_seq_grads(b, a, L);
     g_last_launches = L.count;
     return e == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
 }
@@ -388,8 +419,8 @@ ssd_status_t ssd_backward(const ssd_problem_t* prob, const void* x, const float*
                           const void* B, const void* C, const int32_t* cu_seqlens,
                           const void* dy, void* dx, float* d_raw_dt, void* dB, void* dC,
                           void* workspace, size_t workspace_bytes, void* stream) {
-    return backward_impl(prob, x, raw_dt, B, C, cu_seqlens, dy, dx, d_raw_dt, dB, dC, workspace,
-                         workspace_bytes, stream, false);
+    return backward_impl(prob, x, raw_dt, B, C, cu_seqlens, nullptr, dy, nullptr, dx, d_raw_dt,
+                         dB, dC, nullptr, workspace, workspace_bytes, stream, false);
 }
 
 ssd_status_t ssd_backward_after_forward(const ssd_problem_t* prob, const void* x,
@@ -397,8 +428,19 @@ ssd_status_t ssd_backward_after_forward(const ssd_problem_t* prob, const void* x
                                         const int32_t* cu_seqlens, const void* dy, void* dx,
                                         float* d_raw_dt, void* dB, void* dC, void* workspace,
                                         size_t workspace_bytes, void* stream) {
-    return backward_impl(prob, x, raw_dt, B, C, cu_seqlens, dy, dx, d_raw_dt, dB, dC, workspace,
-                         workspace_bytes, stream, true);
+    return backward_impl(prob, x, raw_dt, B, C, cu_seqlens, nullptr, dy, nullptr, dx, d_raw_dt,
+                         dB, dC, nullptr, workspace, workspace_bytes, stream, true);
+}
+
+ssd_status_t ssd_backward_state(const ssd_problem_t* prob, const void* x, const float* raw_dt,
+                                const void* B, const void* C, const int32_t* cu_seqlens,
+                                const float* initial_state, const void* dy,
+                                const float* d_final_state, void* dx, float* d_raw_dt, void* dB,
+                                void* dC, float* d_initial_state, int after_forward,
+                                void* workspace, size_t workspace_bytes, void* stream) {
+    return backward_impl(prob, x, raw_dt, B, C, cu_seqlens, initial_state, dy, d_final_state, dx,
+                         d_raw_dt, dB, dC, d_initial_state, workspace, workspace_bytes, stream,
+                         after_forward != 0);
 }
 
 ssd_status_t ssd_device_status(const void* workspace, void* stream, int32_t* device_status) {

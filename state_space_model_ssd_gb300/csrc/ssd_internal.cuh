@@ -32,8 +32,8 @@ struct WsHeader {
     int sig_valid;
     int sig_dims[7];            // H, P, N, G, Ls, dtype, delta_init (bits)
     long long sig_T;
-    const void* sig_ptr[5];     // x, raw_dt, B, C, cu_seqlens
-    int pad[42];
+    const void* sig_ptr[6];     // x, raw_dt, B, C, cu_seqlens, initial_state
+    int pad[40];
 };
 static_assert(sizeof(WsHeader) == 256, "WsHeader layout");
 
@@ -53,7 +53,7 @@ struct Prob {
 
 // Byte offsets of the workspace regions.
 struct Layout {
-    size_t header, segtab, A, lam, adj, rq, rqsuf, dbacc, dcacc, rtok, l0, fac, fb, cb32, total;
+    size_t header, segtab, A, lam, adj, rq, rqsuf, dbacc, dcacc, rtok, kfin, l0, fac, fb, cb32, total;
 };
 
 // Everything a kernel needs; passed by value.
@@ -66,6 +66,9 @@ struct Args {
     const void* dy;
     void* y;
     float* final_state;
+    const float* h0;   // [nseq][H][P][N] initial states (row-major), NULL: zero
+    const float* dhT;  // [nseq][H][P][N] upstream gradient of final_state, NULL: zero
+    float* dh0;        // [nseq][H][P][N] gradient of the initial states, NULL: not wanted
     void* dx;
     float* draw;
     void* dB;
@@ -79,6 +82,7 @@ struct Args {
     float* rqsuf;   // [nseg_max][H]
     float* dbacc;   // [T][G][N] fp32
     float* dcacc;   // [T][G][N] fp32
+    float* kfin;    // [nseg_max][H]: <d final_state, final state> of a sequence's last segment
     float* rtok;    // [T][H] fp32 (tensor-core backward): the part of dy_t . y_t that comes from
                     // tokens before t's chunk
     unsigned char* l0;  // tensor-core path: [nseg_max][Ls / Q][G] 8 KB tiles, masked C B^T per chunk
@@ -139,6 +143,8 @@ cudaError_t launch_seg_table(const Prob& pb, const Args& a, Launch& L);
 // Checks that the workspace's segment table was built for this problem and these inputs;
 // otherwise records SSD_ERR_WORKSPACE and empties the table, so that no kernel does work.
 cudaError_t launch_forward_match(const Prob& pb, const Args& a, Launch& L);
+// d_initial_state of the empty packed sequences: their d_final_state (or zero).
+cudaError_t launch_empty_seq_grads(const Prob& pb, const Args& a, Launch& L);
 cudaError_t launch_state_scan(const Prob& pb, const Args& a, Launch& L, bool write_final);
 cudaError_t launch_adjoint_scan(const Prob& pb, const Args& a, Launch& L);
 cudaError_t launch_bwd_epilogue(const Prob& pb, const Args& a, Launch& L);

@@ -59,12 +59,13 @@ __global__ void __launch_bounds__(kTableThreads) seg_table_kernel(Args a) {
         for (int s = tid; s < a.nseq; s += blockDim.x)
             if (a.cu[s + 1] < a.cu[s]) bad = 1;
     __syncthreads();
-    // final states that no segment writes: every row when the boundaries are malformed,
-    // else the rows of empty packed sequences
+    // final states that no segment writes: every row (zero) when the boundaries are
+    // malformed, else the rows of empty packed sequences (their initial states, or zero)
     const long long row4 = (long long)a.H * a.P * a.N / 4;
     if (a.final_state && (bad || a.cu)) {
         float4* fs4 = reinterpret_cast<float4*>(a.final_state);
-        // one sequence per thread and pass; the block zeroes the rows of the empty ones
+        const float4* h04 = reinterpret_cast<const float4*>(a.h0);
+        // one sequence per thread and pass; the block writes the rows of the empty ones
         for (int s0 = 0; s0 < a.nseq; s0 += blockDim.x) {
             const int s = s0 + tid;
             const bool empty = s < a.nseq && (bad || a.cu[s + 1] == a.cu[s]);
@@ -73,7 +74,9 @@ __global__ void __launch_bounds__(kTableThreads) seg_table_kernel(Args a) {
                 const int sk = s0 + k;
                 if (bad || a.cu[sk + 1] == a.cu[sk])
                     for (long long i = tid; i < row4; i += blockDim.x)
-                        fs4[(long long)sk * row4 + i] = make_float4(0.f, 0.f, 0.f, 0.f);
+                        fs4[(long long)sk * row4 + i] = (h04 && !bad)
+                                                            ? h04[(long long)sk * row4 + i]
+                                                            : make_float4(0.f, 0.f, 0.f, 0.f);
             }
         }
     }
@@ -156,6 +159,7 @@ __global__ void __launch_bounds__(kTableThreads) seg_table_kernel(Args a) {
         h->sig_ptr[2] = a.B;
         h->sig_ptr[3] = a.C;
         h->sig_ptr[4] = a.cu;
+        h->sig_ptr[5] = a.h0;
         h->sig_valid = 1;
     }
 }
@@ -169,7 +173,7 @@ __global__ void forward_match_kernel(Args a) {
                     h->sig_dims[4] == a.Ls && h->sig_dims[5] == a.dtype &&
                     h->sig_dims[6] == __float_as_int(a.delta_init) && h->sig_ptr[0] == a.x &&
                     h->sig_ptr[1] == a.raw && h->sig_ptr[2] == a.B && h->sig_ptr[3] == a.C &&
-                    h->sig_ptr[4] == a.cu;
+                    h->sig_ptr[4] == a.cu && h->sig_ptr[5] == a.h0;
     if (!ok) {
         set_status(h, SSD_ERR_WORKSPACE);
         h->nseg = 0;
@@ -220,7 +224,9 @@ __global__ void __launch_bounds__(kScanThreads) state_scan_kernel(Args a, int wr
         for (int u = 0; u < kScanUnroll; ++u) {
             const int s = s0 + u;
             if (s >= nseg) break;
-            if (flags[u] & SEG_FIRST) carry = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (flags[u] & SEG_FIRST)
+                carry = a.h0 ? reinterpret_cast<const float4*>(a.h0)[((long long)seq[u] * a.H + h) * PN4 + fe4]
+                             : make_float4(0.f, 0.f, 0.f, 0.f);
             A4[((long long)s * a.H + h) * PN4 + e4] = carry;
             carry.x = fmaf(dec[u], carry.x, agg[u].x);
             carry.y = fmaf(dec[u], carry.y, agg[u].y);
@@ -250,11 +256,17 @@ __global__ void __launch_bounds__(kScanThreads) adjoint_scan_kernel(Args a) {
     if (e4 >= PN4) return;
     const int nseg = a.hdr->nseg;
     float4* G4 = reinterpret_cast<float4*>(a.adj);
+    // row-major float4 index of this thread's four elements (d_final_state, d_initial_state)
+    int fe4 = e4;
+    if (a.state_lm) {
+        const int N4 = a.N >> 2, blk = e4 / (32 * N4), j = e4 - blk * 32 * N4;
+        fe4 = (blk * 32 + (j & 31)) * N4 + (j >> 5);
+    }
     float4 carry = make_float4(0.f, 0.f, 0.f, 0.f);
     float4 agg[kScanUnroll], nagg[kScanUnroll];
     float dec[kScanUnroll], ndec[kScanUnroll];
-    int flags[kScanUnroll], nflags[kScanUnroll];
-    auto load = [&](int s0, float4* g, float* dc, int* fl) {
+    int flags[kScanUnroll], nflags[kScanUnroll], seq[kScanUnroll], nseqi[kScanUnroll];
+    auto load = [&](int s0, float4* g, float* dc, int* fl, int* sq) {
 #pragma unroll
         for (int u = 0; u < kScanUnroll; ++u) {
             const int s = s0 - u;
@@ -262,30 +274,50 @@ __global__ void __launch_bounds__(kScanThreads) adjoint_scan_kernel(Args a) {
                 g[u] = G4[((long long)s * a.H + h) * PN4 + e4];
                 dc[u] = expf(a.lam[(long long)s * a.H + h]);
                 fl[u] = a.segtab[s].flags;
+                sq[u] = a.segtab[s].seq;
             }
         }
     };
-    load(nseg - 1, agg, dec, flags);
+    load(nseg - 1, agg, dec, flags, seq);
     for (int s0 = nseg - 1; s0 >= 0; s0 -= kScanUnroll) {
-        if (s0 - kScanUnroll >= 0) load(s0 - kScanUnroll, nagg, ndec, nflags);
+        if (s0 - kScanUnroll >= 0) load(s0 - kScanUnroll, nagg, ndec, nflags, nseqi);
 #pragma unroll
         for (int u = 0; u < kScanUnroll; ++u) {
             const int s = s0 - u;
             if (s < 0) break;
-            if (flags[u] & SEG_LAST) carry = make_float4(0.f, 0.f, 0.f, 0.f);
+            const long long srow = ((long long)seq[u] * a.H + h) * PN4 + fe4;
+            // the adjoint arriving at a sequence's last token: the gradient of its final state
+            if (flags[u] & SEG_LAST)
+                carry = a.dhT ? reinterpret_cast<const float4*>(a.dhT)[srow]
+                              : make_float4(0.f, 0.f, 0.f, 0.f);
             G4[((long long)s * a.H + h) * PN4 + e4] = carry;
             carry.x = fmaf(dec[u], carry.x, agg[u].x);
             carry.y = fmaf(dec[u], carry.y, agg[u].y);
             carry.z = fmaf(dec[u], carry.z, agg[u].z);
             carry.w = fmaf(dec[u], carry.w, agg[u].w);
+            // before a sequence's first token: the gradient of its initial state
+            if (a.dh0 && (flags[u] & SEG_FIRST)) reinterpret_cast<float4*>(a.dh0)[srow] = carry;
         }
 #pragma unroll
         for (int u = 0; u < kScanUnroll; ++u) {
             agg[u] = nagg[u];
             dec[u] = ndec[u];
             flags[u] = nflags[u];
+            seq[u] = nseqi[u];
         }
     }
+}
+
+// d_initial_state of the empty packed sequences, which have no segment: their
+// d_final_state (H = initial state at their end), or zero.
+__global__ void empty_seq_grads_kernel(Args a) {
+    const int s = blockIdx.x;
+    if (a.cu[s + 1] != a.cu[s]) return;
+    const long long row4 = (long long)a.H * a.P * a.N / 4;
+    float4* d4 = reinterpret_cast<float4*>(a.dh0) + (long long)s * row4;
+    const float4* t4 = reinterpret_cast<const float4*>(a.dhT) + (long long)s * row4;
+    for (long long i = threadIdx.x; i < row4; i += blockDim.x)
+        d4[i] = a.dhT ? t4[i] : make_float4(0.f, 0.f, 0.f, 0.f);
 }
 
 // Sum of (r - q) over the later segments of the same sequence, per head.
@@ -347,6 +379,12 @@ cudaError_t launch_forward_match(const Prob& pb, const Args& a, Launch& L) {
     (void)pb;
     L.begin("forward_match");
     forward_match_kernel<<<1, 1, 0, L.stream>>>(a);
+    return L.end();
+}
+
+cudaError_t launch_empty_seq_grads(const Prob& pb, const Args& a, Launch& L) {
+    L.begin("empty_seq_grads");
+    empty_seq_grads_kernel<<<(unsigned)pb.nseq, 256, 0, L.stream>>>(a);
     return L.end();
 }
 

@@ -1132,6 +1132,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const SegInfo si = a.segtab[seg];
     const int g = h0 / (a.H / a.G);
     const int nchunks = (si.len + kQ - 1) / kQ;
+    // a sequence's last segment under an upstream final-state gradient: this walk also
+    // forms the final state and writes <d final_state, final state> per head (kfin)
+    const bool tail = (si.flags & SEG_LAST) && a.dhT != nullptr;
 
     extern __shared__ __align__(1024) unsigned char smraw[];
     unsigned char* sm = reinterpret_cast<unsigned char*>(
@@ -1252,7 +1255,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 tc_fence_after();
                 const uint32_t xs = smem_u32(sm + Lay::OFF_STAGE + s * Lay::STAGE);
                 const uint32_t ys = xs + 16384, bs = xs + 32768;
-                if (c < nchunks - 1) {  // chunk state, needed only for later chunks
+                // chunk state, needed for later chunks and, with an upstream final-state
+                // gradient, for the final state of a sequence's last segment
+                if (c < nchunks - 1 || tail) {
 #pragma unroll
                     for (int k = 0; k < 4; ++k)
                         mma_bf16(tmem + T_S, mdesc(xs, k, 8192), mdesc(bs, k, 8192), id_s,
@@ -1388,6 +1393,39 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 write_state<NH>(sm + Lay::OFF_S + (s ^ 1) * Lay::SBUF, Hs, r, n0);
                 fence_proxy_async();
                 mbar_arrive(&h_ready[s ^ 1]);
+            } else if (tail) {
+                // final state = exp(-half_c) (Hs_c + S_c) (the chain's update with no next
+                // chunk), dotted with the upstream gradient of the final state
+                const bool ok = wait_or_abort(s_full, pc, abort_flag, a.hdr);
+                tc_fence_after();
+                const float gend = expf(-F.scal[(s * 2 + rh) * 4]);
+                const float* dT =
+                    a.dhT + (((long long)si.seq * a.H + h0 + rh) * kP + rp) * N + n0;
+                float kp = 0.f;
+#pragma unroll
+                for (int c0 = 0; c0 < NH; c0 += 32) {
+                    uint32_t v[32];
+                    tmem_ld16(tq + T_S + n0 + c0, *reinterpret_cast<uint32_t(*)[16]>(&v[0]));
+                    tmem_ld16(tq + T_S + n0 + c0 + 16, *reinterpret_cast<uint32_t(*)[16]>(&v[16]));
+                    tmem_wait_ld_regs<32>(v);
+#pragma unroll
+                    for (int u = 0; u < 32; u += 4) {
+                        const float4 d4 = *reinterpret_cast<const float4*>(dT + c0 + u);
+                        kp = fmaf(gend * (Hs[c0 + u] + __uint_as_float(v[u])), d4.x, kp);
+                        kp = fmaf(gend * (Hs[c0 + u + 1] + __uint_as_float(v[u + 1])), d4.y, kp);
+                        kp = fmaf(gend * (Hs[c0 + u + 2] + __uint_as_float(v[u + 2])), d4.z, kp);
+                        kp = fmaf(gend * (Hs[c0 + u + 3] + __uint_as_float(v[u + 3])), d4.w, kp);
+                    }
+                }
+                tc_fence_before();
+                mbar_arrive(s_free);
+                kp = warp_sum(kp);
+                if (lane == 0) F.red[wg * 4 + q] = ok ? kp : 0.f;
+                named_sync(1, kCT);
+                // quadrants 0-1 hold head 0, 2-3 head 1; both warpgroups hold column halves
+                if (ct < 2)
+                    a.kfin[(long long)seg * a.H + h0 + ct] =
+                        (F.red[2 * ct] + F.red[2 * ct + 1]) + (F.red[4 + 2 * ct] + F.red[5 + 2 * ct]);
             } else {
                 mbar_arrive(s_free);
             }
@@ -1755,8 +1793,11 @@ __global__ void __launch_bounds__(kDxThreads, 1)
             const float* rtok = a.rtok;
             float carry = 0.f;  // sum of (r - q) over the later chunks of the segment, head hf
             wait_or_abort(kseg_ready, 0, abort_flag, a.hdr);
-            const float kseg = (red[8 + 2 * hf] + red[9 + 2 * hf]) +
-                               (red[12 + 2 * hf] + red[13 + 2 * hf]);
+            // a sequence's last segment: <d final_state, final state>, from the dC walk
+            const float kseg = ((si.flags & SEG_LAST) && a.dhT)
+                                   ? a.kfin[(long long)seg * a.H + h0 + hf]
+                                   : (red[8 + 2 * hf] + red[9 + 2 * hf]) +
+                                         (red[12 + 2 * hf] + red[13 + 2 * hf]);
             for (int it = 0; it < nchunks; ++it) {
                 const int c = nchunks - 1 - it;
                 const int s = it & 1, sl = it % kDFS;

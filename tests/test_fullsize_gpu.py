@@ -107,3 +107,47 @@ def test_genomics_2m(ssd, oracle_mod):
     for k in num:
         e = num[k] / den[k]
         assert e <= TOL[w.dtype], "%s rel err %g (all heads)" % (k, e)
+
+
+def _check_all_states(ssd, oracle_mod, name):
+    """The workload with an initial state per sequence and an upstream final-state
+    gradient: every output and gradient, d_initial_state included, over whole tensors."""
+    import torch
+    from state_space_model_ssd_gb300.inputs import WORKLOADS, make_inputs
+    w = WORKLOADS[name]
+    d = make_inputs(w, seed=0)
+    nseq = w.batch if d["cu_seqlens"] is None else len(d["cu_seqlens"]) - 1
+    rng = np.random.default_rng(1)
+    shape = (nseq, w.nheads, w.headdim, w.dstate)
+    h0 = rng.standard_normal(shape, dtype=np.float32) * np.float32(0.5)
+    dhT = rng.standard_normal(shape, dtype=np.float32)
+    t = to_device(d, w.dtype)
+    th0, tdhT = torch.from_numpy(h0).cuda(), torch.from_numpy(dhT).cuda()
+    y, fs = ssd.forward(t["x"], t["raw_dt"], t["B"], t["C"], delta_init=w.delta_init,
+                        cu_seqlens=t["cu_seqlens"], initial_state=th0)
+    g = ssd.backward(t["x"], t["raw_dt"], t["B"], t["C"], t["dy"], delta_init=w.delta_init,
+                     cu_seqlens=t["cu_seqlens"], initial_state=th0, d_final_state=tdhT,
+                     d_initial_state=True)
+    out = {"y": to_np(y), "final_state": to_np(fs)}
+    out.update({k: to_np(v) for k, v in g.items()})
+    del t, y, fs, g
+    torch.cuda.empty_cache()
+    yr, fr = oracle_mod.forward(d["x"], d["raw_dt"], d["B"], d["C"], w.delta_init,
+                                cu_seqlens=d["cu_seqlens"], initial_state=h0)
+    _check(out["y"], yr, "y", TOL[w.dtype])
+    _check(out["final_state"], fr, "final_state", TOL[w.dtype])
+    del yr, fr
+    r = oracle_mod.backward(d["x"], d["raw_dt"], d["B"], d["C"], d["dy"], w.delta_init,
+                            cu_seqlens=d["cu_seqlens"], initial_state=h0, d_final_state=dhT)
+    for k in ("dx", "d_raw_dt", "dB", "dC", "d_initial_state"):
+        _check(out[k], r[k], k, TOL[w.dtype])
+
+
+def test_mamba28b_layer_32k_with_states(ssd, oracle_mod):
+    """mamba-2.8b layer at L=32768 with initial state and final-state gradient."""
+    _check_all_states(ssd, oracle_mod, "mamba2.8b_32k")
+
+
+def test_varlen_packed_64k_with_states(ssd, oracle_mod):
+    """65536 packed tokens, 24 heads, with initial states and final-state gradients."""
+    _check_all_states(ssd, oracle_mod, "varlen_64k")
