@@ -405,6 +405,39 @@ def long_seq_record(args, ssd, torch, dev, stream, barrier, peaks, peak_kind, cl
     return rec
 
 
+def decode_record(ssd, torch, dev, stream, barrier, peaks, peak_kind, batch=128, steps=50):
+    """Single-token decode (ssd_decode_step) for `batch` sequences of the mamba-2.8b layer
+    (80 heads x P = 64, N = 128, bf16 x/B/C/y, fp32 state), state updated in place: bytes
+    per step against the measured HBM bandwidth.  The state (batch x 80 x 32 KB) is larger
+    than L2, so every step reads it from HBM."""
+    w = WORKLOADS[DEFAULT_WORKLOAD]
+    H, P, N, G = w.nheads, w.headdim, w.dstate, w.ngroups
+    g = torch.Generator(device=dev).manual_seed(0)
+    state = torch.randn(batch, H, P, N, device=dev, generator=g) * 0.5
+    x = torch.randn(batch, H, P, device=dev, generator=g).to(torch.bfloat16)
+    raw = torch.randn(batch, H, device=dev, generator=g) * 0.5
+    B = (torch.randn(batch, G, N, device=dev, generator=g) / N ** 0.5).to(torch.bfloat16)
+    C = (torch.randn(batch, G, N, device=dev, generator=g) / N ** 0.5).to(torch.bfloat16)
+    y = torch.empty_like(x)
+
+    def run():
+        ssd.decode_step(state, x, raw, B, C, w.delta_init, out=y)
+        return 1
+
+    ms, launches, _, _, _ = timed_loop(ssd, torch, stream, run, steps, 3, barrier, profile=False)
+    nbytes = (2 * state.numel() * 4 + 2 * x.numel() * 2 + raw.numel() * 4
+              + 2 * B.numel() * 2)
+    ach = nbytes / (ms * 1e-3) / 1e9
+    return {"workload": "mamba2.8b layer decode: %d sequences x 80 heads x P=64, N=128, fp32 "
+                        "state in place, bf16 x/B/C/y" % batch,
+            "value": batch / (ms * 1e-3), "unit": "tokens/s", "ms_per_step": ms,
+            "steps": steps, "gpu_launches": launches,
+            "roofline": {"kernel": "decode_step", "bound": "hbm", "achieved": ach,
+                         "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": ach / peaks["hbm_gbs"], "algorithmic_bytes": nbytes,
+                         "peak_source": "%s hbm_gbs (copy)" % peak_kind}}
+
+
 def gpu_arm(args, w, rank, world, dist):
     import torch
 
@@ -538,6 +571,9 @@ def gpu_arm(args, w, rank, world, dist):
         torch.cuda.empty_cache()
         long_seq = long_seq_record(args, ssd, torch, dev, stream, barrier, peaks, peak_kind,
                                    {"sm_max_mhz": None}, rank)
+    decode = None
+    if rank == 0 and args.workload == DEFAULT_WORKLOAD:
+        decode = decode_record(ssd, torch, dev, stream, barrier, peaks, peak_kind)
     clocks = sampler.stop()
     if prev_affinity is not None:  # the oracle baseline below runs on all the cores again
         os.sched_setaffinity(0, prev_affinity)
@@ -593,6 +629,7 @@ def gpu_arm(args, w, rank, world, dist):
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                 "host_buffers": host_node},
         "long_seq": long_seq,
+        "decode": decode,
         "gpu_launches": launches,
         "clocks": clocks,
     }

@@ -159,6 +159,20 @@ ssd_status_t ssd_backward_state(const ssd_problem_t* prob, const void* x, const 
                                 void* dC, float* d_initial_state, int after_forward,
                                 void* workspace, size_t workspace_bytes, void* stream);
 
+/* One token of the recurrence for every sequence of a batch (single-token decode), from
+ * a carried state (page "Mamba-2架构与LaCT并行计算技术解析" §1.1):
+ *     delta = softplus(raw_dt + delta_init),
+ *     state <- exp(-delta) state + delta x B^T,   y = state C.
+ * prob: batch = number of sequences, seqlen = 1, nseq = 0; H, P, N, G, dtype, delta_init
+ * as for ssd_forward (chunk_size must be a supported value and is otherwise unused).
+ * state_in, state_out: [batch][H][P][N] float32 (the same pointer updates in place; other
+ * overlaps are SSD_ERR_INVALID_ARG); x, y: [batch][H][P]; raw_dt: [batch][H] float32;
+ * B, C: [batch][G][N].  Device memory, 16-byte aligned; no workspace.  Bound by the
+ * state's bytes: it is read and written once. */
+ssd_status_t ssd_decode_step(const ssd_problem_t* prob, const float* state_in, float* state_out,
+                             const void* x, const float* raw_dt, const void* B, const void* C,
+                             void* y, void* stream);
+
 /* Device bytes that ssd_step_host needs for `prob`: the backward workspace followed by
  * device copies of the step's inputs and results.  Pure host function. */
 ssd_status_t ssd_step_host_size(const ssd_problem_t* prob, size_t* bytes);

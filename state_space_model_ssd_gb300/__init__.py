@@ -21,7 +21,7 @@ from typing import Optional
 from . import _lib
 from ._lib import SSDError, check
 
-__all__ = ["forward", "backward", "step_host", "step_host_size", "workspace_size",
+__all__ = ["forward", "backward", "decode_step", "step_host", "step_host_size", "workspace_size",
            "dispatch_path", "make_problem", "last_launch_count", "profiler", "SSDError"]
 
 
@@ -181,6 +181,34 @@ def backward(x, raw_dt, B, C, dy, delta_init: float, chunk_size: int = 64, cu_se
             _ptr(ws), ws.numel(), _stream(stream))
     check(st, "ssd_backward_state")
     return out
+
+
+def decode_step(state, x, raw_dt, B, C, delta_init: float, out=None, state_out=None,
+                stream=None):
+    """Runs ssd_decode_step for one token of every sequence of a batch: ``state``
+    float32 ``[batch, H, P, N]`` (updated in place unless ``state_out`` is given), ``x``
+    ``[batch, H, P]``, ``raw_dt`` float32 ``[batch, H]``, ``B``/``C`` ``[batch, G, N]``.
+    Returns ``(y [batch, H, P], new state)``."""
+    torch = _torch()
+    dev = x.device
+    _check_tensor(state, "state", torch.float32, dev)
+    _check_tensor(x, "x")
+    _check_tensor(raw_dt, "raw_dt", torch.float32, dev)
+    _check_tensor(B, "B", x.dtype, dev)
+    _check_tensor(C, "C", x.dtype, dev)
+    if x.dim() != 3 or B.dim() != 3 or state.dim() != 4:
+        raise ValueError("x must be [batch, H, P], B/C [batch, G, N], state [batch, H, P, N]")
+    prob = make_problem(x.unsqueeze(1), B.unsqueeze(1), delta_init, 64)
+    if tuple(state.shape) != (prob.batch, prob.nheads, prob.headdim, prob.dstate):
+        raise ValueError("state must be [batch, H, P, N]")
+    so = state if state_out is None else state_out
+    y = torch.empty_like(x) if out is None else out
+    with torch.cuda.device(dev):
+        st = _lib.lib().ssd_decode_step(ctypes.byref(prob), _ptr(state), _ptr(so), _ptr(x),
+                                        _ptr(raw_dt), _ptr(B), _ptr(C), _ptr(y),
+                                        _stream(stream))
+    check(st, "ssd_decode_step")
+    return y, so
 
 
 def step_host_size(problem: _lib.Problem) -> int:

@@ -58,6 +58,7 @@ _SIGS = {
                                          _VP]),
     "ssd_backward_state": (ctypes.c_int, [_PP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP,
                                           _VP, _VP, _VP, ctypes.c_int, _VP, _SZ, _VP]),
+    "ssd_decode_step": (ctypes.c_int, [_PP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP]),
     "ssd_forward_noalloc": (ctypes.c_int, [_PP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP]),
     "ssd_forward_noalloc_status": (ctypes.c_int, [_VP, ctypes.POINTER(ctypes.c_int32)]),
     "ssd_step_host_size": (ctypes.c_int, [_PP, ctypes.POINTER(_SZ)]),

@@ -443,6 +443,28 @@ ssd_status_t ssd_backward_state(const ssd_problem_t* prob, const void* x, const 
                          after_forward != 0);
 }
 
+ssd_status_t ssd_decode_step(const ssd_problem_t* prob, const float* state_in, float* state_out,
+                             const void* x, const float* raw_dt, const void* B, const void* C,
+                             void* y, void* stream) {
+    Prob b;
+    ssd_status_t st = make_prob(prob, &b);
+    if (st != SSD_OK) return st;
+    if (prob->nseq != 0 || prob->seqlen != 1) return SSD_ERR_INVALID_ARG;
+    if (!state_in || !state_out || !x || !raw_dt || !B || !C || !y) return SSD_ERR_INVALID_ARG;
+    if (!aligned16(state_in) || !aligned16(state_out) || !aligned16(x) || !aligned16(raw_dt) ||
+        !aligned16(B) || !aligned16(C) || !aligned16(y))
+        return SSD_ERR_ALIGNMENT;
+    const long long sbytes = (long long)b.nseq * b.H * b.P * b.N * 4;
+    const char* si = static_cast<const char*>(static_cast<const void*>(state_in));
+    const char* so = static_cast<const char*>(static_cast<void*>(state_out));
+    if (si != so && si < so + sbytes && so < si + sbytes) return SSD_ERR_INVALID_ARG;
+    g_last_launches = 1;
+    return launch_decode_step(b, state_in, state_out, x, raw_dt, B, C, y,
+                              static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? SSD_OK
+               : SSD_ERR_CUDA;
+}
+
 ssd_status_t ssd_device_status(const void* workspace, void* stream, int32_t* device_status) {
     if (!workspace || !device_status) return SSD_ERR_INVALID_ARG;
     cudaStream_t s = static_cast<cudaStream_t>(stream);

@@ -138,6 +138,11 @@ cudaError_t tc_forward(const Prob& pb, const Args& a, Launch& L);
 cudaError_t tc_backward(const Prob& pb, const Args& a, Launch& L, bool reuse_forward = false);
 bool tc_supported(int dtype, int P, int N, int Q, int H, int G);
 
+// One decode step for pb.nseq sequences (the batch rows).
+cudaError_t launch_decode_step(const Prob& pb, const float* hin, float* hout, const void* x,
+                               const float* raw, const void* B, const void* C, void* y,
+                               cudaStream_t stream);
+
 // Shared small kernels (segment table, state scans, gradient epilogues).
 cudaError_t launch_seg_table(const Prob& pb, const Args& a, Launch& L);
 // Checks that the workspace's segment table was built for this problem and these inputs;

@@ -136,3 +136,19 @@ def test_profiler_filter_is_host_only(lib):
     """Setting or clearing the profiler's kernel filter touches no GPU state."""
     assert lib.ssd_profiler_only(b"tc_bwd_dxdb") == 0
     assert lib.ssd_profiler_only(None) == 0
+
+
+def test_decode_step_host_checks(lib):
+    """Host-side checks of ssd_decode_step (nothing is launched): seqlen must be 1, packed
+    input is refused, overlapping distinct state buffers are refused, misaligned ones too."""
+    p = _prob(seqlen=1, batch=3)
+    a = ctypes.c_void_p(1 << 20)
+    assert lib.ssd_decode_step(ctypes.byref(_prob(seqlen=2)), a, a, a, a, a, a, a, None) == 1
+    assert lib.ssd_decode_step(ctypes.byref(_prob(seqlen=1, nseq=1)), a, a, a, a, a, a, a,
+                               None) == 1
+    # state_out starts 16 bytes into state_in: an overlap that is not in place
+    assert lib.ssd_decode_step(ctypes.byref(p), a, ctypes.c_void_p((1 << 20) + 16), a, a, a, a,
+                               a, None) == 1
+    assert lib.ssd_decode_step(ctypes.byref(p), ctypes.c_void_p((1 << 20) + 4), a, a, a, a, a,
+                               a, None) == 3
+    assert lib.ssd_decode_step(ctypes.byref(p), None, a, a, a, a, a, a, None) == 1
