@@ -141,6 +141,13 @@ Layout make_layout(const Prob& b, bool bwd) {
     off = align_up(off + sizeof(float) * (size_t)b.nseg_max * b.H * PN);
     l.lam = off;
     off = align_up(off + sizeof(float) * (size_t)b.nseg_max * b.H);
+    l.scan_state = l.scan_dec = 0;
+    if (const int nblk = scan_blocks(b)) {
+        l.scan_state = off;
+        off = align_up(off + sizeof(float) * (size_t)nblk * b.H * PN);
+        l.scan_dec = off;
+        off = align_up(off + sizeof(float) * (size_t)nblk * b.H);
+    }
     // regions both passes use come first, so that a forward's workspace is a prefix of
     // the backward's (ssd_backward_after_forward reuses it)
     l.l0 = l.fac = l.fb = 0;
@@ -189,6 +196,10 @@ Args make_args(const Prob& b, const Layout& l, void* ws) {
     a.segtab = reinterpret_cast<SegInfo*>(base + l.segtab);
     a.A = reinterpret_cast<float*>(base + l.A);
     a.lam = reinterpret_cast<float*>(base + l.lam);
+    if (l.scan_state) {
+        a.scan_state = reinterpret_cast<float*>(base + l.scan_state);
+        a.scan_dec = reinterpret_cast<float*>(base + l.scan_dec);
+    }
     if (l.adj) {
         a.adj = reinterpret_cast<float*>(base + l.adj);
         a.rq = reinterpret_cast<float*>(base + l.rq);

@@ -53,7 +53,8 @@ struct Prob {
 
 // Byte offsets of the workspace regions.
 struct Layout {
-    size_t header, segtab, A, lam, adj, rq, rqsuf, dbacc, dcacc, rtok, kfin, l0, fac, fb, cb32, total;
+    size_t header, segtab, A, lam, scan_state, scan_dec, adj, rq, rqsuf, dbacc, dcacc, rtok, kfin, l0,
+        fac, fb, cb32, total;
 };
 
 // Everything a kernel needs; passed by value.
@@ -77,6 +78,8 @@ struct Args {
     SegInfo* segtab;
     float* A;       // [nseg_max][H][P][N]: segment aggregates, then the state entering each segment
     float* lam;     // [nseg_max][H]: segment log-decay, sum of -delta
+    float* scan_state;  // [scan blocks][H][P][N]: block summaries of the scans over many segments
+    float* scan_dec;    // [scan blocks][H]
     float* adj;     // [nseg_max][H][P][N]: adjoint aggregates, then the adjoint leaving each segment
     float* rq;      // [nseg_max][H]
     float* rqsuf;   // [nseg_max][H]
@@ -150,6 +153,8 @@ cudaError_t launch_seg_table(const Prob& pb, const Args& a, Launch& L);
 cudaError_t launch_forward_match(const Prob& pb, const Args& a, Launch& L);
 // d_initial_state of the empty packed sequences: their d_final_state (or zero).
 cudaError_t launch_empty_seq_grads(const Prob& pb, const Args& a, Launch& L);
+// Blocks of segments the scans over segments summarise first (0: a single pass).
+int scan_blocks(const Prob& pb);
 cudaError_t launch_state_scan(const Prob& pb, const Args& a, Launch& L, bool write_final);
 cudaError_t launch_adjoint_scan(const Prob& pb, const Args& a, Launch& L);
 cudaError_t launch_bwd_epilogue(const Prob& pb, const Args& a, Launch& L);

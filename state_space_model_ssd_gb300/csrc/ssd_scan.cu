@@ -182,26 +182,48 @@ __global__ void forward_match_kernel(Args a) {
 
 constexpr int kScanThreads = 128;
 constexpr int kScanUnroll = 4;  // segments per batch; the next batch loads while this one is stored
+// Scans over more than 2 kScanBlockSegs segments run in three passes: a summary of every
+// block of kScanBlockSegs segments, a short serial pass over the block summaries, then
+// each block's scan from its carry-in, so that the serial chain is kScanBlockSegs + blocks
+// + kScanBlockSegs steps long instead of one step per segment.
+constexpr int kScanBlockSegs = 64;
 
-// Forward scan over segments, per head and per state element (4 per thread; the
-// scan is the same for either storage order of the states).
-// On entry a.A holds the segment aggregates; on exit the state entering each
-// segment.  Optionally writes the state after the last segment of every
-// sequence to final_state.
-__global__ void __launch_bounds__(kScanThreads) state_scan_kernel(Args a, int write_final) {
+// Row-major float4 index of state piece e4 (final_state, the initial state and their
+// gradients are row-major; the segment states may be lane-major).
+__device__ __forceinline__ int row_major_e4(const Args& a, int e4) {
+    if (!a.state_lm) return e4;
+    const int N4 = a.N >> 2, blk = e4 / (32 * N4), j = e4 - blk * 32 * N4;
+    return (blk * 32 + (j & 31)) * N4 + (j >> 5);
+}
+
+__device__ __forceinline__ float4 fma4(float d, float4 c, float4 g) {
+    return make_float4(fmaf(d, c.x, g.x), fmaf(d, c.y, g.y), fmaf(d, c.z, g.z), fmaf(d, c.w, g.w));
+}
+
+// Forward scan over segments, per head and per state piece (4 elements per thread; the
+// scan is the same for either storage order of the states).  On entry a.A holds the
+// segment aggregates; on exit the state entering each segment (the sequence's initial
+// state, or zero, at its first segment).  Optionally writes the state after the last
+// segment of every sequence to final_state.
+//   mode 0: every segment in one pass;
+//   mode 1: the summary of block blockIdx.z: its carry-out from a zero carry-in and the
+//           factor a carry-in gets by its end (zero once a sequence starts in the block);
+//   mode 2: the scan of block blockIdx.z from its carry-in (bstate after the block pass).
+__global__ void __launch_bounds__(kScanThreads)
+    state_scan_kernel(Args a, int write_final, int mode, float4* bstate, float* bdec) {
     const int h = blockIdx.y;
     const int PN4 = (a.P * a.N) >> 2;
     const int e4 = blockIdx.x * blockDim.x + threadIdx.x;
     if (e4 >= PN4) return;
     const int nseg = a.hdr->nseg;
+    const int blk = blockIdx.z;
+    const int j0 = mode == 0 ? 0 : blk * kScanBlockSegs;
+    const int j1 = mode == 0 ? nseg : min(nseg, j0 + kScanBlockSegs);
+    const long long bi = ((long long)blk * a.H + h) * PN4 + e4;
     float4* A4 = reinterpret_cast<float4*>(a.A);
-    // row-major float4 index of this thread's four elements (final_state is row-major)
-    int fe4 = e4;
-    if (a.state_lm) {
-        const int N4 = a.N >> 2, blk = e4 / (32 * N4), j = e4 - blk * 32 * N4;
-        fe4 = (blk * 32 + (j & 31)) * N4 + (j >> 5);
-    }
-    float4 carry = make_float4(0.f, 0.f, 0.f, 0.f);
+    const int fe4 = row_major_e4(a, e4);
+    float4 carry = mode == 2 ? bstate[bi] : make_float4(0.f, 0.f, 0.f, 0.f);
+    float dprod = 1.f;
     float4 agg[kScanUnroll], nagg[kScanUnroll];
     float dec[kScanUnroll], ndec[kScanUnroll];
     int flags[kScanUnroll], seq[kScanUnroll], nflags[kScanUnroll], nseqi[kScanUnroll];
@@ -209,7 +231,7 @@ __global__ void __launch_bounds__(kScanThreads) state_scan_kernel(Args a, int wr
 #pragma unroll
         for (int u = 0; u < kScanUnroll; ++u) {
             const int s = s0 + u;
-            if (s < nseg) {
+            if (s < j1) {
                 g[u] = A4[((long long)s * a.H + h) * PN4 + e4];
                 dc[u] = expf(a.lam[(long long)s * a.H + h]);
                 fl[u] = a.segtab[s].flags;
@@ -217,22 +239,22 @@ __global__ void __launch_bounds__(kScanThreads) state_scan_kernel(Args a, int wr
             }
         }
     };
-    load(0, agg, dec, flags, seq);
-    for (int s0 = 0; s0 < nseg; s0 += kScanUnroll) {
-        if (s0 + kScanUnroll < nseg) load(s0 + kScanUnroll, nagg, ndec, nflags, nseqi);
+    if (j0 < j1) load(j0, agg, dec, flags, seq);
+    for (int s0 = j0; s0 < j1; s0 += kScanUnroll) {
+        if (s0 + kScanUnroll < j1) load(s0 + kScanUnroll, nagg, ndec, nflags, nseqi);
 #pragma unroll
         for (int u = 0; u < kScanUnroll; ++u) {
             const int s = s0 + u;
-            if (s >= nseg) break;
-            if (flags[u] & SEG_FIRST)
+            if (s >= j1) break;
+            if (flags[u] & SEG_FIRST) {
                 carry = a.h0 ? reinterpret_cast<const float4*>(a.h0)[((long long)seq[u] * a.H + h) * PN4 + fe4]
                              : make_float4(0.f, 0.f, 0.f, 0.f);
-            A4[((long long)s * a.H + h) * PN4 + e4] = carry;
-            carry.x = fmaf(dec[u], carry.x, agg[u].x);
-            carry.y = fmaf(dec[u], carry.y, agg[u].y);
-            carry.z = fmaf(dec[u], carry.z, agg[u].z);
-            carry.w = fmaf(dec[u], carry.w, agg[u].w);
-            if (write_final && (flags[u] & SEG_LAST))
+                dprod = 0.f;
+            }
+            if (mode != 1) A4[((long long)s * a.H + h) * PN4 + e4] = carry;
+            carry = fma4(dec[u], carry, agg[u]);
+            dprod *= dec[u];
+            if (mode != 1 && write_final && (flags[u] & SEG_LAST))
                 reinterpret_cast<float4*>(a.final_state)[((long long)seq[u] * a.H + h) * PN4 + fe4] =
                     carry;
         }
@@ -244,25 +266,51 @@ __global__ void __launch_bounds__(kScanThreads) state_scan_kernel(Args a, int wr
             seq[u] = nseqi[u];
         }
     }
+    if (mode == 1) {
+        bstate[bi] = carry;
+        if (e4 == 0) bdec[(long long)blk * a.H + h] = dprod;
+    }
 }
 
-// Reverse scan of the adjoint over segments.  On entry a.adj holds, per
-// segment, sum_u exp(Lambda_u - Lambda_before) dy_u C_u^T; on exit the adjoint
-// arriving at the segment's last token from later tokens of its sequence.
-__global__ void __launch_bounds__(kScanThreads) adjoint_scan_kernel(Args a) {
+// The serial pass over block summaries, per head and state piece: replaces each block's
+// carry-out by its carry-in.  reverse: the adjoint's order (from the last block).
+__global__ void __launch_bounds__(kScanThreads)
+    scan_blocks_kernel(Args a, int nblk, int reverse, float4* bstate, const float* bdec) {
+    const int h = blockIdx.y;
+    const int PN4 = (a.P * a.N) >> 2;
+    const int e4 = blockIdx.x * blockDim.x + threadIdx.x;
+    if (e4 >= PN4) return;
+    float4 c = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int k = 0; k < nblk; ++k) {
+        const int blk = reverse ? nblk - 1 - k : k;
+        const long long bi = ((long long)blk * a.H + h) * PN4 + e4;
+        const float4 out = bstate[bi];
+        bstate[bi] = c;
+        c = fma4(bdec[(long long)blk * a.H + h], c, out);
+    }
+}
+
+// Reverse scan of the adjoint over segments.  On entry a.adj holds, per segment,
+// sum_u exp(Lambda_u - Lambda_before) dy_u C_u^T; on exit the adjoint arriving at the
+// segment's last token from later tokens of its sequence (the sequence's final-state
+// gradient, or zero, at its last segment).  Writes d_initial_state (the adjoint before a
+// sequence's first token) when asked.  Modes as state_scan_kernel's, blocks walked from
+// their end.
+__global__ void __launch_bounds__(kScanThreads)
+    adjoint_scan_kernel(Args a, int mode, float4* bstate, float* bdec) {
     const int h = blockIdx.y;
     const int PN4 = (a.P * a.N) >> 2;
     const int e4 = blockIdx.x * blockDim.x + threadIdx.x;
     if (e4 >= PN4) return;
     const int nseg = a.hdr->nseg;
+    const int blk = blockIdx.z;
+    const int j0 = mode == 0 ? 0 : blk * kScanBlockSegs;
+    const int j1 = mode == 0 ? nseg : min(nseg, j0 + kScanBlockSegs);
+    const long long bi = ((long long)blk * a.H + h) * PN4 + e4;
     float4* G4 = reinterpret_cast<float4*>(a.adj);
-    // row-major float4 index of this thread's four elements (d_final_state, d_initial_state)
-    int fe4 = e4;
-    if (a.state_lm) {
-        const int N4 = a.N >> 2, blk = e4 / (32 * N4), j = e4 - blk * 32 * N4;
-        fe4 = (blk * 32 + (j & 31)) * N4 + (j >> 5);
-    }
-    float4 carry = make_float4(0.f, 0.f, 0.f, 0.f);
+    const int fe4 = row_major_e4(a, e4);
+    float4 carry = mode == 2 ? bstate[bi] : make_float4(0.f, 0.f, 0.f, 0.f);
+    float dprod = 1.f;
     float4 agg[kScanUnroll], nagg[kScanUnroll];
     float dec[kScanUnroll], ndec[kScanUnroll];
     int flags[kScanUnroll], nflags[kScanUnroll], seq[kScanUnroll], nseqi[kScanUnroll];
@@ -270,7 +318,7 @@ __global__ void __launch_bounds__(kScanThreads) adjoint_scan_kernel(Args a) {
 #pragma unroll
         for (int u = 0; u < kScanUnroll; ++u) {
             const int s = s0 - u;
-            if (s >= 0) {
+            if (s >= j0) {
                 g[u] = G4[((long long)s * a.H + h) * PN4 + e4];
                 dc[u] = expf(a.lam[(long long)s * a.H + h]);
                 fl[u] = a.segtab[s].flags;
@@ -278,25 +326,26 @@ __global__ void __launch_bounds__(kScanThreads) adjoint_scan_kernel(Args a) {
             }
         }
     };
-    load(nseg - 1, agg, dec, flags, seq);
-    for (int s0 = nseg - 1; s0 >= 0; s0 -= kScanUnroll) {
-        if (s0 - kScanUnroll >= 0) load(s0 - kScanUnroll, nagg, ndec, nflags, nseqi);
+    if (j0 < j1) load(j1 - 1, agg, dec, flags, seq);
+    for (int s0 = j1 - 1; s0 >= j0; s0 -= kScanUnroll) {
+        if (s0 - kScanUnroll >= j0) load(s0 - kScanUnroll, nagg, ndec, nflags, nseqi);
 #pragma unroll
         for (int u = 0; u < kScanUnroll; ++u) {
             const int s = s0 - u;
-            if (s < 0) break;
+            if (s < j0) break;
             const long long srow = ((long long)seq[u] * a.H + h) * PN4 + fe4;
             // the adjoint arriving at a sequence's last token: the gradient of its final state
-            if (flags[u] & SEG_LAST)
+            if (flags[u] & SEG_LAST) {
                 carry = a.dhT ? reinterpret_cast<const float4*>(a.dhT)[srow]
                               : make_float4(0.f, 0.f, 0.f, 0.f);
-            G4[((long long)s * a.H + h) * PN4 + e4] = carry;
-            carry.x = fmaf(dec[u], carry.x, agg[u].x);
-            carry.y = fmaf(dec[u], carry.y, agg[u].y);
-            carry.z = fmaf(dec[u], carry.z, agg[u].z);
-            carry.w = fmaf(dec[u], carry.w, agg[u].w);
+                dprod = 0.f;
+            }
+            if (mode != 1) G4[((long long)s * a.H + h) * PN4 + e4] = carry;
+            carry = fma4(dec[u], carry, agg[u]);
+            dprod *= dec[u];
             // before a sequence's first token: the gradient of its initial state
-            if (a.dh0 && (flags[u] & SEG_FIRST)) reinterpret_cast<float4*>(a.dh0)[srow] = carry;
+            if (mode != 1 && a.dh0 && (flags[u] & SEG_FIRST))
+                reinterpret_cast<float4*>(a.dh0)[srow] = carry;
         }
 #pragma unroll
         for (int u = 0; u < kScanUnroll; ++u) {
@@ -305,6 +354,10 @@ __global__ void __launch_bounds__(kScanThreads) adjoint_scan_kernel(Args a) {
             flags[u] = nflags[u];
             seq[u] = nseqi[u];
         }
+    }
+    if (mode == 1) {
+        bstate[bi] = carry;
+        if (e4 == 0) bdec[(long long)blk * a.H + h] = dprod;
     }
 }
 
@@ -388,19 +441,57 @@ cudaError_t launch_empty_seq_grads(const Prob& pb, const Args& a, Launch& L) {
     return L.end();
 }
 
+int scan_blocks(const Prob& pb) {
+    return pb.nseg_max > 2 * kScanBlockSegs ? (int)((pb.nseg_max + kScanBlockSegs - 1) / kScanBlockSegs)
+                                            : 0;
+}
+
+namespace {
+
+template <typename K>
+cudaError_t scan_three_pass(const Prob& pb, const Args& a, Launch& L, const char* name, K pass,
+                            int reverse) {
+    const int PN4 = (pb.P * pb.N) / 4;
+    const int nblk = scan_blocks(pb);
+    const dim3 g1((PN4 + kScanThreads - 1) / kScanThreads, pb.H, nblk);
+    const dim3 g2((PN4 + kScanThreads - 1) / kScanThreads, pb.H);
+    float4* bs = reinterpret_cast<float4*>(a.scan_state);
+    L.begin(name);
+    pass(g1, 1);
+    cudaError_t e = L.end();
+    if (e != cudaSuccess) return e;
+    L.begin("scan_blocks");
+    scan_blocks_kernel<<<g2, kScanThreads, 0, L.stream>>>(a, nblk, reverse, bs, a.scan_dec);
+    if ((e = L.end()) != cudaSuccess) return e;
+    L.begin(name);
+    pass(g1, 2);
+    return L.end();
+}
+
+}  // namespace
+
 cudaError_t launch_state_scan(const Prob& pb, const Args& a, Launch& L, bool write_final) {
     const int PN4 = (pb.P * pb.N) / 4;
-    dim3 grid((PN4 + kScanThreads - 1) / kScanThreads, pb.H);
+    float4* bs = reinterpret_cast<float4*>(a.scan_state);
+    auto pass = [&](dim3 grid, int mode) {
+        state_scan_kernel<<<grid, kScanThreads, 0, L.stream>>>(a, write_final ? 1 : 0, mode, bs,
+                                                               a.scan_dec);
+    };
+    if (scan_blocks(pb)) return scan_three_pass(pb, a, L, "state_scan", pass, 0);
     L.begin("state_scan");
-    state_scan_kernel<<<grid, kScanThreads, 0, L.stream>>>(a, write_final ? 1 : 0);
+    pass(dim3((PN4 + kScanThreads - 1) / kScanThreads, pb.H), 0);
     return L.end();
 }
 
 cudaError_t launch_adjoint_scan(const Prob& pb, const Args& a, Launch& L) {
     const int PN4 = (pb.P * pb.N) / 4;
-    dim3 grid((PN4 + kScanThreads - 1) / kScanThreads, pb.H);
+    float4* bs = reinterpret_cast<float4*>(a.scan_state);
+    auto pass = [&](dim3 grid, int mode) {
+        adjoint_scan_kernel<<<grid, kScanThreads, 0, L.stream>>>(a, mode, bs, a.scan_dec);
+    };
+    if (scan_blocks(pb)) return scan_three_pass(pb, a, L, "adjoint_scan", pass, 1);
     L.begin("adjoint_scan");
-    adjoint_scan_kernel<<<grid, kScanThreads, 0, L.stream>>>(a);
+    pass(dim3((PN4 + kScanThreads - 1) / kScanThreads, pb.H), 0);
     return L.end();
 }
 

@@ -121,3 +121,15 @@ def test_split_and_continue(ssd):
                          initial_state=f1)
     assert rel_err(to_np(torch.cat([y1, y2], 1)), to_np(y)) <= TOL["bf16"]
     assert rel_err(to_np(f2), to_np(fs)) <= TOL["bf16"]
+
+
+@pytest.mark.parametrize("dtype,P,N,H", [("f32", 16, 16, 2), ("bf16", 64, 64, 2)])
+def test_many_segments_blocked_scans(ssd, oracle_mod, monkeypatch, dtype, P, N, H):
+    """More than 128 segments (one chunk each): the scans over segments run as block
+    summaries, a pass over the blocks and per-block scans, with sequences starting inside
+    blocks, initial states and final-state gradients."""
+    monkeypatch.setenv("SSD_SEGMENT_CHUNKS", "1")
+    lens = [3000, 64, 1, 4100, 700, 0, 2000]
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    d = _draw(36, int(cu[-1]), H, P, N, dtype, cu=cu)
+    _check_all(ssd, oracle_mod, d, dtype, -4.6)
