@@ -159,6 +159,33 @@ ssd_status_t ssd_backward_state(const ssd_problem_t* prob, const void* x, const 
                                 void* dC, float* d_initial_state, int after_forward,
                                 void* workspace, size_t workspace_bytes, void* stream);
 
+/* Bidirectional mode (page "Mamba-2架构与LaCT并行计算技术解析" §3.1): the scan over each
+ * sequence (dense row or packed sequence) and the scan over the same sequence reversed,
+ * on the same x, raw_dt, B, C; the reverse direction's output is put back at its tokens'
+ * positions and the two are concatenated along the last dimension:
+ *     y[t][h] = [ y_forward[t][h] (P values) | y_reverse[t][h] (P values) ],
+ * y_reverse[t] depending on tokens t .. the sequence's end.  y: [T][H][2P] (dtype of x).
+ * final_state_fwd / final_state_rev ([nseq or batch][H][P][N] float32, NULL: not written):
+ * each direction's state after its last token (the state size doubles).  workspace: >=
+ * ssd_bidirectional_workspace_size(prob, 0) bytes, 256-byte aligned; it holds the
+ * reversed inputs and both directions' outputs besides ssd_forward's workspace. */
+ssd_status_t ssd_bidirectional_workspace_size(const ssd_problem_t* prob, int for_backward,
+                                              size_t* bytes);
+ssd_status_t ssd_bidirectional_forward(const ssd_problem_t* prob, const void* x,
+                                       const float* raw_dt, const void* B, const void* C,
+                                       const int32_t* cu_seqlens, void* y,
+                                       float* final_state_fwd, float* final_state_rev,
+                                       void* workspace, size_t workspace_bytes, void* stream);
+/* Backward of ssd_bidirectional_forward for an upstream gradient dy [T][H][2P] of y (zero
+ * final-state gradients): dx, d_raw_dt, dB, dC as ssd_backward writes them, each the sum of
+ * the two directions' contributions.  workspace: >= ssd_bidirectional_workspace_size(prob,
+ * 1) bytes. */
+ssd_status_t ssd_bidirectional_backward(const ssd_problem_t* prob, const void* x,
+                                        const float* raw_dt, const void* B, const void* C,
+                                        const int32_t* cu_seqlens, const void* dy, void* dx,
+                                        float* d_raw_dt, void* dB, void* dC, void* workspace,
+                                        size_t workspace_bytes, void* stream);
+
 /* One token of the recurrence for every sequence of a batch (single-token decode), from
  * a carried state (page "Mamba-2架构与LaCT并行计算技术解析" §1.1):
  *     delta = softplus(raw_dt + delta_init),

@@ -138,3 +138,43 @@ def backward(x, raw_dt, B, C, dy, delta_init: float, cu_seqlens=None, initial_st
     if rc != 0:
         raise ValueError("oracle backward failed (code %d)" % rc)
     return {"dx": dx, "d_raw_dt": draw, "dB": dB, "dC": dC, "d_initial_state": dh0}
+
+
+def _flip_sequences(a, cu_seqlens):
+    """Each sequence of a [batch, L, ...] array reversed along its token axis (dense rows,
+    or the packed sequences of cu_seqlens)."""
+    a = np.asarray(a)
+    if cu_seqlens is None:
+        return np.ascontiguousarray(a[:, ::-1])
+    out = np.empty_like(a)
+    cu = np.asarray(cu_seqlens, dtype=np.int64)
+    for s in range(len(cu) - 1):
+        out[:, cu[s]:cu[s + 1]] = a[:, cu[s]:cu[s + 1]][:, ::-1]
+    return out
+
+
+def bidirectional_forward(x, raw_dt, B, C, delta_init: float, cu_seqlens=None, threads: int = 0):
+    """Bidirectional mode (page "Mamba-2架构与LaCT并行计算技术解析" §3.1): the scan over
+    each sequence and over the sequence reversed, the reverse direction's outputs put back
+    at their tokens' positions, concatenated along the last dimension.  Both directions
+    read the same x, raw_dt, B, C.  Returns ``(y [batch, L, H, 2P], final_state_forward,
+    final_state_reverse)`` in fp64."""
+    fl = lambda a: _flip_sequences(a, cu_seqlens)  # noqa: E731
+    yf, ff = forward(x, raw_dt, B, C, delta_init, cu_seqlens=cu_seqlens, threads=threads)
+    yr, fr = forward(fl(x), fl(raw_dt), fl(B), fl(C), delta_init, cu_seqlens=cu_seqlens,
+                     threads=threads)
+    return np.concatenate([yf, fl(yr)], axis=-1), ff, fr
+
+
+def bidirectional_backward(x, raw_dt, B, C, dy, delta_init: float, cu_seqlens=None,
+                           threads: int = 0):
+    """Gradients of sum(dy * y) for y = bidirectional_forward(...)[0], dy [batch, L, H, 2P]:
+    each input's gradient is the forward direction's plus the reverse direction's put back
+    at its tokens' positions."""
+    fl = lambda a: _flip_sequences(a, cu_seqlens)  # noqa: E731
+    P = np.asarray(x).shape[-1]
+    dy = np.asarray(dy)
+    gf = backward(x, raw_dt, B, C, dy[..., :P], delta_init, cu_seqlens=cu_seqlens, threads=threads)
+    gr = backward(fl(x), fl(raw_dt), fl(B), fl(C), fl(dy[..., P:]), delta_init,
+                  cu_seqlens=cu_seqlens, threads=threads)
+    return {k: gf[k] + fl(gr[k]) for k in ("dx", "d_raw_dt", "dB", "dC")}

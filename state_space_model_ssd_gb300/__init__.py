@@ -21,7 +21,7 @@ from typing import Optional
 from . import _lib
 from ._lib import SSDError, check
 
-__all__ = ["forward", "backward", "decode_step", "step_host", "step_host_size", "workspace_size",
+__all__ = ["forward", "backward", "bidirectional_forward", "bidirectional_backward", "decode_step", "step_host", "step_host_size", "workspace_size",
            "dispatch_path", "make_problem", "last_launch_count", "profiler", "SSDError"]
 
 
@@ -180,6 +180,68 @@ def backward(x, raw_dt, B, C, dy, delta_init: float, chunk_size: int = 64, cu_se
             _ptr(out.get("d_initial_state") if d_initial_state else None), int(after_forward),
             _ptr(ws), ws.numel(), _stream(stream))
     check(st, "ssd_backward_state")
+    return out
+
+
+def bidirectional_workspace_size(problem: _lib.Problem, for_backward: bool) -> int:
+    n = ctypes.c_size_t(0)
+    check(_lib.lib().ssd_bidirectional_workspace_size(ctypes.byref(problem), int(for_backward),
+                                                      ctypes.byref(n)),
+          "ssd_bidirectional_workspace_size")
+    return int(n.value)
+
+
+def bidirectional_forward(x, raw_dt, B, C, delta_init: float, chunk_size: int = 64,
+                          cu_seqlens=None, final_state: bool = True, workspace=None,
+                          stream=None):
+    """Runs ssd_bidirectional_forward.  Returns ``(y [batch, L, H, 2P], final state of the
+    forward direction, final state of the reverse direction)`` (None without final_state)."""
+    torch = _torch()
+    dev = x.device
+    for t, n in ((x, "x"), (B, "B"), (C, "C")):
+        _check_tensor(t, n)
+    _check_tensor(raw_dt, "raw_dt", torch.float32, dev)
+    if cu_seqlens is not None:
+        _check_tensor(cu_seqlens, "cu_seqlens", torch.int32, dev)
+    prob = make_problem(x, B, delta_init, chunk_size, cu_seqlens)
+    nseq = prob.nseq if prob.nseq > 0 else prob.batch
+    y = torch.empty(x.shape[:-1] + (2 * x.shape[-1],), dtype=x.dtype, device=dev)
+    fs = [None, None]
+    if final_state:
+        fs = [torch.empty((nseq, prob.nheads, prob.headdim, prob.dstate), dtype=torch.float32,
+                          device=dev) for _ in range(2)]
+    ws = _workspace(bidirectional_workspace_size(prob, False), dev, workspace)
+    with torch.cuda.device(dev):
+        st = _lib.lib().ssd_bidirectional_forward(
+            ctypes.byref(prob), _ptr(x), _ptr(raw_dt), _ptr(B), _ptr(C), _ptr(cu_seqlens),
+            _ptr(y), _ptr(fs[0]), _ptr(fs[1]), _ptr(ws), ws.numel(), _stream(stream))
+    check(st, "ssd_bidirectional_forward")
+    return y, fs[0], fs[1]
+
+
+def bidirectional_backward(x, raw_dt, B, C, dy, delta_init: float, chunk_size: int = 64,
+                           cu_seqlens=None, workspace=None, stream=None):
+    """Runs ssd_bidirectional_backward for dy ``[batch, L, H, 2P]``.  Returns a dict
+    ``dx, d_raw_dt, dB, dC``."""
+    torch = _torch()
+    dev = x.device
+    for t, n in ((x, "x"), (B, "B"), (C, "C"), (dy, "dy")):
+        _check_tensor(t, n)
+    _check_tensor(raw_dt, "raw_dt", torch.float32, dev)
+    if tuple(dy.shape) != tuple(x.shape[:-1]) + (2 * x.shape[-1],) or dy.dtype != x.dtype:
+        raise ValueError("dy must be [batch, L, H, 2P] in the dtype of x")
+    if cu_seqlens is not None:
+        _check_tensor(cu_seqlens, "cu_seqlens", torch.int32, dev)
+    prob = make_problem(x, B, delta_init, chunk_size, cu_seqlens)
+    out = {"dx": torch.empty_like(x), "d_raw_dt": torch.empty_like(raw_dt),
+           "dB": torch.empty_like(B), "dC": torch.empty_like(C)}
+    ws = _workspace(bidirectional_workspace_size(prob, True), dev, workspace)
+    with torch.cuda.device(dev):
+        st = _lib.lib().ssd_bidirectional_backward(
+            ctypes.byref(prob), _ptr(x), _ptr(raw_dt), _ptr(B), _ptr(C), _ptr(cu_seqlens),
+            _ptr(dy), _ptr(out["dx"]), _ptr(out["d_raw_dt"]), _ptr(out["dB"]), _ptr(out["dC"]),
+            _ptr(ws), ws.numel(), _stream(stream))
+    check(st, "ssd_bidirectional_backward")
     return out
 
 

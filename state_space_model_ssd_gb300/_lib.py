@@ -59,6 +59,11 @@ _SIGS = {
     "ssd_backward_state": (ctypes.c_int, [_PP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP,
                                           _VP, _VP, _VP, ctypes.c_int, _VP, _SZ, _VP]),
     "ssd_decode_step": (ctypes.c_int, [_PP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP]),
+    "ssd_bidirectional_workspace_size": (ctypes.c_int, [_PP, ctypes.c_int, ctypes.POINTER(_SZ)]),
+    "ssd_bidirectional_forward": (ctypes.c_int, [_PP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP,
+                                                 _VP, _SZ, _VP]),
+    "ssd_bidirectional_backward": (ctypes.c_int, [_PP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP,
+                                                  _VP, _VP, _VP, _SZ, _VP]),
     "ssd_forward_noalloc": (ctypes.c_int, [_PP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP]),
     "ssd_forward_noalloc_status": (ctypes.c_int, [_VP, ctypes.POINTER(ctypes.c_int32)]),
     "ssd_step_host_size": (ctypes.c_int, [_PP, ctypes.POINTER(_SZ)]),

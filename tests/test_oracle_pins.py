@@ -250,3 +250,74 @@ def test_rejects_bad_boundaries(oracle_mod):
         oracle_mod.forward(x, raw, B, C, -1.0, cu_seqlens=np.array([0, 7, 5, 10]))
     with pytest.raises(ValueError):
         oracle_mod.forward(x, raw, B, C, -1.0, cu_seqlens=np.array([0, 4, 9]))
+
+
+def _reverse_quadratic_form(x, raw, B, C, delta_init):
+    """The right-to-left recurrence H_t = exp(-delta_t) H_{t+1} + delta_t x_t B_t^T,
+    y_t = H_t C_t, written out as its upper-triangular quadratic form:
+    y[t] = sum_{s>=t} exp(-sum_{k=t..s-1} delta_k) (C_t . B_s) delta_s x_s."""
+    L, H, P = x.shape
+    G = B.shape[1]
+    delta = np.logaddexp(0.0, raw + delta_init)
+    y = np.zeros_like(x)
+    for h in range(H):
+        g = h // (H // G)
+        for t in range(L):
+            for s in range(t, L):
+                decay = np.exp(-np.sum(delta[t:s, h]))
+                y[t, h] += decay * np.dot(C[t, g], B[s, g]) * delta[s, h] * x[s, h]
+    return y
+
+
+def test_bidirectional_halves(oracle_mod):
+    """Bidirectional mode (page "Mamba-2架构与LaCT并行计算技术解析" §3.1): the first half
+    of each output row is the causal quadratic form, the second the reverse one, per packed
+    sequence."""
+    rng = np.random.default_rng(17)
+    H, P, N = 2, 3, 4
+    cu = np.array([0, 9, 10, 25], dtype=np.int32)
+    x, raw, B, C = _rand_problem(rng, 1, 25, H, P, N, raw_scale=1.0)
+    y, ff, fr = oracle_mod.bidirectional_forward(x, raw, B, C, -1.0, cu_seqlens=cu)
+    assert y.shape == (1, 25, H, 2 * P)
+    for s in range(3):
+        a, b = cu[s], cu[s + 1]
+        np.testing.assert_allclose(y[0, a:b, :, :P], _quadratic_form(
+            x[0, a:b], raw[0, a:b], B[0, a:b], C[0, a:b], -1.0), rtol=1e-11, atol=1e-13)
+        np.testing.assert_allclose(y[0, a:b, :, P:], _reverse_quadratic_form(
+            x[0, a:b], raw[0, a:b], B[0, a:b], C[0, a:b], -1.0), rtol=1e-11, atol=1e-13)
+
+
+def test_bidirectional_reversal_swaps_halves(oracle_mod):
+    """Reversing every sequence swaps the two directions (and reverses the tokens)."""
+    rng = np.random.default_rng(18)
+    x, raw, B, C = _rand_problem(rng, 2, 14, 2, 3, 4)
+    y, ff, fr = oracle_mod.bidirectional_forward(x, raw, B, C, -0.5)
+    r = lambda a: np.ascontiguousarray(a[:, ::-1])  # noqa: E731
+    y2, ff2, fr2 = oracle_mod.bidirectional_forward(r(x), r(raw), r(B), r(C), -0.5)
+    np.testing.assert_allclose(y2[..., :3], r(y[..., 3:]), rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(y2[..., 3:], r(y[..., :3]), rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(ff2, fr, rtol=1e-12, atol=1e-14)
+
+
+def test_bidirectional_backward_finite_differences(oracle_mod):
+    rng = np.random.default_rng(19)
+    cu = np.array([0, 5, 12], dtype=np.int32)
+    x, raw, B, C = _rand_problem(rng, 1, 12, 2, 2, 3, raw_scale=1.0)
+    dy = rng.standard_normal((1, 12, 2, 4))
+    g = oracle_mod.bidirectional_backward(x, raw, B, C, dy, -1.0, cu_seqlens=cu)
+
+    def loss(x_, raw_, B_, C_):
+        y, _, _ = oracle_mod.bidirectional_forward(x_, raw_, B_, C_, -1.0, cu_seqlens=cu)
+        return float(np.sum(y * dy))
+
+    eps = 1e-6
+    for name, arr, idx in (("dx", x, (0, 3, 1, 0)), ("dx", x, (0, 10, 0, 1)),
+                           ("d_raw_dt", raw, (0, 2, 1)), ("d_raw_dt", raw, (0, 7, 0)),
+                           ("dB", B, (0, 4, 0, 2)), ("dC", C, (0, 9, 0, 1))):
+        hi, lo = arr.copy(), arr.copy()
+        hi[idx] += eps
+        lo[idx] -= eps
+        args_hi = [hi if a is arr else a for a in (x, raw, B, C)]
+        args_lo = [lo if a is arr else a for a in (x, raw, B, C)]
+        fd = (loss(*args_hi) - loss(*args_lo)) / (2 * eps)
+        assert abs(fd - g[name][idx]) <= 1e-7 * max(1.0, abs(fd)), (name, idx, fd, g[name][idx])
