@@ -154,12 +154,13 @@ Layout make_layout(const Prob& b, bool bwd) {
     if (b.tc) {  // one 64 x 64 bf16 tile per chunk slot of every segment and group
         l.l0 = off;
         off = align_up(off + (size_t)8192 * b.nseg_max * (b.Ls / b.Q) * b.G);
-        // one factor record per chunk slot and head
+        // one factor record per chunk slot and head slot of every pair
+        const int npairs = b.G * ((b.H / b.G + 1) / 2);
         l.fac = off;
-        off = align_up(off + sizeof(float) * kFacRec * b.nseg_max * (b.Ls / b.Q) * b.H);
+        off = align_up(off + sizeof(float) * kFacRec * b.nseg_max * (b.Ls / b.Q) * 2 * npairs);
         // one fallback flag per (segment, head pair)
         l.fb = off;
-        off = align_up(off + sizeof(int) * b.nseg_max * (b.H / 2));
+        off = align_up(off + sizeof(int) * b.nseg_max * npairs);
     }
     l.adj = l.rq = l.rqsuf = l.dbacc = l.dcacc = l.rtok = l.kfin = l.cb32 = 0;
     if (bwd) {
@@ -221,6 +222,10 @@ Args make_args(const Prob& b, const Layout& l, void* ws) {
     a.P = b.P;
     a.N = b.N;
     a.G = b.G;
+    a.Hg = b.H / b.G;
+    a.ppg = (a.Hg + 1) / 2;
+    a.npairs = b.G * a.ppg;
+    a.Hf = 2 * a.npairs;
     a.Q = b.Q;
     a.Ls = b.Ls;
     a.delta_init = b.delta_init;

@@ -98,10 +98,33 @@ struct Args {
     long long T, rowlen;
     long long nseg_max;
     int nseq, H, P, N, G, Q, Ls;
+    // Tensor-core work items take heads in pairs inside a B/C group: Hg = H / G heads per
+    // group, ppg = (Hg + 1) / 2 pairs per group, npairs = G ppg.  With Hg odd, a group's
+    // last pair has one head; its second slot is a dummy (zero x / dy tiles, zero factor
+    // records, nothing written).  Factor records are kept per pair slot: Hf = 2 npairs
+    // records per chunk (= H when Hg is even).
+    int Hg, ppg, npairs, Hf;
     float delta_init;
     int dtype;
     int state_lm;   // A and adj stored lane-major (tensor-core path), see lm_row
 };
+
+// The heads of tensor-core pair p.
+struct HeadPair {
+    int h0;    // first head
+    int g;     // B / C group
+    bool v1;   // the second slot holds head h0 + 1
+    int h1c;   // tile coordinate of the second slot: h0 + 1, or H (outside: zero tiles)
+};
+__host__ __device__ __forceinline__ HeadPair head_pair(const Args& a, int p) {
+    HeadPair r;
+    r.g = p / a.ppg;
+    const int j = p - r.g * a.ppg;
+    r.h0 = r.g * a.Hg + 2 * j;
+    r.v1 = 2 * j + 1 < a.Hg;
+    r.h1c = r.v1 ? r.h0 + 1 : a.H;
+    return r;
+}
 
 // Segment states A / adj of one (segment, head) are P x N fp32.  The SIMT path keeps
 // them row-major.  The tensor-core path keeps them lane-major: in each block of 32

@@ -90,7 +90,7 @@ __global__ void __launch_bounds__(kTableThreads) seg_table_kernel(Args a) {
     // tensor-core path: no work item falls back to the SIMT evaluation until the chunk
     // factors say so
     if (a.fb)
-        for (long long i = tid; i < a.nseg_max * (a.H / 2); i += blockDim.x) a.fb[i] = 0;
+        for (long long i = tid; i < a.nseg_max * a.npairs; i += blockDim.x) a.fb[i] = 0;
     for (int s0 = 0; s0 < a.nseq; s0 += blockDim.x) {
         const int s = s0 + tid;
         long long start = 0;

@@ -39,30 +39,33 @@ namespace {
 // Work items (segment, pair of heads) with a chunk whose delta sum exceeds kMaxChunkDecay
 // run the SIMT recurrence on the first simt::kSimtThreads threads of the CTA.
 template <int N>
-__device__ __forceinline__ void fallback_seg_state(const Args& a, int seg, int h0, float* sm,
-                                                int bar, int mode) {
+__device__ __forceinline__ void fallback_seg_state(const Args& a, int seg, int p, float* sm,
+                                                   int bar, int mode) {
     const simt::Ctx cx{(int)threadIdx.x, bar};
-    for (int hh = 0; hh < 2; ++hh) {
+    const HeadPair hp = head_pair(a, p);
+    for (int hh = 0; hh < (hp.v1 ? 2 : 1); ++hh) {
         if (mode == 0)
-            simt::seg_state_body<__nv_bfloat16, kP / 8, N / 32>(a, seg, h0 + hh, sm, cx);
+            simt::seg_state_body<__nv_bfloat16, kP / 8, N / 32>(a, seg, hp.h0 + hh, sm, cx);
         else
-            simt::adj_state_body<__nv_bfloat16, kP / 8, N / 32>(a, seg, h0 + hh, sm, cx);
+            simt::adj_state_body<__nv_bfloat16, kP / 8, N / 32>(a, seg, hp.h0 + hh, sm, cx);
         cx.sync();
     }
 }
 template <int N>
-__device__ __forceinline__ void fallback_walk(const Args& a, int seg, int h0, float* sm, int bar) {
+__device__ __forceinline__ void fallback_walk(const Args& a, int seg, int p, float* sm, int bar) {
     const simt::Ctx cx{(int)threadIdx.x, bar};
-    for (int hh = 0; hh < 2; ++hh) {
-        simt::seg_walk_body<__nv_bfloat16, kP / 8, N / 32>(a, seg, h0 + hh, sm, cx);
+    const HeadPair hp = head_pair(a, p);
+    for (int hh = 0; hh < (hp.v1 ? 2 : 1); ++hh) {
+        simt::seg_walk_body<__nv_bfloat16, kP / 8, N / 32>(a, seg, hp.h0 + hh, sm, cx);
         cx.sync();
     }
 }
 template <int N>
-__device__ __forceinline__ void fallback_bwd(const Args& a, int seg, int h0, float* sm, int bar) {
+__device__ __forceinline__ void fallback_bwd(const Args& a, int seg, int p, float* sm, int bar) {
     const simt::Ctx cx{(int)threadIdx.x, bar};
-    for (int hh = 0; hh < 2; ++hh) {
-        simt::bwd_walk_body<__nv_bfloat16, kP / 8, N / 32>(a, seg, h0 + hh, sm, cx, true);
+    const HeadPair hp = head_pair(a, p);
+    for (int hh = 0; hh < (hp.v1 ? 2 : 1); ++hh) {
+        simt::bwd_walk_body<__nv_bfloat16, kP / 8, N / 32>(a, seg, hp.h0 + hh, sm, cx, true);
         cx.sync();
     }
 }
@@ -105,16 +108,18 @@ __global__ void __launch_bounds__(kStateThreads, 3)
         }
     }
     const int seg = blockIdx.x;
-    const int h0 = blockIdx.y * 2;
+    const int pr = blockIdx.y;
+    const HeadPair hp = head_pair(a, pr);
+    const int h0 = hp.h0;
     if (seg >= a.hdr->nseg) return;
-    if (a.fb[(long long)seg * (a.H / 2) + blockIdx.y]) {
+    if (a.fb[(long long)seg * a.npairs + pr]) {
         // a chunk decay beyond the factorisation's range: the SIMT recurrence, both heads
         extern __shared__ float fsm[];
-        if (threadIdx.x < simt::kSimtThreads) fallback_seg_state<N>(a, seg, h0, fsm, 3, MODE);
+        if (threadIdx.x < simt::kSimtThreads) fallback_seg_state<N>(a, seg, pr, fsm, 3, MODE);
         return;
     }
     const SegInfo si = a.segtab[seg];
-    const int g = h0 / (a.H / a.G);
+    const int g = hp.g;
     const int nchunks = (si.len + kQ - 1) / kQ;
     constexpr int SB = StateSmem::stage_bytes(N);
 
@@ -162,7 +167,7 @@ __global__ void __launch_bounds__(kStateThreads, 3)
                 const int tok = (int)(si.start + (long long)c * kQ);
                 mbar_expect_tx(&full[s], SB);
                 tma_load_3d(st, &map_x, &full[s], 0, h0, tok);
-                tma_load_3d(st + 8192, &map_x, &full[s], 0, h0 + 1, tok);
+                tma_load_3d(st + 8192, &map_x, &full[s], 0, hp.h1c, tok);
                 for (int nb = 0; nb < N / 64; ++nb)
                     tma_load_3d(st + 16384 + nb * 8192, &map_b, &full[s], nb * 64, g, tok);
             }
@@ -199,7 +204,7 @@ __global__ void __launch_bounds__(kStateThreads, 3)
         if (ct < 32) {
             const int head = ct >> 4, c = ct & 15;
             const float hv = (c < nchunks)
-                                 ? a.fac[((long long)(seg * cps + c) * a.H + h0 + head) * kFacRec + FAC_HALF]
+                                 ? a.fac[((long long)(seg * cps + c) * a.Hf + 2 * pr + head) * kFacRec + FAC_HALF]
                                  : 0.f;
             // inclusive prefix over the head's 16 chunks (lanes 16 head .. 16 head + 15)
             float pre = hv;
@@ -210,7 +215,8 @@ __global__ void __launch_bounds__(kStateThreads, 3)
             }
             const float tot = __shfl_sync(0xffffffffu, pre, 15, 16);
             csc[head * 16 + c] = MODE == 0 ? expf(-hv - 2.f * (tot - pre)) : expf(-hv - 2.f * (pre - hv));
-            if (MODE == 0 && c == 0) a.lam[(long long)seg * a.H + h0 + head] = -2.f * tot;
+            if (MODE == 0 && c == 0 && (head == 0 || hp.v1))
+                a.lam[(long long)seg * a.H + h0 + head] = -2.f * tot;
         }
         named_sync(2, 256);
         {
@@ -219,7 +225,7 @@ __global__ void __launch_bounds__(kStateThreads, 3)
 #pragma unroll
             for (int k = 0; k < 2 * kMaxSeg / 256; ++k) {
                 const int i = ct + 256 * k, head = i >> 10, t = min(i & (kMaxSeg - 1), si.len - 1);
-                v[k] = __ldg(a.fac + ((long long)(seg * cps + (t >> 6)) * a.H + h0 + head) * kFacRec +
+                v[k] = __ldg(a.fac + ((long long)(seg * cps + (t >> 6)) * a.Hf + 2 * pr + head) * kFacRec +
                              (MODE == 0 ? FAC_G : FAC_F) + (t & 63));
             }
 #pragma unroll
@@ -260,7 +266,7 @@ __global__ void __launch_bounds__(kStateThreads, 3)
             uint32_t v[16];
             tmem_ld16(tmem + ((uint32_t)(32 * q) << 16) + c0, v);
             tmem_wait_ld_regs<16>(v);
-            if (ok) {
+            if (ok && ((r >> 6) == 0 || hp.v1)) {  // nothing for a dummy second slot
 #pragma unroll
                 for (int i = 0; i < 16; i += 4)
                     *reinterpret_cast<float4*>(Arow + (c0 + i) * 32) =
@@ -435,39 +441,48 @@ __global__ void __launch_bounds__(kFacThreads) tc_factors_kernel(Args a) {
     if (seg >= a.hdr->nseg) return;
     const SegInfo si = a.segtab[seg];
     if (c >= (si.len + kQ - 1) / kQ) return;
-    __shared__ float zt[kFacHeads][kQ + 1];  // raw_dt + delta_init, [head][token]
+    __shared__ float zt[kFacHeads][kQ + 1];  // raw_dt + delta_init, [record slot][token]
     const int ct = threadIdx.x, lane = ct & 31, warp = ct >> 5;
+    // record slots hb .. hb + kFacHeads - 1: slot r is lane r % 2 of pair r / 2 (a dummy
+    // slot gets an all-zero record)
     const int hb = blockIdx.y * kFacHeads;
+    auto head_of = [&](int r) -> int {
+        const HeadPair hp = head_pair(a, r >> 1);
+        return ((r & 1) == 0 || hp.v1) ? hp.h0 + (r & 1) : -1;
+    };
     const int vc = min(kQ, si.len - c * kQ);
     const long long tok0 = si.start + (long long)c * kQ;
 #pragma unroll
     for (int k = 0; k < kQ * kFacHeads / kFacThreads; ++k) {
         const int idx = ct + kFacThreads * k, t = idx / kFacHeads, hh = idx % kFacHeads;
         float z = 0.f;
-        if (t < vc && hb + hh < a.H) z = a.raw[(tok0 + t) * a.H + hb + hh] + a.delta_init;
+        const int h = (hb + hh < a.Hf) ? head_of(hb + hh) : -1;
+        if (t < vc && h >= 0) z = a.raw[(tok0 + t) * a.H + h] + a.delta_init;
         zt[hh][t] = z;
     }
     __syncthreads();
-    for (int hh = warp; hh < kFacHeads && hb + hh < a.H; hh += kFacThreads / 32) {
-        const int h = hb + hh, t0 = 2 * lane;
-        const float d0 = (t0 < vc) ? softplus_f(zt[hh][t0]) : 0.f;
-        const float d1 = (t0 + 1 < vc) ? softplus_f(zt[hh][t0 + 1]) : 0.f;
+    for (int hh = warp; hh < kFacHeads && hb + hh < a.Hf; hh += kFacThreads / 32) {
+        const int r = hb + hh, t0 = 2 * lane;
+        const bool real = head_of(r) >= 0;
+        const float d0 = (real && t0 < vc) ? softplus_f(zt[hh][t0]) : 0.f;
+        const float d1 = (real && t0 + 1 < vc) ? softplus_f(zt[hh][t0 + 1]) : 0.f;
         const float incl = warp_scan(d0 + d1, lane);
         float excl = __shfl_up_sync(0xffffffffu, incl, 1);
         if (lane == 0) excl = 0.f;
         const float send = __shfl_sync(0xffffffffu, incl, 31);  // sum of delta over the chunk
         const float half = 0.5f * send;
         const float s0 = excl + d0, s1 = s0 + d1;  // inclusive sums at tokens t0, t0 + 1
-        float* rec = a.fac + ((long long)(seg * cps + c) * a.H + h) * kFacRec;
+        float* rec = a.fac + ((long long)(seg * cps + c) * a.Hf + r) * kFacRec;
         *reinterpret_cast<float2*>(rec + FAC_F + t0) =
-            make_float2((t0 < vc) ? expf(half - s0) : 0.f, (t0 + 1 < vc) ? expf(half - s1) : 0.f);
+            make_float2((real && t0 < vc) ? expf(half - s0) : 0.f,
+                        (real && t0 + 1 < vc) ? expf(half - s1) : 0.f);
         *reinterpret_cast<float2*>(rec + FAC_G + t0) =
             make_float2(d0 * expf(s0 - half), d1 * expf(s1 - half));
         *reinterpret_cast<float2*>(rec + FAC_D + t0) = make_float2(d0, d1);
         if (lane < 4) rec[FAC_HALF + lane] = (lane == 0) ? half : 0.f;
         // beyond this decay the factors would leave fp32 range: the (segment, head pair)
         // is evaluated by the SIMT recurrence instead (every writer stores the same 1)
-        if (lane == 0 && !(send <= kMaxChunkDecay)) a.fb[(long long)seg * (a.H / 2) + h / 2] = 1;
+        if (lane == 0 && !(send <= kMaxChunkDecay)) a.fb[(long long)seg * a.npairs + (r >> 1)] = 1;
     }
 }
 
@@ -523,19 +538,24 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
     // role walks the same items; rings and mbarrier phases run on the CTA's global chunk
     // count gc, so the next item's copies start while the current item's last chunks run.
     const int nseg = a.hdr->nseg;
-    const int npairs = a.H / 2;
+    const int npairs = a.npairs;
     const int nitems = nseg * npairs;
     if ((int)blockIdx.x >= nitems) return;
     const int cps = a.Ls / kQ;
     struct Item {
-        int seg, h0, g, nchunks;
+        int seg, p, h0, h1c, g, nchunks;
+        bool v1;
         SegInfo si;
     };
     auto item_of = [&](int it) -> Item {
         Item r;
         r.seg = it / npairs;
-        r.h0 = (it % npairs) * 2;
-        r.g = r.h0 / (a.H / a.G);
+        r.p = it % npairs;
+        const HeadPair hp = head_pair(a, r.p);
+        r.h0 = hp.h0;
+        r.h1c = hp.h1c;
+        r.v1 = hp.v1;
+        r.g = hp.g;
         r.si = a.segtab[r.seg];
         r.nchunks = (r.si.len + kQ - 1) / kQ;
         return r;
@@ -617,7 +637,7 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
                     }
                     mbar_expect_tx(&fac_full[fs], kFSlot);
                     bulk_load(sm + Lay::OFF_F + fs * kFSlot,
-                              a.fac + ((long long)(I.seg * cps + c) * a.H + I.h0) * kFacRec, kFSlot,
+                              a.fac + ((long long)(I.seg * cps + c) * a.Hf + 2 * I.p) * kFacRec, kFSlot,
                               &fac_full[fs]);
                     const int xs = gc % kXS;
                     if (gc >= kXS &&
@@ -628,7 +648,7 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
                     unsigned char* sx = sm + Lay::OFF_X + xs * Lay::XSLOT;
                     mbar_expect_tx(&full_x[xs], Lay::XSLOT);
                     tma_load_3d(sx, &map_x, &full_x[xs], 0, I.h0, tok);
-                    tma_load_3d(sx + 8192, &map_x, &full_x[xs], 0, I.h0 + 1, tok);
+                    tma_load_3d(sx + 8192, &map_x, &full_x[xs], 0, I.h1c, tok);
                     const int b = gc & 1;
                     if (gc >= 2 &&
                         !wait_or_abort(&empty_bc[b], ((gc >> 1) - 1) & 1, abort_flag, a.hdr)) {
@@ -797,7 +817,7 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
                             tc_fence_before();
                             mbar_arrive(&y_free[s]);
                         }
-                        if (ok && tt < vc) {
+                        if (ok && tt < vc && (hf == 0 || I.v1)) {
                             store_bf16x16(dst + (j >> 3), v, fv, wide);
                             store_bf16x16(dst + ((j + 16) >> 3), v + 16, fv, wide);
                         }
@@ -840,9 +860,11 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
                     wait_or_abort(&fac_full[gc % kFS], (gc / kFS) & 1, abort_flag, a.hdr);
                     if (gc >= 2)
                         wait_or_abort(&h_free[gc & 1], ((gc - 2) >> 1) & 1, abort_flag, a.hdr);
-                    const float sc0 = expf(-frec(gc % kFS, rh)[FAC_HALF]);  // exp(m_0)
+                    // exp(m_0); a dummy second slot starts (and stays) at zero
+                    const float sc0 = (rh == 0 || I.v1) ? expf(-frec(gc % kFS, rh)[FAC_HALF]) : 0.f;
                     const float* Hin =
-                        a.A + ((long long)I.seg * a.H + I.h0 + rh) * kP * N + lm_row(rp, N) + n0 * 32;
+                        a.A + ((long long)I.seg * a.H + I.h0 + (I.v1 ? rh : 0)) * kP * N +
+                        lm_row(rp, N) + n0 * 32;
 #pragma unroll
                     for (int c0 = 0; c0 < NH; c0 += 32) {
                         float h[32];
@@ -912,10 +934,10 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
 template <int N>
 __global__ void __launch_bounds__(simt::kSimtThreads) tc_fallback_walk_kernel(Args a) {
     extern __shared__ float fsm[];
-    const int npairs = a.H / 2;
+    const int npairs = a.npairs;
     const int nitems = a.hdr->nseg * npairs;
     for (int it = blockIdx.x; it < nitems; it += gridDim.x)
-        if (a.fb[it]) fallback_walk<N>(a, it / npairs, (it % npairs) * 2, fsm, 1);
+        if (a.fb[it]) fallback_walk<N>(a, it / npairs, it % npairs, fsm, 1);
 }
 
 // ================================================================ backward walks
@@ -982,13 +1004,13 @@ struct ChunkFactors {
 struct FacVals {
     float f, g, d, half;
 };
-__device__ __forceinline__ FacVals load_fac_vals(const Args& a, int seg, int h0, int cc,
+__device__ __forceinline__ FacVals load_fac_vals(const Args& a, int seg, int pr, int cc,
                                                  int nchunks, int ct) {
     FacVals v = {0.f, 0.f, 0.f, 0.f};
     if (ct < 128 && cc >= 0 && cc < nchunks) {
         const int head = ct >> 6, t = ct & 63;
         const float* rec =
-            a.fac + ((long long)(seg * (a.Ls / kQ) + cc) * a.H + h0 + head) * kFacRec;
+            a.fac + ((long long)(seg * (a.Ls / kQ) + cc) * a.Hf + 2 * pr + head) * kFacRec;
         v.f = rec[FAC_F + t];
         v.g = rec[FAC_G + t];
         v.d = rec[FAC_D + t];
@@ -1125,12 +1147,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                      const __grid_constant__ CUtensorMap map_acc, Args a) {
     using Lay = BwdLayout<N>;
     const int seg = blockIdx.x;
-    const int h0 = blockIdx.y * 2;
+    const int pr = blockIdx.y;
+    const HeadPair hp = head_pair(a, pr);
+    const int h0 = hp.h0;
     if (seg >= a.hdr->nseg) return;
     // an item beyond the factorisation's range: the dx/dB walk's SIMT evaluation adds dC
-    if (a.fb[(long long)seg * (a.H / 2) + blockIdx.y]) return;
+    if (a.fb[(long long)seg * a.npairs + pr]) return;
     const SegInfo si = a.segtab[seg];
-    const int g = h0 / (a.H / a.G);
+    const int g = hp.g;
     const int nchunks = (si.len + kQ - 1) / kQ;
     // a sequence's last segment under an upstream final-state gradient: this walk also
     // forms the final state and writes <d final_state, final state> per head (kfin)
@@ -1223,9 +1247,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 const int tok = (int)(si.start + (long long)c * kQ);
                 mbar_expect_tx(&full[s], Lay::STAGE);
                 tma_load_3d(st, &map_x, &full[s], 0, h0, tok);
-                tma_load_3d(st + 8192, &map_x, &full[s], 0, h0 + 1, tok);
+                tma_load_3d(st + 8192, &map_x, &full[s], 0, hp.h1c, tok);
                 tma_load_3d(st + 16384, &map_dy, &full[s], 0, h0, tok);
-                tma_load_3d(st + 24576, &map_dy, &full[s], 0, h0 + 1, tok);
+                tma_load_3d(st + 24576, &map_dy, &full[s], 0, hp.h1c, tok);
                 for (int nb = 0; nb < N / 64; ++nb) {
                     tma_load_3d(st + 32768 + nb * 8192, &map_b, &full[s], nb * 64, g, tok);
                     tma_load_3d(st + 32768 + N * 128 + nb * 8192, &map_c, &full[s], nb * 64, g,
@@ -1304,11 +1328,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const uint32_t tq = tmem + ((uint32_t)(32 * q) << 16);
         float Hs[NH];
 
-        bwd_factors(F, load_fac_vals(a, seg, h0, 0, nchunks, ct), 0, ct);
+        bwd_factors(F, load_fac_vals(a, seg, pr, 0, nchunks, ct), 0, ct);
         {
-            const float sc0 = expf(-F.scal[(0 * 2 + rh) * 4 + 0]);
-            const float* Hin =
-                a.A + ((long long)seg * a.H + h0 + rh) * kP * N + lm_row(rp, N) + n0 * 32;
+            // a dummy second slot starts (and stays) at zero
+            const float sc0 = (rh == 0 || hp.v1) ? expf(-F.scal[(0 * 2 + rh) * 4 + 0]) : 0.f;
+            const float* Hin = a.A + ((long long)seg * a.H + h0 + (hp.v1 ? rh : 0)) * kP * N +
+                               lm_row(rp, N) + n0 * 32;
 #pragma unroll
             for (int i = 0; i < NH; i += 4) {
                 const float4 v = *reinterpret_cast<const float4*>(Hin + i * 32);
@@ -1339,7 +1364,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             const int vc = min(kQ, si.len - c * kQ);
             const long long tok0 = si.start + (long long)c * kQ;
             unsigned char* st = sm + Lay::OFF_STAGE + s * Lay::STAGE;
-            const FacVals fac_next = load_fac_vals(a, seg, h0, c + 1, nchunks, ct);
+            const FacVals fac_next = load_fac_vals(a, seg, pr, c + 1, nchunks, ct);
             // B: W_h = P1_h masked to s <= t (warpgroup h handles head h), and two in-chunk
             // sums of row t for the delta gradient:
             //   ri_t = sum_s W_h[t, s] C_t . B_s, the part of r_t from the chunk's own tokens
@@ -1400,7 +1425,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 tc_fence_after();
                 const float gend = expf(-F.scal[(s * 2 + rh) * 4]);
                 const float* dT =
-                    a.dhT + (((long long)si.seq * a.H + h0 + rh) * kP + rp) * N + n0;
+                    a.dhT + (((long long)si.seq * a.H + h0 + (hp.v1 ? rh : 0)) * kP + rp) * N + n0;
                 float kp = 0.f;
 #pragma unroll
                 for (int c0 = 0; c0 < NH; c0 += 32) {
@@ -1420,10 +1445,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 tc_fence_before();
                 mbar_arrive(s_free);
                 kp = warp_sum(kp);
-                if (lane == 0) F.red[wg * 4 + q] = ok ? kp : 0.f;
+                if (lane == 0) F.red[wg * 4 + q] = (ok && (rh == 0 || hp.v1)) ? kp : 0.f;
                 named_sync(1, kCT);
                 // quadrants 0-1 hold head 0, 2-3 head 1; both warpgroups hold column halves
-                if (ct < 2)
+                if (ct < (hp.v1 ? 2 : 1))
                     a.kfin[(long long)seg * a.H + h0 + ct] =
                         (F.red[2 * ct] + F.red[2 * ct + 1]) + (F.red[4 + 2 * ct] + F.red[5 + 2 * ct]);
             } else {
@@ -1496,8 +1521,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 if (wg == 0 && hf == 0 && t < vc && ok) {
                     a.rtok[(tok0 + t) * a.H + h0] =
                         (rpart[0 * 64 + t] + rpart[2 * 64 + t]) - rint[t];
-                    a.rtok[(tok0 + t) * a.H + h0 + 1] =
-                        (rpart[1 * 64 + t] + rpart[3 * 64 + t]) - rint[64 + t];
+                    if (hp.v1)
+                        a.rtok[(tok0 + t) * a.H + h0 + 1] =
+                            (rpart[1 * 64 + t] + rpart[3 * 64 + t]) - rint[64 + t];
                 }
             }
             named_sync(1, kCT);  // rpart reuse
@@ -1546,17 +1572,19 @@ __global__ void __launch_bounds__(kDxThreads, 1)
                        const __grid_constant__ CUtensorMap map_acc, Args a) {
     using Lay = DxLayout<N>;
     const int seg = blockIdx.x;
-    const int h0 = blockIdx.y * 2;
+    const int pr = blockIdx.y;
+    const HeadPair hpr = head_pair(a, pr);
+    const int h0 = hpr.h0;
     if (seg >= a.hdr->nseg) return;
-    if (a.fb[(long long)seg * (a.H / 2) + blockIdx.y]) {
+    if (a.fb[(long long)seg * a.npairs + pr]) {
         // a chunk decay beyond the factorisation's range: the SIMT recurrence for both heads
         // (dx, dB and dC added into the accumulators, the finished d_raw_dt)
         extern __shared__ float fsm[];
-        if (threadIdx.x < simt::kSimtThreads) fallback_bwd<N>(a, seg, h0, fsm, 10);
+        if (threadIdx.x < simt::kSimtThreads) fallback_bwd<N>(a, seg, pr, fsm, 10);
         return;
     }
     const SegInfo si = a.segtab[seg];
-    const int g = h0 / (a.H / a.G);
+    const int g = hpr.g;
     const int nchunks = (si.len + kQ - 1) / kQ;
 
     extern __shared__ __align__(1024) unsigned char smraw[];
@@ -1639,7 +1667,7 @@ __global__ void __launch_bounds__(kDxThreads, 1)
                 const int fs = j % kDFS, cc = nchunks - 1 - j;
                 mbar_expect_tx(&fac_full[fs], kFSlot);
                 bulk_load(sm + Lay::OFF_F + fs * kFSlot,
-                          a.fac + ((long long)(seg * cps + cc) * a.H + h0) * kFacRec, kFSlot,
+                          a.fac + ((long long)(seg * cps + cc) * a.Hf + 2 * pr) * kFacRec, kFSlot,
                           &fac_full[fs]);
             };
             for (int j = 0; j < 2 && j < nchunks; ++j) load_fac(j);
@@ -1651,9 +1679,9 @@ __global__ void __launch_bounds__(kDxThreads, 1)
                 const int tok = (int)(si.start + (long long)c * kQ);
                 mbar_expect_tx(&full[s], Lay::STAGE);
                 tma_load_3d(st, &map_x, &full[s], 0, h0, tok);
-                tma_load_3d(st + 8192, &map_x, &full[s], 0, h0 + 1, tok);
+                tma_load_3d(st + 8192, &map_x, &full[s], 0, hpr.h1c, tok);
                 tma_load_3d(st + 16384, &map_dy, &full[s], 0, h0, tok);
-                tma_load_3d(st + 24576, &map_dy, &full[s], 0, h0 + 1, tok);
+                tma_load_3d(st + 24576, &map_dy, &full[s], 0, hpr.h1c, tok);
                 for (int nb = 0; nb < N / 64; ++nb) {
                     tma_load_3d(st + 32768 + nb * 8192, &map_b, &full[s], nb * 64, g, tok);
                     tma_load_3d(st + 32768 + N * 128 + nb * 8192, &map_c, &full[s], nb * 64, g,
@@ -1795,7 +1823,7 @@ __global__ void __launch_bounds__(kDxThreads, 1)
             wait_or_abort(kseg_ready, 0, abort_flag, a.hdr);
             // a sequence's last segment: <d final_state, final state>, from the dC walk
             const float kseg = ((si.flags & SEG_LAST) && a.dhT)
-                                   ? a.kfin[(long long)seg * a.H + h0 + hf]
+                                   ? ((hf == 0 || hpr.v1) ? a.kfin[(long long)seg * a.H + h0 + hf] : 0.f)
                                    : (red[8 + 2 * hf] + red[9 + 2 * hf]) +
                                          (red[12 + 2 * hf] + red[13 + 2 * hf]);
             for (int it = 0; it < nchunks; ++it) {
@@ -1803,7 +1831,8 @@ __global__ void __launch_bounds__(kDxThreads, 1)
                 const int s = it & 1, sl = it % kDFS;
                 const int vc = min(kQ, si.len - c * kQ);
                 const long long tok0 = si.start + (long long)c * kQ;
-                const float rv = (tt < vc) ? rtok[(tok0 + tt) * a.H + h0 + hf] : 0.f;
+                const bool real = hf == 0 || hpr.v1;  // this thread's head slot holds a head
+                const float rv = (tt < vc && real) ? rtok[(tok0 + tt) * a.H + h0 + hf] : 0.f;
                 {
                 // P2 of both heads masked to u >= t, bf16 into P2M once dB of the previous
                 // chunk has read it (thread (token tt, column half hf) of each tile)
@@ -1856,7 +1885,7 @@ __global__ void __launch_bounds__(kDxThreads, 1)
                     // this warpgroup is done with the stage's xg rows
                     if (j == 32) mbar_arrive(&empty[s]);
                     if (ok) {
-                        if (tt < vc) {
+                        if (tt < vc && real) {
 #pragma unroll
                             for (int e = 0; e < 32; e += 8)
                                 *reinterpret_cast<uint4*>(dxrow + j + e) = make_uint4(
@@ -1888,7 +1917,7 @@ __global__ void __launch_bounds__(kDxThreads, 1)
                 }
                 named_sync(6, 128);  // rqs is rewritten by the next chunk
                 suf += later;
-                if (ok && tt < vc)
+                if (ok && tt < vc && real)
                     a.draw[(tok0 + tt) * a.H + h0 + hf] =
                         -expm1f(-dt) * (xgb - (carry + suf + kseg));
                 carry += tot;
@@ -1922,12 +1951,14 @@ __global__ void __launch_bounds__(kDxThreads, 1)
                 // the quadratic form with one end in or before this segment and the other
                 // after it (both states from the fp32 scans)
                 wait_or_abort(&fac_full[0], 0, abort_flag, a.hdr);
-                const float sc = expf(-frec(0, rh)[FAC_HALF]);
-                const float* Gin =
-                    a.adj + ((long long)seg * a.H + h0 + rh) * kP * N + lm_row(rp, N) + n0 * 32;
-                const bool more = !(si.flags & SEG_LAST);
-                const float* Hend =
-                    a.A + ((long long)(seg + 1) * a.H + h0 + rh) * kP * N + lm_row(rp, N) + n0 * 32;
+                // a dummy second slot starts (and stays) at zero, with no boundary term
+                const bool realr = rh == 0 || hpr.v1;
+                const float sc = realr ? expf(-frec(0, rh)[FAC_HALF]) : 0.f;
+                const float* Gin = a.adj + ((long long)seg * a.H + h0 + (hpr.v1 ? rh : 0)) * kP * N +
+                                   lm_row(rp, N) + n0 * 32;
+                const bool more = !(si.flags & SEG_LAST) && realr;
+                const float* Hend = a.A + ((long long)(seg + 1) * a.H + h0 + (hpr.v1 ? rh : 0)) * kP * N +
+                                    lm_row(rp, N) + n0 * 32;
                 float kp = 0.f;
 #pragma unroll
                 for (int c0 = 0; c0 < NH; c0 += 16) {
@@ -2070,7 +2101,7 @@ cudaError_t launch_l0(const Prob& pb, const Args& a, Launch& L, const CUtensorMa
 }
 
 cudaError_t launch_factors(const Prob& pb, const Args& a, Launch& L) {
-    const dim3 grid((unsigned)(pb.nseg_max * (pb.Ls / kQ)), (pb.H + kFacHeads - 1) / kFacHeads);
+    const dim3 grid((unsigned)(pb.nseg_max * (pb.Ls / kQ)), (a.Hf + kFacHeads - 1) / kFacHeads);
     L.begin("tc_factors");
     tc_factors_kernel<<<grid, kFacThreads, 0, L.stream>>>(a);
     return L.end();
@@ -2086,7 +2117,7 @@ cudaError_t forward_n(const Prob& pb, const Args& a, Launch& L) {
     if (e != cudaSuccess) return e;
     if ((e = launch_l0<N>(pb, a, L, mb, mc)) != cudaSuccess) return e;
     if ((e = launch_factors(pb, a, L)) != cudaSuccess) return e;
-    const dim3 grid((unsigned)pb.nseg_max, pb.H / 2);
+    const dim3 grid((unsigned)pb.nseg_max, a.npairs);
     e = set_smem(tc_seg_state_kernel<N, 0>, state_smem_bytes(N));
     if (e != cudaSuccess) return e;
     L.begin("tc_fwd_state");
@@ -2098,7 +2129,7 @@ cudaError_t forward_n(const Prob& pb, const Args& a, Launch& L) {
     e = set_smem(tc_fwd_walk_kernel<N>, WalkLayout<N>::TOTAL);
     if (e != cudaSuccess) return e;
     // persistent: one CTA per SM, each walking items (segment, pair of heads)
-    const long long items = pb.nseg_max * (pb.H / 2);
+    const long long items = pb.nseg_max * a.npairs;
     const dim3 pgrid((unsigned)(items < sm_count() ? items : sm_count()));
     L.begin("tc_fwd_walk");
     tc_fwd_walk_kernel<N><<<pgrid, kWalkThreads, WalkLayout<N>::TOTAL, L.stream>>>(mx, mb, mc, a);
@@ -2116,7 +2147,7 @@ cudaError_t backward_n(const Prob& pb, const Args& a, Launch& L, bool reuse_forw
         !make_map(&mb, a.B, pb.T, pb.G, N) || !make_map(&mc, a.C, pb.T, pb.G, N) ||
         !make_map_f32(&mdb, a.dbacc, pb.T, pb.G, N) || !make_map_f32(&mdc, a.dcacc, pb.T, pb.G, N))
         return cudaErrorInvalidValue;
-    const dim3 grid((unsigned)pb.nseg_max, pb.H / 2);
+    const dim3 grid((unsigned)pb.nseg_max, a.npairs);
     cudaError_t e;
     if (reuse_forward) {
         // the forward's segment table, tiles, factors and segment states are in the
@@ -2160,8 +2191,10 @@ cudaError_t backward_n(const Prob& pb, const Args& a, Launch& L, bool reuse_forw
 }  // namespace
 
 bool tc_supported(int dtype, int P, int N, int Q, int H, int G) {
+    (void)H;
+    (void)G;
     return dtype == SSD_DTYPE_BF16 && P == kP && (N == 64 || N == 128) && Q == kQ &&
-           ((H / G) % 2) == 0 && encode_fn() != nullptr;
+           encode_fn() != nullptr;
 }
 
 cudaError_t tc_forward(const Prob& pb, const Args& a, Launch& L) {

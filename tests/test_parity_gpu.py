@@ -198,16 +198,33 @@ def test_single_token(ssd, oracle_mod, N, H):
     _bwd_check(ssd, oracle_mod, d, "bf16", -4.6)
 
 
-@pytest.mark.parametrize("H,N,L,expect", [(2, 128, 64, "tensor-core"),
-                                           (24, 64, 100, "tensor-core"),
-                                           (3, 128, 64, "simt"), (2, 128, 63, "simt")])
-def test_dispatch_path(ssd, H, N, L, expect):
-    """bf16, P = 64, chunk 64, an even number of heads per group and at least one chunk's
-    worth of tokens take the tensor cores."""
+@pytest.mark.parametrize("H,G,N,L,expect", [(2, 1, 128, 64, "tensor-core"),
+                                             (24, 1, 64, 100, "tensor-core"),
+                                             (3, 1, 128, 64, "tensor-core"),
+                                             (6, 2, 64, 64, "tensor-core"),
+                                             (2, 1, 128, 63, "simt"), (2, 1, 32, 64, "simt")])
+def test_dispatch_path(ssd, H, G, N, L, expect):
+    """bf16, P = 64, N in {64, 128}, chunk 64 and at least one chunk's worth of tokens take
+    the tensor cores, with any number of heads per B/C group."""
     import torch
     x = torch.empty(1, L, H, 64, dtype=torch.bfloat16, device="cuda")
-    B = torch.empty(1, L, 1, N, dtype=torch.bfloat16, device="cuda")
+    B = torch.empty(1, L, G, N, dtype=torch.bfloat16, device="cuda")
     assert ssd.dispatch_path(ssd.make_problem(x, B, -4.6)) == expect
+
+
+@pytest.mark.parametrize("H,G,N,packed", [(3, 1, 128, False), (6, 2, 64, False),
+                                          (4, 2, 128, False), (5, 5, 64, False),
+                                          (3, 1, 64, True), (6, 2, 128, True)])
+def test_bf16_head_group_layouts(ssd, oracle_mod, monkeypatch, H, G, N, packed):
+    """Tensor-core path with an odd number of heads per group (a group's last pair holds
+    one head), several groups, and one head per group; 4-chunk segments, ragged tail."""
+    monkeypatch.setenv("SSD_SEGMENT_CHUNKS", "4")
+    cu = [0, 333, 334, 1000, 1300] if packed else None
+    d = _draw(17, 1, 1300, H, 64, N, G=G, dtype="bf16", cu=cu)
+    t = to_device(d, "bf16")
+    assert ssd.dispatch_path(ssd.make_problem(t["x"], t["B"], -4.6)) == "tensor-core"
+    _fwd_check(ssd, oracle_mod, d, "bf16", -4.6)
+    _bwd_check(ssd, oracle_mod, d, "bf16", -4.6)
 
 
 def test_long_segments_bf16(ssd, oracle_mod):
