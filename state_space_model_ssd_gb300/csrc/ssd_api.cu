@@ -73,20 +73,26 @@ bool is_pow2_in(int v, int lo, int hi) {
 }
 
 // Segment length: whole chunks, and enough (segment, head) work units to
-// fill the GPU several times over; at most 16 chunks so that the states kept
-// between segments stay small next to the activations.
+// fill the GPU several times over.  Up to 16 chunks as a rule; longer (up to 64)
+// only while the units still fill the GPU 32 times, as on sequences of millions
+// of tokens, where every segment boundary costs a materialised state read and
+// written by each pass (64 x 64 x 4 bytes per head at N = 64 against 4096 tokens
+// of x at 64 chunks).
 int choose_segment_length(long long T, int nseq, int H, int Q) {
-    // SSD_SEGMENT_CHUNKS (1..16) fixes the number of chunks per segment; the
+    // SSD_SEGMENT_CHUNKS (1..64) fixes the number of chunks per segment; the
     // result does not depend on it (tests use it to cover multi-chunk segments
     // at small sizes).
     if (const char* env = getenv("SSD_SEGMENT_CHUNKS")) {
         const int k = atoi(env);
-        if (k >= 1 && k <= 16) return k * Q;
+        if (k >= 1 && k <= 64) return k * Q;
     }
     const long long target_units = 8LL * 152;
     const long long chunks = (T + Q - 1) / Q;
+    const long long extra = nseq > 1 ? nseq : 0;
     int k = 16;
-    while (k > 1 && (chunks / k + (nseq > 1 ? nseq : 0)) * H < target_units) k >>= 1;
+    while (k > 1 && (chunks / k + extra) * H < target_units) k >>= 1;
+    if (k == 16)
+        while (k < 64 && (chunks / (2 * k) + extra) * H >= 4 * target_units) k <<= 1;
     return k * Q;
 }
 

@@ -74,7 +74,7 @@ __device__ __forceinline__ void fallback_bwd(const Args& a, int seg, int p, floa
 // Warps: 0 = TMA producer, 1 = MMA issuer (and TMEM owner), 2..9 = compute.
 constexpr int kStateStages = 2;  // with three CTAs per SM (shared memory and TMEM allow it)
 constexpr int kStateThreads = 320;  // TMA warp, MMA warp, 8 compute warps
-constexpr int kMaxSeg = 1024;  // segment length bound for the per-token weights
+constexpr int kMaxSegChunks = 64;  // chunks per segment the per-chunk scales cover
 
 struct StateSmem {
     // stage = X h0 (8K) | X h1 (8K) | B (N/64 x 8K)
@@ -85,8 +85,6 @@ struct StateSmem {
 //         (operands x, B; also writes the segment log-decay).
 // MODE 1: adjoint aggregates Ad_j = sum_u exp(Lambda_u - Lambda_before) dy_u C_u^T
 //         (operands dy, C).
-constexpr int kWPad = kMaxSeg + kMaxSeg / 16;  // per-head weight row, padded against bank conflicts
-__device__ __forceinline__ int widx(int t) { return t + (t >> 4); }
 
 template <int N, int MODE>
 __global__ void __launch_bounds__(kStateThreads, 3)
@@ -127,9 +125,9 @@ __global__ void __launch_bounds__(kStateThreads, 3)
     unsigned char* sm = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smraw) + 1023) & ~(uintptr_t)1023);
     unsigned char* stages = sm;
-    float* wts = reinterpret_cast<float*>(sm + kStateStages * SB);   // [2][kWPad]
-    float* csc = wts + 2 * kWPad;                                   // [2 head][16 chunk]
-    uint64_t* full = reinterpret_cast<uint64_t*>(csc + 32);
+    float* csc = reinterpret_cast<float*>(sm + kStateStages * SB);  // [2 head][kMaxSegChunks]
+    float* ctot = csc + 2 * kMaxSegChunks;  // [2 head] first 32 chunks, [2 head] all chunks
+    uint64_t* full = reinterpret_cast<uint64_t*>(ctot + 4);
     uint64_t* empty = full + kStateStages;
     uint64_t* ready = empty + kStateStages;
     uint64_t* done = ready + kStateStages;
@@ -199,55 +197,64 @@ __global__ void __launch_bounds__(kStateThreads, 3)
         //              = g(t) exp(-half_c - 2 sum_{chunks c' > c} half_c'),
         //   MODE 1: w_t = exp(-(sum of delta over [start, t]))
         //              = f(t) exp(-half_c - 2 sum_{chunks c' < c} half_c').
+        // The per-chunk scales csc[head][c] come from a scan over the chunks' halves (two
+        // warps per head, 32 chunks each); the record values of a chunk are loaded while
+        // the chunk before it is scaled.
         const int ct = tid - 64;            // 0..255
         const int cps = a.Ls / kQ;
-        if (ct < 32) {
-            const int head = ct >> 4, c = ct & 15;
-            const float hv = (c < nchunks)
-                                 ? a.fac[((long long)(seg * cps + c) * a.Hf + 2 * pr + head) * kFacRec + FAC_HALF]
-                                 : 0.f;
-            // inclusive prefix over the head's 16 chunks (lanes 16 head .. 16 head + 15)
-            float pre = hv;
-#pragma unroll
-            for (int o = 1; o < 16; o <<= 1) {
-                const float nb = __shfl_up_sync(0xffffffffu, pre, o, 16);
-                if ((lane & 15) >= o) pre += nb;
-            }
-            const float tot = __shfl_sync(0xffffffffu, pre, 15, 16);
-            csc[head * 16 + c] = MODE == 0 ? expf(-hv - 2.f * (tot - pre)) : expf(-hv - 2.f * (pre - hv));
+        const long long slot0 = (long long)seg * cps;
+        auto rec = [&](int c, int hh) -> const float* {
+            return a.fac + ((slot0 + c) * a.Hf + 2 * pr + hh) * kFacRec;
+        };
+        float hv = 0.f, pre = 0.f;
+        if (ct < 2 * kMaxSegChunks) {
+            const int head = ct >> 6, c = ct & 63;
+            hv = (c < nchunks) ? rec(c, head)[FAC_HALF] : 0.f;
+            pre = warp_scan(hv, lane);  // inclusive, over this warp's 32 chunks
+            if (lane == 31 && c < 32) ctot[head] = pre;  // the head's first 32 chunks
+        }
+        named_sync(2, 256);
+        if (ct < 2 * kMaxSegChunks) {
+            const int head = ct >> 6, c = ct & 63;
+            if (c >= 32) pre += ctot[head];
+            if (c == 63) ctot[2 + head] = pre;  // the head's total over all chunks
+        }
+        named_sync(2, 256);
+        if (ct < 2 * kMaxSegChunks) {
+            const int head = ct >> 6, c = ct & 63;
+            const float tot = ctot[2 + head];
+            csc[head * kMaxSegChunks + c] =
+                MODE == 0 ? expf(-hv - 2.f * (tot - pre)) : expf(-hv - 2.f * (pre - hv));
             if (MODE == 0 && c == 0 && (head == 0 || hp.v1))
                 a.lam[(long long)seg * a.H + h0 + head] = -2.f * tot;
         }
-        named_sync(2, 256);
-        {
-            // 2 heads x len tokens; loads issued together, index clamped into the segment
-            float v[2 * kMaxSeg / 256];
+        named_sync(2, 256);  // the scales are visible to all compute warps
+        // this thread's 16-byte pieces of the two x tiles: (head slot, row) for i = 0..3
+        float wn[4];
+        auto load_w = [&](int c) {
 #pragma unroll
-            for (int k = 0; k < 2 * kMaxSeg / 256; ++k) {
-                const int i = ct + 256 * k, head = i >> 10, t = min(i & (kMaxSeg - 1), si.len - 1);
-                v[k] = __ldg(a.fac + ((long long)(seg * cps + (t >> 6)) * a.Hf + 2 * pr + head) * kFacRec +
-                             (MODE == 0 ? FAC_G : FAC_F) + (t & 63));
+            for (int i = 0; i < 4; ++i) {
+                const int idx = ct + 256 * i, hh = idx >> 9, row = (idx & 511) >> 3;
+                wn[i] = (c < nchunks && c * kQ + row < si.len)
+                            ? __ldg(rec(c, hh) + (MODE == 0 ? FAC_G : FAC_F) + row)
+                            : 0.f;
             }
-#pragma unroll
-            for (int k = 0; k < 2 * kMaxSeg / 256; ++k) {
-                const int i = ct + 256 * k, head = i >> 10, t = i & (kMaxSeg - 1);
-                if (t < si.len) wts[head * kWPad + widx(t)] = v[k] * csc[head * 16 + (t >> 6)];
-            }
-        }
-        named_sync(2, 256);  // the weights are visible to all compute warps
+        };
+        load_w(0);
         // ---- scale x by the weights in place, chunk by chunk
         for (int c = 0; c < nchunks; ++c) {
             const int s = c % kStateStages;
+            float w[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) w[i] = wn[i];
+            if (c + 1 < nchunks) load_w(c + 1);
             if (!wait_or_abort(&full[s], (c / kStateStages) & 1, abort_flag, a.hdr)) break;
             uint4* xs = reinterpret_cast<uint4*>(stages + s * SB);
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const int idx = ct + 256 * i;  // 0..1023 16-byte chunks of the two x tiles
                 const int hh = idx >> 9;
-                const int row = (idx & 511) >> 3;
-                const int t = c * kQ + row;
-                const float w = (t < si.len) ? wts[hh * kWPad + widx(t)] : 0.f;
-                xs[idx] = scale_chunk(xs[idx], w);
+                xs[idx] = scale_chunk(xs[idx], w[i] * csc[hh * kMaxSegChunks + c]);
             }
             fence_proxy_async();
             mbar_arrive(&ready[s]);
@@ -2067,7 +2074,7 @@ __global__ void __launch_bounds__(kDxThreads, 1)
 }
 
 constexpr int state_smem_bytes(int N) {
-    return kStateStages * StateSmem::stage_bytes(N) + 2 * kWPad * 4 + 32 * 4 + 3 * kStateStages * 8 +
+    return kStateStages * StateSmem::stage_bytes(N) + (2 * kMaxSegChunks + 4) * 4 + 3 * kStateStages * 8 +
            8 + 16 + 1024;
 }
 // three CTAs of the aggregate kernel per SM (1 KB per CTA reserved by the system)

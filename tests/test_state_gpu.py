@@ -133,3 +133,21 @@ def test_many_segments_blocked_scans(ssd, oracle_mod, monkeypatch, dtype, P, N, 
     cu = np.concatenate([[0], np.cumsum(lens)])
     d = _draw(36, int(cu[-1]), H, P, N, dtype, cu=cu)
     _check_all(ssd, oracle_mod, d, dtype, -4.6)
+
+
+@pytest.mark.parametrize("k", [33, 64])
+def test_bf16_long_segments(ssd, oracle_mod, monkeypatch, k):
+    """Segments of 33 and 64 chunks (the longest the aggregate kernels take) on the
+    tensor-core path, a ragged last segment, head 0 at delta ~ 8 (its head pair takes the
+    SIMT recurrence), with initial state and final-state gradient."""
+    monkeypatch.setenv("SSD_SEGMENT_CHUNKS", str(k))
+    d = _draw(37, 9000, 4, 64, 128, "bf16")
+    d["raw_dt"][:, :, 0] += np.float32(12.6)
+    _check_all(ssd, oracle_mod, d, "bf16", -4.6)
+
+
+def test_f32_long_segments(ssd, oracle_mod, monkeypatch):
+    """64-chunk segments on the SIMT path (fp32), two rows."""
+    monkeypatch.setenv("SSD_SEGMENT_CHUNKS", "64")
+    d = _draw(38, 5000, 2, 16, 16, "f32", bsz=2)
+    _check_all(ssd, oracle_mod, d, "f32", -3.0)
