@@ -125,15 +125,18 @@ def kernel_model(name, w):
 
 def measured_traffic(name, w):
     """DRAM bytes per launch of `name` at workload `w`, from the committed ncu summary
-    profiles/dram_traffic_walks_mamba2.8b_16k.txt, or None when there is none or the
-    kernel source changed since it was taken (the summary records the source's sha256)."""
-    path = os.path.join(ROOT, "profiles", "dram_traffic_walks_mamba2.8b_16k.txt")
+    profiles/dram_traffic_walks.txt (a line per kernel and d_state, from one capture on a
+    smaller case), or None when there is none or the kernel source changed since it was
+    taken (the summary records the source's sha256).  Bytes scale with tokens x heads."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic_walks.txt")
     if not os.path.exists(path):
         return None
     import hashlib
     for line in open(path):
         parts = line.split()
-        if len(parts) < 4 or line.startswith("#") or parts[0] != name:
+        if len(parts) < 6 or line.startswith("#") or parts[0] != name:
+            continue
+        if int(parts[5]) != w.dstate:
             continue
         per_token, src, sha = float(parts[1]), parts[2], parts[3]
         srcp = os.path.join(ROOT, src)
@@ -141,8 +144,7 @@ def measured_traffic(name, w):
             return None
         if hashlib.sha256(open(srcp, "rb").read()).hexdigest() != sha:
             return None
-        heads_scale = w.nheads / float(parts[4]) if len(parts) > 4 else 1.0
-        return per_token * w.total_tokens * heads_scale
+        return per_token * w.total_tokens * w.nheads / float(parts[4])
     return None
 
 
