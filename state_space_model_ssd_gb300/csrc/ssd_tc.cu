@@ -935,6 +935,418 @@ __global__ void __launch_bounds__(kWalkThreads, 1)
     if (warp == 1) tmem_dealloc(tmem, 512);
 }
 
+// ---------------------------------------------------------------- the walk at two CTAs an SM
+// N = 64 (the long-sequence workload): the same chunk walk with one Y accumulator, one G3
+// operand buffer, two x slots, four factor record slots and 11 warps, so that two CTAs
+// share each SM (103 KB of shared memory, 256 TMEM columns and 352 threads each) and
+// each hides the other's hand-off latency.  Warps: 0 = TMA producer, 1 = MMA issuer of
+// G4 (onto the state in TMEM), 10 = MMA issuer of G2 and G3, 2..5 = x -> g x of a chunk,
+// then the y epilogue of the chunk before it, 6..9 = the state update and the G3 operand.
+constexpr int kWalk2Threads = 64 + 2 * 128 + 32;
+constexpr int kW2XS = 2;  // x slots
+constexpr int kW2FS = 4;  // factor record slots
+
+struct Walk2Layout {
+    static constexpr int XSLOT = 16384;               // X h0 | X h1
+    static constexpr int BCSLOT = 2 * 64 * 128 + 8192;  // B | C | L0
+    static constexpr int C_IN_BC = 64 * 128;
+    static constexpr int L0_IN_BC = 2 * 64 * 128;
+    static constexpr int OFF_X = 0;
+    static constexpr int OFF_BC = kW2XS * XSLOT;
+    static constexpr int OFF_H = OFF_BC + 2 * BCSLOT;   // 16 KB
+    static constexpr int OFF_F = OFF_H + 16384;
+    static constexpr int OFF_BAR = OFF_F + kW2FS * kFSlot;
+    static constexpr int NBAR = 24;
+    static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+    static constexpr int TOTAL = OFF_MISC + 16 + 1024;
+};
+static_assert(2 * (Walk2Layout::TOTAL + 1024) <= 233472, "two walk CTAs an SM");
+
+__global__ void __launch_bounds__(kWalk2Threads, 2)
+    tc_fwd_walk2_kernel(const __grid_constant__ CUtensorMap map_x,
+                        const __grid_constant__ CUtensorMap map_b,
+                        const __grid_constant__ CUtensorMap map_c, Args a) {
+    constexpr int N = 64;
+    using Lay = Walk2Layout;
+    const int nseg = a.hdr->nseg;
+    const int npairs = a.npairs;
+    const int nitems = nseg * npairs;
+    if ((int)blockIdx.x >= nitems) return;
+    const int cps = a.Ls / kQ;
+    struct Item {
+        int seg, p, h0, h1c, g, nchunks;
+        bool v1;
+        SegInfo si;
+    };
+    auto item_of = [&](int it) -> Item {
+        Item r;
+        r.seg = it / npairs;
+        r.p = it % npairs;
+        const HeadPair hp = head_pair(a, r.p);
+        r.h0 = hp.h0;
+        r.h1c = hp.h1c;
+        r.v1 = hp.v1;
+        r.g = hp.g;
+        r.si = a.segtab[r.seg];
+        r.nchunks = (r.si.len + kQ - 1) / kQ;
+        return r;
+    };
+
+    extern __shared__ __align__(1024) unsigned char smraw[];
+    unsigned char* sm = reinterpret_cast<unsigned char*>(
+        (reinterpret_cast<uintptr_t>(smraw) + 1023) & ~(uintptr_t)1023);
+    auto frec = [&](int sl, int head) -> const float* {
+        return reinterpret_cast<const float*>(sm + Lay::OFF_F + sl * kFSlot) + head * kFacRec;
+    };
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + Lay::OFF_BAR);
+    uint64_t* full_x = bars + 0;      // [2] x of a chunk landed
+    uint64_t* empty_x = bars + 2;     // [2] x read by G4 and G2
+    uint64_t* xg_ready = bars + 4;    // [2] x scaled in place
+    uint64_t* full_bc = bars + 6;     // [2] B, C, L0 landed
+    uint64_t* empty_bc = bars + 8;    // [2] B, C, L0 read by the MMAs
+    uint64_t* y_full = bars + 10;     // Y accumulated
+    uint64_t* y_free = bars + 11;     // Y read by the epilogue
+    uint64_t* h_ready = bars + 12;    // G3 operand written
+    uint64_t* h_free = bars + 13;     // G3 operand read by the MMAs
+    uint64_t* s_full = bars + 14;     // S accumulated onto the state
+    uint64_t* s_free = bars + 15;     // the state rescaled in place
+    uint64_t* fac_full = bars + 16;   // [kW2FS]
+    uint64_t* fac_empty = bars + 20;  // [kW2FS]
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + Lay::OFF_MISC);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tslot + 1);
+    constexpr uint32_t kColY = 0, kColSt = 128;  // TMEM: Y (M=64) 128 columns | state N
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    if (tid == 0) {
+        for (int i = 0; i < kW2XS; ++i) {
+            mbar_init(&full_x[i], 1);
+            mbar_init(&empty_x[i], 2);
+            mbar_init(&xg_ready[i], 128);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&full_bc[i], 1);
+            mbar_init(&empty_bc[i], 2);
+        }
+        mbar_init(y_full, 1);
+        mbar_init(y_free, 128);
+        mbar_init(h_ready, 128);
+        mbar_init(h_free, 1);
+        mbar_init(s_full, 1);
+        mbar_init(s_free, 128);
+        for (int i = 0; i < kW2FS; ++i) {
+            mbar_init(&fac_full[i], 1);
+            mbar_init(&fac_empty[i], 128 + 128 + 128);  // scaling, epilogue, state
+        }
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(tslot, 256);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tslot;
+
+    if (warp == 0) {
+        // ------------------------------------------------ TMA producer
+        if (lane == 0) {
+            int gc = 0;
+            bool stop = false;
+            for (int it = blockIdx.x; it < nitems && !stop; it += gridDim.x) {
+                if (a.fb[it]) continue;
+                const Item I = item_of(it);
+                for (int c = 0; c < I.nchunks; ++c, ++gc) {
+                    const int tok = (int)(I.si.start + (long long)c * kQ);
+                    const int fs = gc % kW2FS;
+                    if (gc >= kW2FS &&
+                        !wait_or_abort(&fac_empty[fs], ((gc / kW2FS) - 1) & 1, abort_flag, a.hdr)) {
+                        stop = true;
+                        break;
+                    }
+                    mbar_expect_tx(&fac_full[fs], kFSlot);
+                    bulk_load(sm + Lay::OFF_F + fs * kFSlot,
+                              a.fac + ((long long)(I.seg * cps + c) * a.Hf + 2 * I.p) * kFacRec, kFSlot,
+                              &fac_full[fs]);
+                    const int xs = gc % kW2XS;
+                    if (gc >= kW2XS &&
+                        !wait_or_abort(&empty_x[xs], ((gc / kW2XS) - 1) & 1, abort_flag, a.hdr)) {
+                        stop = true;
+                        break;
+                    }
+                    unsigned char* sx = sm + Lay::OFF_X + xs * Lay::XSLOT;
+                    mbar_expect_tx(&full_x[xs], Lay::XSLOT);
+                    tma_load_3d(sx, &map_x, &full_x[xs], 0, I.h0, tok);
+                    tma_load_3d(sx + 8192, &map_x, &full_x[xs], 0, I.h1c, tok);
+                    const int b = gc & 1;
+                    if (gc >= 2 &&
+                        !wait_or_abort(&empty_bc[b], ((gc >> 1) - 1) & 1, abort_flag, a.hdr)) {
+                        stop = true;
+                        break;
+                    }
+                    unsigned char* st = sm + Lay::OFF_BC + b * Lay::BCSLOT;
+                    mbar_expect_tx(&full_bc[b], Lay::BCSLOT);
+                    tma_load_3d(st, &map_b, &full_bc[b], 0, I.g, tok);
+                    tma_load_3d(st + Lay::C_IN_BC, &map_c, &full_bc[b], 0, I.g, tok);
+                    bulk_load(st + Lay::L0_IN_BC,
+                              a.l0 + (((long long)I.seg * cps + c) * a.G + I.g) * 8192, 8192,
+                              &full_bc[b]);
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------ MMA issuer: G4 onto the state
+        if (lane == 0) {
+            const uint32_t id_s = idesc_bf16(128, N, 1, 1);
+            int gc = 0;
+            bool stop = false;
+            for (int it = blockIdx.x; it < nitems && !stop; it += gridDim.x) {
+                if (a.fb[it]) continue;
+                const Item I = item_of(it);
+                for (int c = 0; c < I.nchunks; ++c, ++gc) {
+                    const int b = gc & 1, bph = (gc >> 1) & 1;
+                    const int xsl = gc % kW2XS, xph = (gc / kW2XS) & 1;
+                    // one s_free and one s_full phase per chunk, also where no G4 is issued
+                    if (!wait_or_abort(&full_bc[b], bph, abort_flag, a.hdr) ||
+                        !wait_or_abort(&xg_ready[xsl], xph, abort_flag, a.hdr) ||
+                        !wait_or_abort(s_free, gc & 1, abort_flag, a.hdr)) {
+                        stop = true;
+                        break;
+                    }
+                    if (c < I.nchunks - 1) {
+                        tc_fence_after();
+                        const uint32_t xs = smem_u32(sm + Lay::OFF_X + xsl * Lay::XSLOT);
+                        const uint32_t bs = smem_u32(sm + Lay::OFF_BC + b * Lay::BCSLOT);
+#pragma unroll
+                        for (int k = 0; k < kQ / 16; ++k)
+                            mma_bf16(tmem + kColSt, sw128_desc(xs + k * 2048, 8192, 1024),
+                                     sw128_desc(bs + k * 2048, 8192, 1024), id_s, 1u);
+                    }
+                    mma_commit(s_full);
+                    mma_commit(&empty_x[xsl]);
+                    mma_commit(&empty_bc[b]);
+                }
+            }
+        }
+    } else if (warp == 10) {
+        // ------------------------------------------------ MMA issuer: G2, G3 into Y
+        if (lane == 0) {
+            const uint32_t id_y = idesc_bf16(64, 128, 0, 1);
+            const uint32_t id_h = idesc_bf16(64, 128, 0, 0);
+            int gc = 0;
+            bool stop = false;
+            for (int it = blockIdx.x; it < nitems && !stop; it += gridDim.x) {
+                if (a.fb[it]) continue;
+                const Item I = item_of(it);
+                for (int c = 0; c < I.nchunks; ++c, ++gc) {
+                    const int b = gc & 1, bph = (gc >> 1) & 1;
+                    const int xsl = gc % kW2XS, xph = (gc / kW2XS) & 1;
+                    if (!wait_or_abort(&full_bc[b], bph, abort_flag, a.hdr) ||
+                        !wait_or_abort(&xg_ready[xsl], xph, abort_flag, a.hdr) ||
+                        (gc >= 1 && !wait_or_abort(y_free, (gc - 1) & 1, abort_flag, a.hdr))) {
+                        stop = true;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t xs = smem_u32(sm + Lay::OFF_X + xsl * Lay::XSLOT);
+                    const uint32_t bs = smem_u32(sm + Lay::OFF_BC + b * Lay::BCSLOT);
+                    const uint32_t cs = bs + Lay::C_IN_BC;
+                    const uint32_t l0 = bs + Lay::L0_IN_BC;
+#pragma unroll
+                    for (int k = 0; k < kQ / 16; ++k)
+                        mma_bf16(tmem + kColY, sw128_desc(l0 + k * 32, 16, 1024),
+                                 sw128_desc(xs + k * 2048, 8192, 1024), id_y, k > 0 ? 1u : 0u);
+                    mma_commit(&empty_x[xsl]);
+                    if (!wait_or_abort(h_ready, gc & 1, abort_flag, a.hdr)) {
+                        stop = true;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t hs = smem_u32(sm + Lay::OFF_H);
+#pragma unroll
+                    for (int k = 0; k < N / 16; ++k)
+                        mma_bf16(tmem + kColY, sw128_desc(cs + k * 32, 16, 1024),
+                                 sw128_desc(hs + k * 32, 16, 1024), id_h, 1u);
+                    mma_commit(y_full);
+                    mma_commit(h_free);
+                    mma_commit(&empty_bc[b]);
+                }
+            }
+        }
+    } else if (warp >= 2 && warp < 10) {
+        const int ct = tid - 64;        // 0..255
+        const int wg = ct >> 7;
+        const int q = warp & 3;
+        const uint32_t trow = tmem + ((uint32_t)(32 * q) << 16);
+        if (wg == 0) {
+            // ------------------------------------------------ x -> g x, the y epilogue
+            const int tt = 16 * q + (lane & 15);
+            const int hf = lane >> 4;
+            const bool wide = (reinterpret_cast<uintptr_t>(a.y) & 31) == 0;
+            auto scale_x = [&](int gcs) {
+                const int xsl = gcs % kW2XS, xph = (gcs / kW2XS) & 1, fs = gcs % kW2FS;
+                bool ok = wait_or_abort(&fac_full[fs], (gcs / kW2FS) & 1, abort_flag, a.hdr);
+                ok = wait_or_abort(&full_x[xsl], xph, abort_flag, a.hdr) && ok;
+                if (ok) {
+                    uint4* xs = reinterpret_cast<uint4*>(sm + Lay::OFF_X + xsl * Lay::XSLOT);
+#pragma unroll
+                    for (int i0 = 0; i0 < 8; i0 += 4) {
+                        uint4 v[4];
+                        float gv[4];
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const int idx = ct + 128 * (i0 + i);  // head idx / 512, row (idx / 8) % 64
+                            v[i] = xs[idx];
+                            gv[i] = frec(fs, idx >> 9)[FAC_G + ((idx >> 3) & 63)];
+                        }
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) xs[ct + 128 * (i0 + i)] = scale_chunk(v[i], gv[i]);
+                    }
+                }
+                fence_proxy_async();
+                mbar_arrive(&xg_ready[xsl]);
+                mbar_arrive(&fac_empty[fs]);
+            };
+            struct YChunk {
+                long long tok0;
+                int vc, h0;
+                bool v1;
+            };
+            auto drain_y = [&](int gce, const YChunk& Y) {
+                const int sl = gce % kW2FS;
+                bool ok = wait_or_abort(&fac_full[sl], (gce / kW2FS) & 1, abort_flag, a.hdr);
+                ok = wait_or_abort(y_full, gce & 1, abort_flag, a.hdr) && ok;
+                tc_fence_after();
+                const float fv = frec(sl, hf)[FAC_F + tt];
+                mbar_arrive(&fac_empty[sl]);
+                uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.y) +
+                                                      ((Y.tok0 + tt) * a.H + Y.h0 + hf) * kP);
+#pragma unroll
+                for (int j = 0; j < 64; j += 32) {
+                    uint32_t v[32];
+                    tmem_ld16x2<64>(trow + kColY + j, &v[0]);
+                    tmem_ld16x2<64>(trow + kColY + j + 16, &v[16]);
+                    tmem_wait_ld_regs<32>(v);
+                    if (j == 32) {
+                        tc_fence_before();
+                        mbar_arrive(y_free);
+                    }
+                    if (ok && tt < Y.vc && (hf == 0 || Y.v1)) {
+                        store_bf16x16(dst + (j >> 3), v, fv, wide);
+                        store_bf16x16(dst + ((j + 16) >> 3), v + 16, fv, wide);
+                    }
+                }
+            };
+            int gc = 0;
+            YChunk prev = {0, 0, 0, false};
+            for (int it = blockIdx.x; it < nitems; it += gridDim.x) {
+                if (a.fb[it]) continue;
+                const Item I = item_of(it);
+                for (int c = 0; c < I.nchunks; ++c, ++gc) {
+                    scale_x(gc);
+                    if (gc >= 1) drain_y(gc - 1, prev);
+                    prev.tok0 = I.si.start + (long long)c * kQ;
+                    prev.vc = min(kQ, I.si.len - c * kQ);
+                    prev.h0 = I.h0;
+                    prev.v1 = I.v1;
+                }
+            }
+            if (gc >= 1) drain_y(gc - 1, prev);
+        } else {
+            // ------------------------------------------------ state chain
+            // as in the one-CTA walk: the state Hs_c stays in TMEM, G4 adds S_c onto it, and
+            // this group rewrites it as Hs_{c+1} = gamma (Hs_c + S_c) and stores bf16(Hs_{c+1}),
+            // the G3 operand (row r = (head, p), all N columns)
+            const int r = 32 * q + lane;
+            const int rh = r >> 6, rp = r & 63;
+            const uint32_t tcol = trow + kColSt;
+            auto write_h32 = [&](int c0, const float* h) {
+                unsigned char* hb = sm + Lay::OFF_H + r * 128;
+#pragma unroll
+                for (int c8 = 0; c8 < 32; c8 += 8) {
+                    const int n = c0 + c8;
+                    const uint4 v = make_uint4(pack_bf16(h[c8], h[c8 + 1]),
+                                               pack_bf16(h[c8 + 2], h[c8 + 3]),
+                                               pack_bf16(h[c8 + 4], h[c8 + 5]),
+                                               pack_bf16(h[c8 + 6], h[c8 + 7]));
+                    *reinterpret_cast<uint4*>(hb + ((((n >> 3) ^ r) & 7) << 4)) = v;
+                }
+            };
+            int gc = 0;
+            for (int it = blockIdx.x; it < nitems; it += gridDim.x) {
+                if (a.fb[it]) continue;
+                const Item I = item_of(it);
+                {
+                    // the item's first chunk: state entering the segment; the G3 operand
+                    // buffer was last read by G3 of global chunk gc - 1
+                    wait_or_abort(&fac_full[gc % kW2FS], (gc / kW2FS) & 1, abort_flag, a.hdr);
+                    if (gc >= 1) wait_or_abort(h_free, (gc - 1) & 1, abort_flag, a.hdr);
+                    const float sc0 = (rh == 0 || I.v1) ? expf(-frec(gc % kW2FS, rh)[FAC_HALF]) : 0.f;
+                    const float* Hin =
+                        a.A + ((long long)I.seg * a.H + I.h0 + (I.v1 ? rh : 0)) * kP * N +
+                        lm_row(rp, N);
+#pragma unroll
+                    for (int c0 = 0; c0 < N; c0 += 32) {
+                        float h[32];
+#pragma unroll
+                        for (int i = 0; i < 32; i += 4) {
+                            const float4 v = *reinterpret_cast<const float4*>(Hin + (c0 + i) * 32);
+                            h[i] = v.x * sc0;
+                            h[i + 1] = v.y * sc0;
+                            h[i + 2] = v.z * sc0;
+                            h[i + 3] = v.w * sc0;
+                        }
+                        tmem_st16(tcol + c0, reinterpret_cast<const uint32_t*>(&h[0]));
+                        tmem_st16(tcol + c0 + 16, reinterpret_cast<const uint32_t*>(&h[16]));
+                        write_h32(c0, h);
+                    }
+                    tmem_wait_st();
+                    tc_fence_before();
+                    mbar_arrive(s_free);
+                    fence_proxy_async();
+                    mbar_arrive(h_ready);
+                }
+                for (int c = 0; c + 1 < I.nchunks; ++c, ++gc) {
+                    const int sl = gc % kW2FS, sn = (gc + 1) % kW2FS;
+                    bool ok = wait_or_abort(&fac_full[sn], ((gc + 1) / kW2FS) & 1, abort_flag, a.hdr);
+                    const float gam = expf(-(frec(sl, rh)[FAC_HALF] + frec(sn, rh)[FAC_HALF]));
+                    // the G3 operand buffer is rewritten once G3 of this chunk has read it
+                    wait_or_abort(h_free, gc & 1, abort_flag, a.hdr);
+                    ok = wait_or_abort(s_full, gc & 1, abort_flag, a.hdr) && ok;
+                    tc_fence_after();
+#pragma unroll
+                    for (int c0 = 0; c0 < N; c0 += 32) {
+                        uint32_t v[32];
+                        tmem_ld16(tcol + c0, *reinterpret_cast<uint32_t(*)[16]>(&v[0]));
+                        tmem_ld16(tcol + c0 + 16, *reinterpret_cast<uint32_t(*)[16]>(&v[16]));
+                        tmem_wait_ld_regs<32>(v);
+                        float h[32];
+#pragma unroll
+                        for (int u = 0; u < 32; ++u) h[u] = ok ? gam * __uint_as_float(v[u]) : 0.f;
+                        tmem_st16(tcol + c0, reinterpret_cast<const uint32_t*>(&h[0]));
+                        tmem_st16(tcol + c0 + 16, reinterpret_cast<const uint32_t*>(&h[16]));
+                        write_h32(c0, h);
+                    }
+                    tmem_wait_st();
+                    tc_fence_before();
+                    mbar_arrive(s_free);
+                    mbar_arrive(&fac_empty[sl]);
+                    fence_proxy_async();
+                    mbar_arrive(h_ready);
+                }
+                // the item's last chunk: no update, but its s_full phase is consumed
+                wait_or_abort(s_full, gc & 1, abort_flag, a.hdr);
+                mbar_arrive(&fac_empty[gc % kW2FS]);
+                ++gc;
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) tmem_dealloc(tmem, 256);
+}
+
 // The forward walk of the items (segment, pair of heads) whose chunk decays leave the
 // factorisation's range (tc_fwd_walk skips them): the SIMT recurrence, a persistent grid
 // over the items; it exits at once when there are none.
@@ -2133,13 +2545,23 @@ cudaError_t forward_n(const Prob& pb, const Args& a, Launch& L) {
     if (e != cudaSuccess) return e;
     e = launch_state_scan(pb, a, L, a.final_state != nullptr);
     if (e != cudaSuccess) return e;
-    e = set_smem(tc_fwd_walk_kernel<N>, WalkLayout<N>::TOTAL);
-    if (e != cudaSuccess) return e;
-    // persistent: one CTA per SM, each walking items (segment, pair of heads)
     const long long items = pb.nseg_max * a.npairs;
-    const dim3 pgrid((unsigned)(items < sm_count() ? items : sm_count()));
-    L.begin("tc_fwd_walk");
-    tc_fwd_walk_kernel<N><<<pgrid, kWalkThreads, WalkLayout<N>::TOTAL, L.stream>>>(mx, mb, mc, a);
+    if constexpr (N == 64) {
+        // persistent: two CTAs per SM, each walking items (segment, pair of heads)
+        e = set_smem(tc_fwd_walk2_kernel, Walk2Layout::TOTAL);
+        if (e != cudaSuccess) return e;
+        const long long ctas = 2LL * sm_count();
+        const dim3 pgrid((unsigned)(items < ctas ? items : ctas));
+        L.begin("tc_fwd_walk");
+        tc_fwd_walk2_kernel<<<pgrid, kWalk2Threads, Walk2Layout::TOTAL, L.stream>>>(mx, mb, mc, a);
+    } else {
+        // persistent: one CTA per SM, each walking items (segment, pair of heads)
+        e = set_smem(tc_fwd_walk_kernel<N>, WalkLayout<N>::TOTAL);
+        if (e != cudaSuccess) return e;
+        const dim3 pgrid((unsigned)(items < sm_count() ? items : sm_count()));
+        L.begin("tc_fwd_walk");
+        tc_fwd_walk_kernel<N><<<pgrid, kWalkThreads, WalkLayout<N>::TOTAL, L.stream>>>(mx, mb, mc, a);
+    }
     if ((e = L.end()) != cudaSuccess) return e;
     constexpr int fsmem = sizeof(float) * simt::walk_smem_floats(kP, N);
     L.begin("tc_fallback_walk");
