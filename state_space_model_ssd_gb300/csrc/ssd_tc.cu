@@ -436,19 +436,23 @@ constexpr int l0_smem_bytes() {
 // m = s_end / 2, and f(t) = exp(s_t - m) (zero past the chunk's tokens), g(t) = delta_t
 // exp(m - s_t), half = -m.  With them exp(s_t - s_s) = f(t) g(s) / delta_s keeps every
 // exponent within |s_end| / 2.  The walks of both passes copy these records instead of
-// recomputing them.  One CTA per chunk slot and group of kFacHeads heads: the raw_dt
-// tile (64 tokens x kFacHeads heads) is read with coalesced loads into shared memory,
-// then one warp scans one head's 64 tokens, two per lane.
+// recomputing them.  One CTA per kFacChunks chunk slots of a segment and group of
+// kFacHeads heads: the raw_dt tiles (64 tokens x kFacHeads heads each) are read with
+// coalesced loads into shared memory, then one warp scans one (chunk, head)'s 64 tokens,
+// two per lane.
 constexpr int kFacThreads = 256;
 constexpr int kFacHeads = 16;
+constexpr int kFacChunks = 4;  // chunks of one segment a CTA takes, all loads in flight at once
 
 __global__ void __launch_bounds__(kFacThreads) tc_factors_kernel(Args a) {
     const int cps = a.Ls / kQ;
-    const int seg = blockIdx.x / cps, c = blockIdx.x % cps;
+    const int groups = (cps + kFacChunks - 1) / kFacChunks;
+    const int seg = blockIdx.x / groups, c0 = (blockIdx.x % groups) * kFacChunks;
     if (seg >= a.hdr->nseg) return;
     const SegInfo si = a.segtab[seg];
-    if (c >= (si.len + kQ - 1) / kQ) return;
-    __shared__ float zt[kFacHeads][kQ + 1];  // raw_dt + delta_init, [record slot][token]
+    const int nch = (si.len + kQ - 1) / kQ;
+    if (c0 >= nch) return;
+    __shared__ float zt[kFacChunks][kFacHeads][kQ + 1];  // raw_dt + delta_init
     const int ct = threadIdx.x, lane = ct & 31, warp = ct >> 5;
     // record slots hb .. hb + kFacHeads - 1: slot r is lane r % 2 of pair r / 2 (a dummy
     // slot gets an all-zero record)
@@ -457,22 +461,35 @@ __global__ void __launch_bounds__(kFacThreads) tc_factors_kernel(Args a) {
         const HeadPair hp = head_pair(a, r >> 1);
         return ((r & 1) == 0 || hp.v1) ? hp.h0 + (r & 1) : -1;
     };
-    const int vc = min(kQ, si.len - c * kQ);
-    const long long tok0 = si.start + (long long)c * kQ;
+    int hcol[kQ * kFacHeads / kFacThreads];  // the head each of this thread's loads reads
 #pragma unroll
     for (int k = 0; k < kQ * kFacHeads / kFacThreads; ++k) {
-        const int idx = ct + kFacThreads * k, t = idx / kFacHeads, hh = idx % kFacHeads;
-        float z = 0.f;
-        const int h = (hb + hh < a.Hf) ? head_of(hb + hh) : -1;
-        if (t < vc && h >= 0) z = a.raw[(tok0 + t) * a.H + h] + a.delta_init;
-        zt[hh][t] = z;
+        const int hh = (ct + kFacThreads * k) % kFacHeads;
+        hcol[k] = (hb + hh < a.Hf) ? head_of(hb + hh) : -1;
+    }
+#pragma unroll
+    for (int cc = 0; cc < kFacChunks; ++cc) {
+        const int c = c0 + cc;
+        const int vc = c < nch ? min(kQ, si.len - c * kQ) : 0;
+        const long long tok0 = si.start + (long long)c * kQ;
+#pragma unroll
+        for (int k = 0; k < kQ * kFacHeads / kFacThreads; ++k) {
+            const int idx = ct + kFacThreads * k, t = idx / kFacHeads, hh = idx % kFacHeads;
+            float z = 0.f;
+            if (t < vc && hcol[k] >= 0) z = a.raw[(tok0 + t) * a.H + hcol[k]] + a.delta_init;
+            zt[cc][hh][t] = z;
+        }
     }
     __syncthreads();
-    for (int hh = warp; hh < kFacHeads && hb + hh < a.Hf; hh += kFacThreads / 32) {
-        const int r = hb + hh, t0 = 2 * lane;
+    // one warp scans one (chunk, head) record's 64 tokens, two per lane
+    for (int w = warp; w < kFacChunks * kFacHeads; w += kFacThreads / 32) {
+        const int cc = w / kFacHeads, hh = w % kFacHeads;
+        const int c = c0 + cc, r = hb + hh;
+        if (c >= nch || r >= a.Hf) continue;
+        const int vc = min(kQ, si.len - c * kQ), t0 = 2 * lane;
         const bool real = head_of(r) >= 0;
-        const float d0 = (real && t0 < vc) ? softplus_f(zt[hh][t0]) : 0.f;
-        const float d1 = (real && t0 + 1 < vc) ? softplus_f(zt[hh][t0 + 1]) : 0.f;
+        const float d0 = (real && t0 < vc) ? softplus_f(zt[cc][hh][t0]) : 0.f;
+        const float d1 = (real && t0 + 1 < vc) ? softplus_f(zt[cc][hh][t0 + 1]) : 0.f;
         const float incl = warp_scan(d0 + d1, lane);
         float excl = __shfl_up_sync(0xffffffffu, incl, 1);
         if (lane == 0) excl = 0.f;
@@ -2520,7 +2537,8 @@ cudaError_t launch_l0(const Prob& pb, const Args& a, Launch& L, const CUtensorMa
 }
 
 cudaError_t launch_factors(const Prob& pb, const Args& a, Launch& L) {
-    const dim3 grid((unsigned)(pb.nseg_max * (pb.Ls / kQ)), (a.Hf + kFacHeads - 1) / kFacHeads);
+    const int groups = (pb.Ls / kQ + kFacChunks - 1) / kFacChunks;
+    const dim3 grid((unsigned)(pb.nseg_max * groups), (a.Hf + kFacHeads - 1) / kFacHeads);
     L.begin("tc_factors");
     tc_factors_kernel<<<grid, kFacThreads, 0, L.stream>>>(a);
     return L.end();
