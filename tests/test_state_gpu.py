@@ -135,13 +135,15 @@ def test_many_segments_blocked_scans(ssd, oracle_mod, monkeypatch, dtype, P, N, 
     _check_all(ssd, oracle_mod, d, dtype, -4.6)
 
 
+@pytest.mark.parametrize("N", [64, 128])
 @pytest.mark.parametrize("k", [33, 64])
-def test_bf16_long_segments(ssd, oracle_mod, monkeypatch, k):
+def test_bf16_long_segments(ssd, oracle_mod, monkeypatch, k, N):
     """Segments of 33 and 64 chunks (the longest the aggregate kernels take) on the
-    tensor-core path, a ragged last segment, head 0 at delta ~ 8 (its head pair takes the
-    SIMT recurrence), with initial state and final-state gradient."""
+    tensor-core path (at N = 64 the two-CTA-per-SM forward walk), a ragged last segment,
+    head 0 at delta ~ 8 (its head pair takes the SIMT recurrence), with initial state and
+    final-state gradient."""
     monkeypatch.setenv("SSD_SEGMENT_CHUNKS", str(k))
-    d = _draw(37, 9000, 4, 64, 128, "bf16")
+    d = _draw(37, 9000, 4, 64, N, "bf16")
     d["raw_dt"][:, :, 0] += np.float32(12.6)
     _check_all(ssd, oracle_mod, d, "bf16", -4.6)
 
