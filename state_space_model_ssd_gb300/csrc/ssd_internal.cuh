@@ -157,12 +157,21 @@ struct Launch {
 // SIMT path (any supported shape, f32 or bf16).
 cudaError_t simt_forward(const Prob& pb, const Args& a, Launch& L);
 cudaError_t simt_backward(const Prob& pb, const Args& a, Launch& L);
-// Tensor-core path (bf16, P = 64, N in {64, 128}, Q = 64, an even number of heads per group).
+// Tensor-core path (bf16, P = 64, N in {64, 128}, Q = 64, any number of heads per group).
 cudaError_t tc_forward(const Prob& pb, const Args& a, Launch& L);
 // reuse_forward: the workspace holds the forward's segment table, C B^T tiles, chunk
 // factors and segment states for these inputs (checked on the device).
 cudaError_t tc_backward(const Prob& pb, const Args& a, Launch& L, bool reuse_forward = false);
 bool tc_supported(int dtype, int P, int N, int Q, int H, int G);
+
+// SMs of the current device (persistent grids size themselves by it).
+inline int sm_count() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1)
+        return 1;
+    return n;
+}
 
 // One decode step for pb.nseq sequences (the batch rows).
 cudaError_t launch_decode_step(const Prob& pb, const float* hin, float* hout, const void* x,

@@ -2509,15 +2509,6 @@ constexpr int state_smem_bytes(int N) {
 // three CTAs of the aggregate kernel per SM (1 KB per CTA reserved by the system)
 static_assert(3 * (state_smem_bytes(128) + 1024) <= 233472, "aggregate kernel occupancy");
 
-// SMs of the current device (persistent grids take one CTA per SM).
-int sm_count() {
-    int dev = 0, n = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1)
-        return 1;
-    return n;
-}
-
 template <typename K>
 cudaError_t set_smem(K kernel, int bytes) {
     return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
