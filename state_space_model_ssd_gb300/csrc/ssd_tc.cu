@@ -105,8 +105,9 @@ __global__ void __launch_bounds__(kStateThreads, 3)
             dc4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
         }
     }
-    const int seg = blockIdx.x;
-    const int pr = blockIdx.y;
+    // pairs fastest: the CTAs that run together read whole token rows of x (and dy)
+    const int seg = blockIdx.x / a.npairs;
+    const int pr = blockIdx.x % a.npairs;
     const HeadPair hp = head_pair(a, pr);
     const int h0 = hp.h0;
     if (seg >= a.hdr->nseg) return;
@@ -1582,8 +1583,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                      const __grid_constant__ CUtensorMap map_c,
                      const __grid_constant__ CUtensorMap map_acc, Args a) {
     using Lay = BwdLayout<N>;
-    const int seg = blockIdx.x;
-    const int pr = blockIdx.y;
+    // pairs fastest: the CTAs that run together read whole token rows of x (and dy)
+    const int seg = blockIdx.x / a.npairs;
+    const int pr = blockIdx.x % a.npairs;
     const HeadPair hp = head_pair(a, pr);
     const int h0 = hp.h0;
     if (seg >= a.hdr->nseg) return;
@@ -2007,8 +2009,9 @@ __global__ void __launch_bounds__(kDxThreads, 1)
                        const __grid_constant__ CUtensorMap map_c,
                        const __grid_constant__ CUtensorMap map_acc, Args a) {
     using Lay = DxLayout<N>;
-    const int seg = blockIdx.x;
-    const int pr = blockIdx.y;
+    // pairs fastest: the CTAs that run together read whole token rows of x (and dy)
+    const int seg = blockIdx.x / a.npairs;
+    const int pr = blockIdx.x % a.npairs;
     const HeadPair hpr = head_pair(a, pr);
     const int h0 = hpr.h0;
     if (seg >= a.hdr->nseg) return;
@@ -2545,7 +2548,7 @@ cudaError_t forward_n(const Prob& pb, const Args& a, Launch& L) {
     if (e != cudaSuccess) return e;
     if ((e = launch_l0<N>(pb, a, L, mb, mc)) != cudaSuccess) return e;
     if ((e = launch_factors(pb, a, L)) != cudaSuccess) return e;
-    const dim3 grid((unsigned)pb.nseg_max, a.npairs);
+    const dim3 grid((unsigned)(pb.nseg_max * a.npairs));
     e = set_smem(tc_seg_state_kernel<N, 0>, state_smem_bytes(N));
     if (e != cudaSuccess) return e;
     L.begin("tc_fwd_state");
@@ -2585,7 +2588,7 @@ cudaError_t backward_n(const Prob& pb, const Args& a, Launch& L, bool reuse_forw
         !make_map(&mb, a.B, pb.T, pb.G, N) || !make_map(&mc, a.C, pb.T, pb.G, N) ||
         !make_map_f32(&mdb, a.dbacc, pb.T, pb.G, N) || !make_map_f32(&mdc, a.dcacc, pb.T, pb.G, N))
         return cudaErrorInvalidValue;
-    const dim3 grid((unsigned)pb.nseg_max, a.npairs);
+    const dim3 grid((unsigned)(pb.nseg_max * a.npairs));
     cudaError_t e;
     if (reuse_forward) {
         // the forward's segment table, tiles, factors and segment states are in the
