@@ -4,7 +4,12 @@
 #include <stdlib.h>
 #include <string.h>
 
+#include <functional>
+#include <map>
+#include <mutex>
+#include <queue>
 #include <string>
+#include <tuple>
 #include <vector>
 
 #include "ssd_internal.cuh"
@@ -78,14 +83,7 @@ bool is_pow2_in(int v, int lo, int hi) {
 // of tokens, where every segment boundary costs a materialised state read and
 // written by each pass (64 x 64 x 4 bytes per head at N = 64 against 4096 tokens
 // of x at 64 chunks).
-int choose_segment_length(long long T, int nseq, int H, int Q) {
-    // SSD_SEGMENT_CHUNKS (1..64) fixes the number of chunks per segment; the
-    // result does not depend on it (tests use it to cover multi-chunk segments
-    // at small sizes).
-    if (const char* env = getenv("SSD_SEGMENT_CHUNKS")) {
-        const int k = atoi(env);
-        if (k >= 1 && k <= 64) return k * Q;
-    }
+int default_segment_chunks(long long T, int nseq, int H, int Q) {
     const long long target_units = 8LL * 152;
     const long long chunks = (T + Q - 1) / Q;
     const long long extra = nseq > 1 ? nseq : 0;
@@ -93,7 +91,76 @@ int choose_segment_length(long long T, int nseq, int H, int Q) {
     while (k > 1 && (chunks / k + extra) * H < target_units) k >>= 1;
     if (k == 16)
         while (k < 64 && (chunks / (2 * k) + extra) * H >= 4 * target_units) k <<= 1;
-    return k * Q;
+    return k;
+}
+
+// Finishing time, in half-chunk steps, of a walk that runs one CTA per SM over the
+// (segment, head pair) items of `rows` dense rows in launch order (the segments of each
+// row in turn, head pairs fastest).  An item takes its chunk count plus a fixed start-up
+// cost of about 2.5 chunks (state load, first tiles in flight, state store: measured on
+// the backward walks) and goes to whichever of the `sms` SMs frees first.
+long long walk_makespan(long long row_chunks, long long rows, int k, int npairs, int sms) {
+    std::priority_queue<long long, std::vector<long long>, std::greater<long long>> free_at;
+    for (int i = 0; i < sms; ++i) free_at.push(0);
+    long long end = 0;
+    const long long nseg = (row_chunks + k - 1) / k;
+    for (long long r = 0; r < rows; ++r)
+        for (long long s = 0; s < nseg; ++s) {
+            const long long ch = s + 1 < nseg ? k : row_chunks - s * k;
+            for (int p = 0; p < npairs; ++p) {
+                const long long t = free_at.top() + 2 * ch + 5;
+                free_at.pop();
+                free_at.push(t);
+                if (t > end) end = t;
+            }
+        }
+    return end;
+}
+
+// Tensor-core path on dense rows, where the default rule gives 16 chunks: the walks
+// are one CTA per SM over a few waves of work items, so the last wave's fill decides
+// their time.  Of 8 to 64 chunks, the segment length with the shortest estimated
+// walk (walk_makespan) wins, the longest of those within 1% of it (fewer segment
+// boundaries).  Cached per shape.
+int balanced_segment_chunks(long long row_chunks, long long rows, int npairs, int sms) {
+    static std::mutex mu;
+    static std::map<std::tuple<long long, long long, int, int>, int> cache;
+    const auto key = std::make_tuple(row_chunks, rows, npairs, sms);
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        auto it = cache.find(key);
+        if (it != cache.end()) return it->second;
+    }
+    long long span[65] = {0};
+    long long best = -1;
+    for (int k = 8; k <= 64; ++k) {
+        span[k] = walk_makespan(row_chunks, rows, k, npairs, sms);
+        if (best < 0 || span[k] < best) best = span[k];
+    }
+    int pick = 16;
+    for (int k = 8; k <= 64; ++k)
+        if (span[k] * 100 <= best * 101) pick = k;
+    std::lock_guard<std::mutex> lock(mu);
+    cache[key] = pick;
+    return pick;
+}
+
+int choose_segment_length(const Prob& b) {
+    // SSD_SEGMENT_CHUNKS (1..64) fixes the number of chunks per segment; the
+    // result does not depend on it (tests use it to cover multi-chunk segments
+    // at small sizes).
+    if (const char* env = getenv("SSD_SEGMENT_CHUNKS")) {
+        const int k = atoi(env);
+        if (k >= 1 && k <= 64) return k * b.Q;
+    }
+    const int k = default_segment_chunks(b.T, b.nseq, b.H, b.Q);
+    if (k != 16 || !b.tc || b.varlen) return k * b.Q;
+    const int sms = sm_count();
+    const long long row_chunks = (b.rowlen + b.Q - 1) / b.Q;
+    const int npairs = b.G * ((b.H / b.G + 1) / 2);
+    // no device to size for, or a simulation too long to run on the host
+    if (sms < 8 || row_chunks * b.nseq * npairs > (1LL << 20)) return k * b.Q;
+    return balanced_segment_chunks(row_chunks, b.nseq, npairs, sms) * b.Q;
 }
 
 ssd_status_t make_prob(const ssd_problem_t* p, Prob* out) {
@@ -127,7 +194,7 @@ ssd_status_t make_prob(const ssd_problem_t* p, Prob* out) {
     // heads' terms cancel (bf16 operands would leave their rounding in the small sum).
     b.tc = T >= p->chunk_size &&
            tc_supported(p->dtype, p->headdim, p->dstate, p->chunk_size, p->nheads, p->ngroups);
-    b.Ls = choose_segment_length(T, b.nseq, b.H, b.Q);
+    b.Ls = choose_segment_length(b);
     // every sequence (dense row) may end in a partial segment
     b.nseg_max = (T + b.Ls - 1) / b.Ls + b.nseq;
     if (b.nseg_max < 1) b.nseg_max = 1;
