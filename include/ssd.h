@@ -78,13 +78,15 @@ typedef struct {
 
 /* Supported shapes: P in {8,16,32,64,128}; N in {8,16,32,64,128};
  * chunk_size in {16,32,64,128,256}; T <= 2^31 - 1; G divides H.
- * bf16 problems with P = 64, N in {64,128}, chunk_size = 64, an even number of heads
- * per group and at least chunk_size tokens in all run on the tensor-core path; every
+ * bf16 problems with P = 64, N in {64,128}, chunk_size = 64 and at least chunk_size
+ * tokens in all run on the tensor-core path (any number of heads per group); every
  * other supported problem runs on the SIMT path. */
 
 /* Bytes of device workspace that ssd_forward (for_backward = 0) or
- * ssd_backward (for_backward = 1) needs for `prob`.  Pure host function.
- * Returns SSD_ERR_INVALID_ARG / SSD_ERR_UNSUPPORTED for a bad problem. */
+ * ssd_backward (for_backward = 1) needs for `prob`.  Host function, no launch; on the
+ * tensor-core path with dense rows the segment length, and with it the size, follows
+ * the current device's SM count, so query it with the device current that will run
+ * the calls.  Returns SSD_ERR_INVALID_ARG / SSD_ERR_UNSUPPORTED for a bad problem. */
 ssd_status_t ssd_workspace_size(const ssd_problem_t* prob, int for_backward, size_t* bytes);
 
 /* Forward scan.  Reads x, raw_dt, B, C (and cu_seqlens when prob->nseq > 0,
